@@ -1,0 +1,244 @@
+/*
+ * libmoe: the expert-streaming MoE layer on one NVIDIA GB300 (sm_103a).
+ *
+ * One MoE layer of expert-streaming inference: an 8-bit router with top-k and
+ * renormalised gates, a per-layer expert cache whose slots live in HBM and
+ * whose misses are streamed from pinned host memory, int4-affine expert FFNs,
+ * an always-resident shared expert and the gate-weighted combine.
+ *
+ * Pages cited (by title and section):
+ *   [P1] "在 Rockchip NPU 上实现 turbo-fieldfare 风格 MoE 大模型流式推理的技术方案"
+ *   [P3] "BigMoeOnEdge：端侧 MoE 专家流式推理原理与实测"
+ *
+ * Conventions for every call:
+ *   - Return value: a moe_status. No call throws or aborts. On failure the
+ *     outputs are unspecified and moe_last_error() (thread-local) describes
+ *     the cause. CUDA errors map to MOE_ECUDA.
+ *   - Pointers marked "device" must be device memory of the layer's device;
+ *     pointers marked "host" are ordinary host memory (pageable is fine).
+ *     The caller owns every pointer it passes; the library never frees them
+ *     and keeps none beyond the call, except where a call says otherwise.
+ *   - stream: a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream). Device work is enqueued on it; calls that must read device
+ *     results on the host (moe_forward) synchronise internally on events.
+ *   - One host thread at a time per moe_layer. Different layers may be used
+ *     from different threads.
+ *   - Numeric formats: bf16 = bfloat16 bit patterns, f16 = IEEE binary16 bit
+ *     patterns, both as uint16_t.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_EINVAL = 1,   /* bad argument: shape, pointer, id out of range */
+    MOE_ENOMEM = 2,   /* device or pinned host allocation failed */
+    MOE_ECUDA = 3,    /* a CUDA runtime call failed */
+    MOE_ECOPY = 4,    /* a miss copy failed; the slot is left empty */
+    MOE_ETIMEOUT = 5, /* a bounded device wait expired */
+    MOE_ESTATE = 6    /* call out of order (e.g. forward before set_weights) */
+} moe_status;
+
+typedef struct moe_ctx moe_ctx;
+typedef struct moe_layer moe_layer;
+typedef struct moe_host_cache moe_host_cache;
+
+/* Layer shapes. d_model, d_ff and d_ff_shared are multiples of 64 (the
+ * quantisation group) and of 32; n_experts <= 1024; 1 <= top_k <= min(32,
+ * n_experts); d_model <= 8192. act: 0 = GELU (tanh form), 1 = SiLU. */
+typedef struct {
+    int32_t d_model, n_experts, top_k, d_ff, d_ff_shared, act;
+} moe_shapes;
+
+/* Quantisation layout. Only {4, 64, 8, 64} is accepted: experts are 4-bit
+ * affine in groups of 64 along the input dimension, the router 8-bit affine
+ * in groups of 64 ([P1] §2.1 table, §2.5 "量化方案"). */
+typedef struct {
+    int32_t w_bits, w_group, r_bits, r_group;
+} moe_quant_layout;
+
+/* One quantised matrix W[N][K] in the canonical layout (host memory):
+ *   codes: row-major; 4-bit: K/2 bytes per row, element 2j in the low nibble
+ *          of byte j and 2j+1 in the high nibble, unsigned 0..15;
+ *          8-bit: K bytes per row, unsigned 0..255;
+ *   scale, bias: f16 [N][K/64];  w[n][k] = scale[n][k/64] * q + bias[n][k/64]. */
+typedef struct {
+    const uint8_t* codes;
+    const uint16_t* scale;
+    const uint16_t* bias;
+} moe_qmatrix;
+
+/* All weights of one layer, canonical layout, host memory. Routed experts are
+ * stacked on a leading expert axis (expert-major, [P3] "从实际路由找到 GGUF 权重切片":
+ * slice = base + expert_id * stride):
+ *   gate, up:  codes [E][d_ff][d_model/2],  scale/bias [E][d_ff][d_model/64]
+ *   down:      codes [E][d_model][d_ff/2],  scale/bias [E][d_model][d_ff/64]
+ *   shared_gate/up: [d_ff_shared][d_model], shared_down: [d_model][d_ff_shared]
+ *   router:    codes [E][d_model] (8-bit), scale/bias [E][d_model/64] */
+typedef struct {
+    moe_qmatrix router;
+    moe_qmatrix shared_gate, shared_up, shared_down;
+    moe_qmatrix gate, up, down;
+} moe_host_weights;
+
+/* Cumulative counters of one layer since creation (or the last reset).
+ * Lookups count distinct experts per cache step; bypasses are misses that
+ * found no unpinned slot ([P3] "缓存管理的是专家工作集": the budget may be
+ * exceeded temporarily) and are included in misses. exposed_copy_us is the
+ * time the compute stream spent waiting for miss copies ([P3]
+ * "读取完成后，算子才可以使用切片": overlap hides only part of the reads). */
+typedef struct {
+    uint64_t steps, hits, misses, bypass;
+    uint64_t bytes_h2d;      /* bytes copied host -> device for misses */
+    uint64_t bytes_resident; /* weight bytes the layer's kernels read from HBM */
+    double exposed_copy_us;
+} moe_stats;
+
+/* ---- context ------------------------------------------------------------ */
+
+/* Create a context on CUDA device `device` (made current on the calling
+ * thread). Owns a copy stream and the transient staging arena shared by its
+ * layers. Errors: MOE_EINVAL (no such device), MOE_ECUDA. */
+moe_status moe_ctx_create(int device, moe_ctx** out);
+void moe_ctx_destroy(moe_ctx* ctx); /* after all its layers are destroyed */
+
+/* ---- layer -------------------------------------------------------------- */
+
+/* Create one MoE layer with `cache_slots` HBM expert slots and a replacement
+ * policy (0 = LFU, [P1] §6.2.2-§6.2.3 and §8.3; 1 = LRU, [P3]
+ * "缓存管理的是专家工作集"). Allocates: router, shared expert and slot arena in
+ * device memory; the routed-expert pool (all experts) in pinned host memory.
+ * Nothing is loaded until moe_layer_set_weights.
+ * Errors: MOE_EINVAL (shapes, layout, slots < 1 or > n_experts, policy),
+ * MOE_ENOMEM (allocation failed; nothing is leaked). */
+moe_status moe_layer_create(moe_ctx* ctx, const moe_shapes* shapes, const moe_quant_layout* layout,
+                            int32_t cache_slots, int32_t policy, moe_layer** out);
+
+/* Load weights from canonical host arrays (read during the call only). The
+ * router and shared expert are repacked and copied to HBM; the routed experts
+ * are repacked into the library's pinned host pool, one contiguous blob per
+ * expert at base + e * expert_bytes ([P1] §9.2 item 2: one region per layer,
+ * [offset, size] per expert). Resets the cache to empty.
+ * Blocking. Errors: MOE_EINVAL (NULL pointer), MOE_ECUDA. */
+moe_status moe_layer_set_weights(moe_layer* layer, const moe_host_weights* w);
+
+/* Bytes of one routed expert in the library's blob (gate + up + down codes,
+ * scales and biases); equals the canonical byte count. */
+size_t moe_expert_bytes(const moe_shapes* shapes);
+
+/* Router, top-k and gates ([P3] "每个 token、每层都要重新路由"; [P1] §2.4 cb1):
+ *   logit[t][e] = sum_i x[t][i] * (scale * q + bias)[e][i] + zbias[e]  (fp32)
+ *   ids[t][0..k)  = the k largest logits, descending, ties -> lower expert id
+ *   gates[t][r]   = softmax over the k chosen logits (= the full softmax
+ *                   renormalised over them).
+ * The fp32 sum runs in a fixed order (runs of 16 inputs dealt round-robin to
+ * 32 lanes, each lane sequential with fused multiply-adds, lanes combined by a
+ * butterfly at distances 16, 8, 4, 2, 1), so ids are reproducible bit for bit.
+ * x: device bf16 [T][d_model]; zbias: device f32 [E] or NULL; ids: device
+ * int32 [T][k]; gates: device f32 [T][k]. T >= 1. Asynchronous on `stream`.
+ * Errors: MOE_EINVAL, MOE_ESTATE (no weights), MOE_ECUDA. */
+moe_status moe_route(moe_layer* layer, const void* x_bf16, int32_t T, const float* zbias, int32_t* ids,
+                     float* gates, void* stream);
+
+/* One expert-cache step over n_ids expert ids (host int32, duplicates
+ * allowed): LFU/LRU lookup ([P1] §8.3 flow) in which distinct ids are taken
+ * in ascending order; hits are counted (LFU: use_count += 1; LRU: stamped
+ * with the step index) and their slots pinned for the step; each miss takes
+ * the lowest empty slot, else the unpinned slot with the smallest count (LRU:
+ * oldest stamp), ties to the lowest slot index, and starts at count 1; a miss
+ * that finds no unpinned slot bypasses the cache (slot -1).
+ * For every miss that got a slot, the library enqueues the copy of that
+ * expert from its pinned pool into the slot on its copy stream, ordered after
+ * the layer's previous kernels; the slot's ready event is recorded after the
+ * copy ([P3] "读取完成后，算子才可以使用切片").
+ * Outputs (host): slot_of[n_ids] = slot holding ids[i] after the step or -1;
+ * miss_experts[n_miss] and miss_slots[n_miss] in ascending expert order
+ * (capacity n_ids each); *n_miss. Any output pointer may be NULL.
+ * Errors: MOE_EINVAL (id out of range), MOE_ESTATE, MOE_ECOPY, MOE_ECUDA. */
+moe_status moe_cache_step(moe_layer* layer, const int32_t* ids, int32_t n_ids, int32_t* slot_of,
+                          int32_t* miss_experts, int32_t* miss_slots, int32_t* n_miss);
+
+/* The whole layer on T tokens ([P1] §2.4 cb1 -> io -> cb2, §8.2):
+ *   route -> (host) cache step + miss copies on the copy stream, while the
+ *   shared expert runs on `stream` -> routed expert FFNs (hits first, misses
+ *   after their ready events) -> y[t] = shared(x_t) + sum_{r<k} gate[t][r] *
+ *   FFN_{ids[t][r]}(x_t), the routed terms added in rank order.
+ *   FFN_e(x) = W_down,e (act(W_gate,e x) * (W_up,e x)); fp32 accumulation.
+ * T <= 64 runs the decode path (fused dequant GEMV kernels); larger T runs as
+ * prefill in chunks of 128 tokens, each chunk routed, cached and grouped by
+ * expert before the grouped expert GEMMs ([P1] §2.5, §8.4). Bypassed experts
+ * are streamed into the context's staging arena.
+ * x: device bf16 [T][d_model]; zbias: device f32 [E] or NULL; y: device f32
+ * [T][d_model]. Optional ids_out (device int32 [T][k]) and gates_out (device
+ * f32 [T][k]) receive the routing; pass NULL to skip.
+ * Blocks the calling thread once per chunk until the routing is known on the
+ * host; y is complete when `stream` reaches the end of the call's work.
+ * Errors: MOE_EINVAL, MOE_ESTATE, MOE_ECOPY (the cache is consistent and the
+ * failed expert's slot is empty), MOE_ECUDA. */
+moe_status moe_forward(moe_layer* layer, const void* x_bf16, int32_t T, const float* zbias, float* y,
+                       int32_t* ids_out, float* gates_out, void* stream);
+
+/* Counters (see moe_stats). Waits for the layer's outstanding timing events. */
+moe_status moe_layer_stats(moe_layer* layer, moe_stats* out);
+moe_status moe_layer_reset_stats(moe_layer* layer);
+
+/* Slot table snapshot (host): expert per slot (-1 = empty) and LFU counts,
+ * arrays of cache_slots entries. */
+moe_status moe_cache_dump(const moe_layer* layer, int32_t* slot_expert, uint32_t* counts);
+
+void moe_layer_destroy(moe_layer* layer);
+
+/* ---- host cache manager (no GPU needed) -------------------------------- */
+
+/* The replacement policy that moe_cache_step runs, as a stand-alone host
+ * object, so that its trace can be checked on any machine. Same rules and
+ * outputs as moe_cache_step, without copies. Errors: MOE_EINVAL, MOE_ENOMEM. */
+moe_status moe_host_cache_create(int32_t n_experts, int32_t slots, int32_t policy, moe_host_cache** out);
+moe_status moe_host_cache_step(moe_host_cache* c, const int32_t* ids, int32_t n_ids, int32_t* slot_of,
+                               int32_t* miss_experts, int32_t* miss_slots, int32_t* n_miss, int32_t* n_hit,
+                               int32_t* n_bypass);
+moe_status moe_host_cache_dump(const moe_host_cache* c, int32_t* slot_expert, uint32_t* counts);
+void moe_host_cache_destroy(moe_host_cache* c);
+
+/* Stable grouping of n_pairs (token, rank) pairs by expert, as the prefill
+ * path does it ([P1] §2.5, §8.4: one fetched expert serves all rows of the
+ * chunk): perm lists pair indices of expert 0, then 1, ..., each ascending;
+ * offsets[e]..offsets[e+1] is expert e's range. Host arrays: ids [n_pairs],
+ * offsets [n_experts + 1], perm [n_pairs]. Errors: MOE_EINVAL. */
+moe_status moe_group_pairs(const int32_t* ids, int32_t n_pairs, int32_t n_experts, int32_t* offsets,
+                           int32_t* perm);
+
+/* ---- diagnostics -------------------------------------------------------- */
+
+const char* moe_status_str(moe_status s);
+const char* moe_last_error(void);
+
+/* Per-kernel device time, measured with CUDA events recorded around each
+ * launch on the launching stream while profiling is on (off by default; it
+ * adds event records to the stream). kind: 0 router, 1 shared gate/up,
+ * 2 shared down, 3 routed gate/up, 4 routed down, 5 combine, 6 grouped GEMM
+ * gate/up, 7 grouped GEMM down. Returns launches, total milliseconds and
+ * the algorithmic bytes and flops of those launches. Waits for the events. */
+moe_status moe_ctx_set_profiling(moe_ctx* ctx, int32_t on);
+moe_status moe_ctx_kernel_times(moe_ctx* ctx, int32_t kind, uint64_t* launches, double* total_ms,
+                                double* bytes, double* flops);
+moe_status moe_ctx_reset_kernel_times(moe_ctx* ctx);
+
+/* Fault injection on the host, for tests of the failure path: the nth miss
+ * copy issued from now on (0 = the next one) is reported as failed instead of
+ * being issued, exactly as if cudaMemcpyAsync had returned an error. The call
+ * that hits it returns MOE_ECOPY and leaves the affected slots empty; later
+ * calls proceed normally. nth < 0 disarms. No device fault is involved. */
+moe_status moe_ctx_inject_copy_failure(moe_ctx* ctx, int64_t nth);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H_ */

@@ -1,0 +1,224 @@
+"""GPU parity: the CUDA library against the CPU oracle, through the C ABI.
+
+Bars (fixed before any kernel ran):
+  * expert ids (and so the gates' order) and the cache hit/miss trace: bit-exact;
+  * gates: |g_gpu - g_oracle| <= 1e-6 (fp32 softmax of the same fp32 logits);
+  * layer outputs: max |y_gpu - y_oracle| <= 2e-3 * max |y_oracle| per call.
+The oracle runs the plain definition (double accumulation); the library runs
+fp32 fused dequant GEMVs, so only rounding separates them.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+import expert_streaming_ffn_gb300 as moe  # noqa: E402
+
+Y_TOL = 2e-3
+GATE_TOL = 1e-6
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    moe.load()
+    c = moe.moe_ctx_create(0)
+    yield c
+    moe.moe_ctx_destroy(c)
+
+
+class Rig:
+    """One library layer and the oracle's view of the same weights."""
+
+    def __init__(self, ctx, shapes, layer, slots, policy=moe.LFU, seed=0, weights=None):
+        self.s = shapes
+        self.w = weights if weights is not None else synth.layer_weights(shapes, layer, seed)
+        self.ref = oracle.Layer(self.w, shapes)
+        self.cache = oracle.Cache(shapes.n_experts, slots, policy)
+        self.slots = slots
+        self.h = moe.moe_layer_create(ctx, shapes, slots, policy)
+        moe.moe_layer_set_weights(self.h, self.w)
+        self.layer = layer
+
+    def close(self):
+        moe.moe_layer_destroy(self.h)
+
+    def forward(self, x_bits, zbias=None, check_y=True, y_tokens=None):
+        """Run the library, check ids/gates/trace exactly and y within tolerance."""
+        T = x_bits.shape[0]
+        k = self.s.top_k
+        x = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).cuda()
+        zb = None if zbias is None else torch.from_numpy(zbias).cuda()
+        ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        gates = torch.empty((T, k), dtype=torch.float32, device="cuda")
+        y = moe.moe_forward(self.h, x, zb, ids_out=ids, gates_out=gates)
+        torch.cuda.synchronize()
+        lg = oracle.router_logits(x_bits, self.w.router, self.s.n_experts, zbias)
+        oids, ogates = oracle.topk_gates(lg, k)
+        gids = ids.cpu().numpy()
+        assert (gids == oids).all(), "expert ids differ from the oracle"
+        assert np.abs(gates.cpu().numpy() - ogates).max() <= GATE_TOL
+        # the cache trace: the library's table after the call equals the oracle's
+        chunk = T if T <= 64 else 128
+        for t0 in range(0, T, chunk):
+            self.cache.step(oids[t0:t0 + chunk])
+        se, cnt = moe.moe_cache_dump(self.h, self.slots)
+        ose, ocnt = self.cache.dump()
+        assert (se == ose).all() and (cnt == ocnt).all(), "cache table differs from the oracle trace"
+        if check_y:
+            toks = range(T) if y_tokens is None else y_tokens
+            yg = y.cpu().numpy()
+            for t in toks:
+                ref = self.ref.combine(x_bits[t:t + 1], oids[t:t + 1], ogates[t:t + 1])[0]
+                err = np.abs(yg[t] - ref).max()
+                assert err <= Y_TOL * np.abs(ref).max(), (t, err, np.abs(ref).max())
+        return gids, y
+
+
+def test_tiny_layer_full_parity(ctx):
+    s = synth.SHAPES_TINY
+    r = Rig(ctx, s, 0, 4)
+    try:
+        for step in range(6):
+            r.forward(synth.tokens(s, 0, step, 4, False))
+        st = moe.moe_layer_stats(r.h)
+        assert st["steps"] == 6 and st["hits"] + st["misses"] > 0
+    finally:
+        r.close()
+
+
+def test_tiny_layer_matches_oracle_layer_output(ctx):
+    # the oracle's own fused layer (not only its per-expert pieces)
+    s = synth.SHAPES_TINY
+    r = Rig(ctx, s, 2, 4)
+    try:
+        xb = synth.tokens(s, 2, 0, 4, False)
+        zb = synth.zipf_bias(s, 2, 0.8)
+        _, y = r.forward(xb, zb, check_y=False)
+        _, _, _, yo = r.ref.forward(xb, zb)
+        assert np.abs(y.cpu().numpy() - yo).max() <= Y_TOL * np.abs(yo).max()
+    finally:
+        r.close()
+
+
+@pytest.mark.parametrize("T", [1, 3, 16, 64, 65, 128, 200])
+def test_tiny_ragged_token_counts(ctx, T):
+    # decode (T <= 64) and prefill (chunks of 128 plus a ragged tail)
+    s = synth.SHAPES_TINY
+    r = Rig(ctx, s, 1, 4)
+    try:
+        r.forward(synth.tokens(s, 1, T, T, False), y_tokens=range(0, T, max(1, T // 7)))
+    finally:
+        r.close()
+
+
+@pytest.mark.parametrize("slots,k", [(1, 2), (16, 2), (4, 1), (4, 16)])
+def test_tiny_degenerate_caches_and_top_k(ctx, slots, k):
+    # one slot (almost everything bypasses), all experts resident, k = 1, k = E
+    s = synth.Shapes(512, 16, k, 256, 512, synth.GELU_TANH)
+    r = Rig(ctx, s, 0, slots)
+    try:
+        for step in range(3):
+            r.forward(synth.tokens(s, 0, step, 5, False))
+    finally:
+        r.close()
+
+
+def test_decode_2816_two_layers(ctx):
+    s = synth.SHAPES_2816
+    wl = synth.WORKLOADS["decode_2816"]
+    for layer in (0, 17):
+        r = Rig(ctx, s, layer, wl.cache_slots)
+        zb = synth.zipf_bias(s, layer, wl.zipf_s)
+        try:
+            for step in range(8):
+                x = synth.tokens(s, layer, step, 1, True)
+                r.forward(x, zb, check_y=step in (0, 7))
+            st = moe.moe_layer_stats(r.h)
+            assert st["hits"] > 0 and st["misses"] > 0
+        finally:
+            r.close()
+
+
+@pytest.mark.parametrize("T,policy", [(1, moe.LFU), (8, moe.LRU)])
+def test_decode_2048_silu(ctx, T, policy):
+    s = synth.SHAPES_2048
+    wl = synth.WORKLOADS["decode_2048"]
+    r = Rig(ctx, s, 3, wl.cache_slots, policy)
+    zb = synth.zipf_bias(s, 3, wl.zipf_s)
+    try:
+        for step in range(5):
+            x = synth.tokens(s, 3, step, T, True)
+            r.forward(x, zb, check_y=step == 4, y_tokens=[0, T - 1])
+    finally:
+        r.close()
+
+
+def test_prefill_chunk_2816(ctx):
+    s = synth.SHAPES_2816
+    r = Rig(ctx, s, 5, 16)
+    try:
+        x = synth.tokens(s, 5, 0, 128, True)
+        r.forward(x, None, y_tokens=[0, 61, 127])
+        st = moe.moe_layer_stats(r.h)
+        assert st["bypass"] > 0  # a 128-token chunk touches far more than 16 experts
+    finally:
+        r.close()
+
+
+def test_route_call_matches_oracle(ctx):
+    s = synth.SHAPES_2816
+    r = Rig(ctx, s, 9, 16)
+    try:
+        xb = synth.tokens(s, 9, 0, 37, True)
+        zb = synth.zipf_bias(s, 9, 1.1)
+        x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+        ids, gates = moe.moe_route(r.h, x, s.top_k, torch.from_numpy(zb).cuda())
+        torch.cuda.synchronize()
+        oids, og = oracle.topk_gates(oracle.router_logits(xb, r.w.router, s.n_experts, zb), s.top_k)
+        assert (ids.cpu().numpy() == oids).all()
+        assert np.abs(gates.cpu().numpy() - og).max() <= GATE_TOL
+    finally:
+        r.close()
+
+
+def test_cache_step_call_and_forward_agree(ctx):
+    s = synth.SHAPES_TINY
+    r = Rig(ctx, s, 0, 4)
+    try:
+        ids = np.array([[3, 5], [5, 9]], np.int32)
+        out = moe.moe_cache_step(r.h, ids)
+        o = r.cache.step(ids)
+        assert (out["slot_of"] == o["slot_of"]).all()
+        assert (out["miss_experts"] == o["miss_experts"]).all() and (out["miss_slots"] == o["miss_slots"]).all()
+        # the copies it issued must leave the slots usable by a forward
+        for step in range(3):
+            r.forward(synth.tokens(s, 0, 10 + step, 4, False))
+    finally:
+        r.close()
+
+
+def test_injected_copy_failure_is_reported_and_recovers(ctx):
+    # A host-made fault: the next miss copy reports failure instead of being issued.
+    s = synth.SHAPES_TINY
+    r = Rig(ctx, s, 0, 4)
+    try:
+        x0 = synth.tokens(s, 0, 0, 4, False)
+        moe.moe_ctx_inject_copy_failure(ctx, 0)
+        x = torch.from_numpy(x0.view(np.int16)).view(torch.bfloat16).cuda()
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_forward(r.h, x)
+        assert ei.value.status == moe.MOE_ECOPY
+        torch.cuda.synchronize()
+        se, _ = moe.moe_cache_dump(r.h, 4)
+        assert (se == -1).all()  # every slot whose copy was not issued is left empty
+        # the oracle never saw the failed call; reset the library's view to match
+        moe.moe_layer_set_weights(r.h, r.w)
+        for step in range(3):
+            r.forward(synth.tokens(s, 0, 20 + step, 4, False))
+    finally:
+        r.close()
