@@ -1,0 +1,475 @@
+#!/usr/bin/env python
+"""Benchmark of the expert-streaming MoE layer on GB300.
+
+Workload (default): decode_2816 — 30 MoE layers, one token per step, d=2816,
+256 routed experts (top-8, FFN 2816->704->2816), shared expert 2816->2816->2816,
+int4 affine g64 experts, 8-bit router, a 16-slot LFU expert cache per layer in
+HBM with every other expert in pinned host memory, Zipf(1.1) router bias.
+Inputs are seeded and synthetic (see synth/). A step is one token through all
+30 layers: route, cache step, miss copies, shared expert, routed experts and
+combine, for every layer.
+
+Prints one JSON line. Metric: decode tokens/s (whole job); also the achieved
+HBM bandwidth of the dominant kernel against the measured peak, the prefill
+chunk rate and expert TFLOP/s, the CPU oracle as a baseline, and the same
+decode metric end to end with host buffers.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the layer does not shard); value = all ranks' tokens / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "MoE decode tok/s + achieved HBM GB/s vs peak; prefill-chunk expert TFLOP/s"
+L2_BYTES = 129 * 2 ** 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=240)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=None, help="override the layer count (testing only)")
+    ap.add_argument("--prefill-layers", type=int, default=2)
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only: a barrier and a max, no data exchange)
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None):
+        self.rows = []
+        self.proc = None
+        self.bus_id = bus_id
+
+    def __enter__(self):
+        cmd = ["nvidia-smi", f"--query-gpu=pci.bus_id,{self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.15)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = self.rows
+        if self.bus_id:
+            mine = [r for r in rows if r[0].lower().endswith(self.bus_id.lower()[-12:])]
+            rows = mine or rows
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def gpu_bus_id(dev: int) -> str | None:
+    try:
+        import torch
+
+        p = torch.cuda.get_device_properties(dev)
+        dom, bus, devid = getattr(p, "pci_domain_id", None), getattr(p, "pci_bus_id", None), getattr(p, "pci_device_id", None)
+        if bus is None:
+            return None
+        return f"{dom or 0:08X}:{bus:02X}:{devid or 0:02X}.0"
+    except Exception:
+        return None
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and the reference arm)
+
+
+def oracle_layer_tokens(n_max: int, seconds: float, wl, layers=(0, 1)):
+    """Time the oracle on whole layer-tokens of the workload (single thread)."""
+    import oracle
+    import synth
+
+    s = wl.shapes
+    times = []
+    done = 0
+    for li, layer in enumerate(layers):
+        w = synth.layer_weights(s, layer, wl.seed)
+        L = oracle.Layer(w, s)
+        zb = synth.zipf_bias(s, layer, wl.zipf_s, wl.zipf_beta, wl.seed) if wl.zipf_s else None
+        per_layer = max(1, n_max // len(layers))
+        for step in range(per_layer):
+            x = synth.tokens(s, layer, step, 1, wl.rms_normalise, wl.seed)
+            t = time.perf_counter()
+            L.forward(x, zb)
+            times.append(time.perf_counter() - t)
+            done += 1
+            if sum(times) >= seconds and done >= 2:
+                return times
+        del L, w
+    return times
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle as it stands, on the host cores."""
+    import synth
+
+    if rank != 0:
+        return
+    wl = synth.WORKLOADS["decode_2816"]
+    n_layers = args.layers or wl.n_layers
+    # warm-up layer-tokens, then timed ones; each step is one layer-token sample
+    warm = oracle_layer_tokens(max(1, min(args.warmup, 1)), 0.0, wl, layers=(0,))
+    budget_s = 90.0
+    first = warm[0] if warm else 1.5
+    n = max(2, min(args.steps, int(budget_s / max(first, 1e-3))))
+    times = oracle_layer_tokens(n, 1e9, wl, layers=(0, 1))
+    layer_s = statistics.mean(times)
+    tok_s = 1.0 / (layer_s * n_layers)
+    sample = f"{len(times)} layer-tokens of decode_2816 (layers 0-1), extrapolated to {n_layers} layers per token"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": tok_s, "unit": "tok/s", "n_gpus": args.gpus,
+        "steps": len(times), "warmup": len(warm), "ms_per_step": 1000 * layer_s * n_layers,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": "decode_2816", "layers": n_layers, "tokens_per_step": 1,
+                                        "cache_slots": 16, "policy": "LFU", "zipf_s": 1.1},
+        "cpu_baseline": {"value": tok_s, "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": tok_s, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import expert_streaming_ffn_gb300 as moe
+    import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    moe.load()
+    wl = synth.WORKLOADS["decode_2816"]
+    s = wl.shapes
+    n_layers = args.layers or wl.n_layers
+    steps_total = args.warmup + args.steps
+    seed = wl.seed + 1000 * rank  # independent replicas
+
+    ctx = moe.moe_ctx_create(local)
+    layers, zbs = [], []
+    w = None
+    for l in range(n_layers):
+        w = synth.layer_weights(s, l, seed, reuse=w)
+        h = moe.moe_layer_create(ctx, s, wl.cache_slots, wl.policy)
+        moe.moe_layer_set_weights(h, w)
+        layers.append(h)
+        zbs.append(torch.from_numpy(synth.zipf_bias(s, l, wl.zipf_s, wl.zipf_beta, seed)).to(dev))
+    # inputs resident in HBM: x[step][layer][d] bf16, drawn per (step, layer)
+    xs_np = np.empty((steps_total, n_layers, s.d_model), np.uint16)
+    for st in range(steps_total):
+        for l in range(n_layers):
+            xs_np[st, l] = synth.tokens(s, l, st, 1, wl.rms_normalise, seed)[0]
+    x_dev = torch.from_numpy(xs_np.view(np.int16)).view(torch.bfloat16).to(dev)
+    y_dev = torch.empty((n_layers, s.d_model), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    row = s.d_model * 2
+
+    def step(st):
+        base = x_dev.data_ptr() + st * n_layers * row
+        for l in range(n_layers):
+            moe.moe_forward_ptr(layers[l], base + l * row, 1, zbs[l].data_ptr(), y_dev[l].data_ptr(), sptr)
+
+    for st in range(args.warmup):
+        step(st)
+    torch.cuda.synchronize(dev)
+    for h in layers:
+        moe.moe_layer_reset_stats(h)
+    launches0 = moe.moe_ctx_launches(ctx)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(gpu_bus_id(local)) as clocks:
+        t_wall = time.perf_counter()
+        ev0.record(stream)
+        for st in range(args.warmup, steps_total):
+            step(st)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall
+    barrier(world)
+    ms = ev0.elapsed_time(ev1)
+    launches = moe.moe_ctx_launches(ctx) - launches0
+    ms_max = max_over_ranks(ms, world)
+    stats = [moe.moe_layer_stats(h) for h in layers]
+    hits = sum(x["hits"] for x in stats)
+    misses = sum(x["misses"] for x in stats)
+    h2d = sum(x["bytes_h2d"] for x in stats)
+    resident = sum(x["bytes_resident"] for x in stats)
+    exposed = sum(x["exposed_copy_us"] for x in stats)
+    host_wait = sum(x["host_wait_us"] for x in stats)
+    host_issue = sum(x["host_issue_us"] for x in stats)
+
+    # same steps again with per-kernel CUDA events (on the launching stream)
+    moe.moe_ctx_set_profiling(ctx, True)
+    moe.moe_ctx_reset_kernel_times(ctx)
+    for st in range(args.warmup, steps_total):
+        step(st)
+    torch.cuda.synchronize(dev)
+    kt = moe.moe_ctx_kernel_times(ctx)
+    moe.moe_ctx_set_profiling(ctx, False)
+    peaks, peak_src = measured_peaks()
+    dom = max(kt.items(), key=lambda kv: kv[1][1])
+    name, (n_l, tot_ms, by, fl) = dom
+    achieved = by / (tot_ms * 1e-3) / 1e9 if tot_ms > 0 else 0.0
+    all_ms = sum(v[1] for v in kt.values())
+    all_bytes = sum(v[2] for v in kt.values())
+    kernels = {k: {"launches": v[0], "ms": round(v[1], 4), "share": round(v[1] / all_ms, 4) if all_ms else 0,
+                   "GB_s": round(v[2] / (v[1] * 1e-3) / 1e9, 1) if v[1] > 0 else None}
+               for k, v in kt.items() if v[0] > 0}
+
+    # end to end through the public call with host buffers: per step, the
+    # step's x (all layers) host->device from pinned memory, the 30 layer
+    # calls, and y device->host read back
+    e2e = None
+    if not args.no_e2e:
+        x_host = torch.from_numpy(xs_np.view(np.int16)).view(torch.bfloat16).pin_memory()
+        x_stage = torch.empty((n_layers, s.d_model), dtype=torch.bfloat16, device=dev)
+        y_host = torch.empty((n_layers, s.d_model), dtype=torch.float32).pin_memory()
+
+        def e2e_step(st):
+            x_stage.copy_(x_host[st], non_blocking=True)
+            for l in range(n_layers):
+                moe.moe_forward_ptr(layers[l], x_stage[l].data_ptr(), 1, zbs[l].data_ptr(), y_dev[l].data_ptr(), sptr)
+            y_host.copy_(y_dev, non_blocking=True)
+            torch.cuda.current_stream(dev).synchronize()
+            return float(y_host[0, 0])
+
+        for st in range(min(3, args.warmup)):
+            e2e_step(st)
+        barrier(world)
+        t0 = time.perf_counter()
+        for st in range(args.warmup, steps_total):
+            e2e_step(st)
+        t_e2e = max_over_ranks(time.perf_counter() - t0, world)
+        e2e = {"value": world * args.steps / t_e2e, "unit": "tok/s",
+               "h2d_bytes_per_step": n_layers * s.d_model * 2, "d2h_bytes_per_step": n_layers * s.d_model * 4}
+
+    prefill = None
+    if not args.no_prefill and args.prefill_layers > 0:
+        prefill = run_prefill(args, ctx, dev, stream, seed)
+
+    for h in layers:
+        moe.moe_layer_destroy(h)
+    moe.moe_ctx_destroy(ctx)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        times = oracle_layer_tokens(64, args.cpu_seconds, wl)
+        layer_s = statistics.mean(times)
+        cpu = {"value": 1.0 / (layer_s * n_layers), "unit": "tok/s", "cores": 1, "kind": "oracle",
+               "sample": f"{len(times)} layer-tokens of decode_2816 (layers 0-1) single-threaded, "
+                         f"extrapolated to {n_layers} layers per token"}
+
+    if rank != 0:
+        return
+    tok_s = world * args.steps / (ms_max * 1e-3)
+    lookups = hits + misses
+    out = {
+        "metric": METRIC, "value": tok_s, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded int4/int8 weights and N(0,1) RMS-normalised bf16 activations)",
+        "config": {"workload": "decode_2816", "layers": n_layers, "tokens_per_step": 1, "d_model": s.d_model,
+                   "experts": s.n_experts, "top_k": s.top_k, "d_ff": s.d_ff, "d_ff_shared": s.d_ff_shared,
+                   "cache_slots": wl.cache_slots, "policy": "LFU", "zipf_s": wl.zipf_s,
+                   "l2": f"inputs larger than L2: {resident / args.steps / 1e9:.2f} GB of weights read per step "
+                         f"vs {L2_BYTES / 2**20:.0f} MiB L2",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "hit_rate": hits / lookups if lookups else None,
+        "h2d_MB_per_token": h2d / args.steps / 1e6,
+        "exposed_copy_us_per_token": exposed / args.steps,
+        "host_wait_us_per_token": host_wait / args.steps,
+        "host_issue_us_per_token": host_issue / args.steps,
+        "resident_GB_per_token": resident / args.steps / 1e9,
+        "hbm_GBs_all_kernels": all_bytes / (all_ms * 1e-3) / 1e9 if all_ms else None,
+        "roofline": {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                     else "fallback 6.8 TB/s"},
+        "kernels": kernels,
+        "prefill": prefill,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks.summary(),
+        "wall_s_timed_region": t_wall,
+    }
+    print(json.dumps(out), flush=True)
+
+
+def run_prefill(args, ctx, dev, stream, seed):
+    """prefill_2816: 8 chunks of 128 tokens per layer on a few fresh layers."""
+    import torch
+
+    import expert_streaming_ffn_gb300 as moe
+    import synth
+
+    wl = synth.WORKLOADS["prefill_2816"]
+    s = wl.shapes
+    P = args.prefill_layers
+    prompt = wl.tokens * wl.steps  # 1024
+    layers = []
+    w = None
+    for l in range(P):
+        w = synth.layer_weights(s, l, seed, reuse=w)
+        h = moe.moe_layer_create(ctx, s, wl.cache_slots, wl.policy)
+        moe.moe_layer_set_weights(h, w)
+        layers.append(h)
+    xs = [torch.from_numpy(synth.tokens(s, l, 0, prompt, wl.rms_normalise, seed).view(np.int16))
+          .view(torch.bfloat16).to(dev) for l in range(P)]
+    y = torch.empty((prompt, s.d_model), dtype=torch.float32, device=dev)
+    # warm-up on a separate layer-sized call to load kernels, then reset caches
+    moe.moe_forward(layers[0], xs[0][:128], y=y[:128])
+    torch.cuda.synchronize(dev)
+    w = synth.layer_weights(s, 0, seed, reuse=w)
+    moe.moe_layer_set_weights(layers[0], w)
+    moe.moe_ctx_set_profiling(ctx, True)
+    moe.moe_ctx_reset_kernel_times(ctx)
+    for h in layers:
+        moe.moe_layer_reset_stats(h)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    ev0.record(stream)
+    for l in range(P):
+        moe.moe_forward(layers[l], xs[l], y=y)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = ev0.elapsed_time(ev1)
+    kt = moe.moe_ctx_kernel_times(ctx)
+    moe.moe_ctx_set_profiling(ctx, False)
+    stats = [moe.moe_layer_stats(h) for h in layers]
+    for h in layers:
+        moe.moe_layer_destroy(h)
+    expert_kinds = ("expert_ffn", "gemm_gateup", "gemm_down")
+    fl = sum(kt[k][3] for k in expert_kinds)
+    kms = sum(kt[k][1] for k in expert_kinds)
+    hits = sum(x["hits"] for x in stats)
+    misses = sum(x["misses"] for x in stats)
+    return {
+        "workload": "prefill_2816", "layers_measured": P, "prompt_tokens": prompt, "chunk": wl.tokens,
+        "tok_s_per_layer": prompt * P / (ms * 1e-3),
+        "tok_s_30_layers": prompt / (ms * 1e-3 / P * 30),
+        "expert_TFLOPs": fl / (kms * 1e-3) / 1e12 if kms else None,
+        "expert_kernel_ms": kms, "wall_ms": ms,
+        "hit_rate": hits / (hits + misses) if hits + misses else None,
+        "h2d_GB": sum(x["bytes_h2d"] for x in stats) / 1e9,
+        "exposed_copy_ms": sum(x["exposed_copy_us"] for x in stats) / 1e3,
+        "kernels": {k: {"launches": v[0], "ms": round(v[1], 3),
+                        "TFLOPs": round(v[3] / (v[1] * 1e-3) / 1e12, 2) if v[1] > 0 else None}
+                    for k, v in kt.items() if v[0] > 0},
+    }
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -23,8 +23,7 @@ _lib = None
 MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA, MOE_ECOPY, MOE_ETIMEOUT, MOE_ESTATE = range(7)
 LFU, LRU = 0, 1
 GELU_TANH, SILU = 0, 1
-KERNEL_KINDS = ("router", "shared_gateup", "shared_down", "routed_gateup", "routed_down", "combine",
-                "gemm_gateup", "gemm_down")
+KERNEL_KINDS = ("router", "expert_ffn", "combine", "gemm_gateup", "gemm_down")
 
 
 class MoeError(RuntimeError):
@@ -57,7 +56,8 @@ class moe_host_weights(ctypes.Structure):
 class moe_stats(ctypes.Structure):
     _fields_ = [("steps", ctypes.c_uint64), ("hits", ctypes.c_uint64), ("misses", ctypes.c_uint64),
                 ("bypass", ctypes.c_uint64), ("bytes_h2d", ctypes.c_uint64), ("bytes_resident", ctypes.c_uint64),
-                ("exposed_copy_us", ctypes.c_double)]
+                ("exposed_copy_us", ctypes.c_double), ("host_wait_us", ctypes.c_double),
+                ("host_issue_us", ctypes.c_double)]
 
 
 # (name, restype, argtypes) of every exported symbol in include/moe.h
@@ -87,6 +87,7 @@ SIGNATURES = [
     ("moe_ctx_kernel_times", _i32, [_vp, _i32, _P(ctypes.c_uint64), _P(ctypes.c_double), _P(ctypes.c_double),
                                     _P(ctypes.c_double)]),
     ("moe_ctx_reset_kernel_times", _i32, [_vp]),
+    ("moe_ctx_launches", _i32, [_vp, _P(ctypes.c_uint64)]),
     ("moe_ctx_inject_copy_failure", _i32, [_vp, _i64]),
 ]
 
@@ -324,6 +325,12 @@ def moe_ctx_kernel_times(ctx: int) -> dict:
 
 def moe_ctx_reset_kernel_times(ctx: int) -> None:
     _check(load().moe_ctx_reset_kernel_times(ctx), "moe_ctx_reset_kernel_times")
+
+
+def moe_ctx_launches(ctx: int) -> int:
+    n = ctypes.c_uint64()
+    _check(load().moe_ctx_launches(ctx, ctypes.byref(n)), "moe_ctx_launches")
+    return n.value
 
 
 def moe_ctx_inject_copy_failure(ctx: int, nth: int) -> None:

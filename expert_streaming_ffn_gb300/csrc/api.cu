@@ -4,20 +4,21 @@
 //   [P1] "在 Rockchip NPU 上实现 turbo-fieldfare 风格 MoE 大模型流式推理的技术方案"
 //   [P3] "BigMoeOnEdge：端侧 MoE 专家流式推理原理与实测"
 //
-// Per layer and call (decode), the three phases of [P1] §2.4 / §8.2 map to:
-//   cb1  router kernel on the caller's stream, ids copied to pinned host memory;
-//        the shared expert is enqueued behind it, so it runs while the host
-//        waits and while misses stream ([P1] §2.4: "meanwhile the GPU can start
-//        the shared-expert branch");
+// One decode call maps the three phases of [P1] §2.4 / §8.2 onto the GPU:
+//   cb1  the router kernel publishes each id to mapped host memory as it is
+//        chosen, tagged with the call number;
 //   io   host LFU/LRU step; one cudaMemcpyAsync per miss from the pinned pool
-//        into its HBM slot on the context's copy stream, each followed by that
-//        slot's ready event ([P3] "读取完成后，算子才可以使用切片": a hit is
-//        ready at once, a miss when its read completes);
-//   cb2  routed experts that hit run at once; the compute stream then waits on
-//        the ready events of the misses and runs them; the combine adds the
-//        gate-weighted expert outputs to the shared output in rank order.
-// Ready state is an event per slot, re-recorded by every copy into the slot,
-// so a later wait can never observe a stale "ready" from an earlier round.
+//        into its HBM slot (or, for a bypass, into the staging arena) on the
+//        context's copy stream, each followed by a stream write of the call's
+//        round number into that slot's ready flag ([P3] "读取完成后，算子才可以
+//        使用切片": a hit is ready at once, a miss when its read completes, and
+//        the round number keeps a stale "ready" from being reused);
+//   cb2  one fused kernel runs the shared expert and every routed expert -
+//        the shared expert and the hits at once, each miss as soon as its flag
+//        shows the current round, so the shared branch overlaps the reads
+//        ([P1] §2.4: it does not depend on the routed experts) - and writes
+//        y = shared + the gate-weighted routed outputs in rank order.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdarg.h>
 #include <stdio.h>
@@ -25,7 +26,7 @@
 #include <string.h>
 
 #include <algorithm>
-#include <mutex>
+#include <chrono>
 #include <new>
 #include <thread>
 #include <vector>
@@ -74,7 +75,10 @@ using namespace moe;
 namespace {
 
 constexpr int kKinds = 8;
-enum Kind { K_ROUTER = 0, K_SHARED_GU, K_SHARED_DN, K_ROUTED_GU, K_ROUTED_DN, K_COMBINE, K_GEMM_GU, K_GEMM_DN };
+enum Kind { K_ROUTER = 0, K_FFN = 1, K_COMBINE = 2, K_GEMM_GU = 3, K_GEMM_DN = 4 };
+constexpr double kHostWaitLimitS = 10.0;  // longest the host waits for the routing of one call
+
+using WriteValue32 = CUresult (*)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
 
 struct ProfRec {
     int kind;
@@ -83,7 +87,7 @@ struct ProfRec {
 };
 
 struct WaitRec {
-    cudaEvent_t a, b;
+    cudaEvent_t ffn_start, copies_done;
 };
 
 }  // namespace
@@ -94,6 +98,7 @@ struct moe_ctx {
     uint8_t* staging = nullptr;  // transient arena for bypassed experts
     size_t staging_bytes = 0;
     cudaEvent_t staging_free = nullptr;  // after the last kernels that read staging
+    WriteValue32 write_value = nullptr;  // cuStreamWriteValue32
     bool profiling = false;
     std::vector<ProfRec> prof;
     struct Acc {
@@ -101,9 +106,12 @@ struct moe_ctx {
         double ms = 0, bytes = 0, flops = 0;
     } acc[kKinds];
     std::vector<cudaEvent_t> timing_pool;
+    uint64_t launches = 0;          // kernels launched by this context's layers
+    unsigned* err_host = nullptr;   // mapped pinned word that kernels report expired waits into
+    unsigned* err_dev = nullptr;
+    uint32_t err_generation = 0;  // bumped whenever a kernel reported an expired wait
     long fail_copy_at = -1;  // test hook: the n-th miss copy from now reports failure
     long copies_issued = 0;
-    std::mutex mu;
 
     cudaEvent_t timing_event() {
         if (!timing_pool.empty()) {
@@ -126,22 +134,33 @@ struct moe_layer {
     uint32_t* d_router_sb = nullptr;
     uint8_t* d_shared = nullptr;
     uint8_t* d_slots = nullptr;
-    uint8_t* h_pool = nullptr;  // pinned, E * ebytes
+    uint8_t* h_pool = nullptr;    // pinned, E * ebytes
+    uint32_t* d_ready = nullptr;  // ready flags: slots, then staging entries
+    uint32_t epoch = 0;           // round number of the current call
+    uint32_t seq = 0;             // routing publication number
     HostCache cache;
     StepResult step;
-    std::vector<cudaEvent_t> slot_ready;
-    cudaEvent_t ev_ids = nullptr, ev_done = nullptr, ev_bypass = nullptr;
+    cudaEvent_t ev_done = nullptr;     // end of the layer's last call
+    cudaEvent_t ev_pending = nullptr;  // copies issued by moe_cache_step
     bool loaded = false;
-    // scratch, sized for cap_T tokens
+    // scratch, sized for cap_T tokens per call
     int cap_T = 0;
     float* d_logits = nullptr;
-    unsigned* d_counters = nullptr;
+    unsigned* d_rcount = nullptr;  // router block counters
     int32_t* d_ids = nullptr;
     float* d_gates = nullptr;
     float* d_h = nullptr;
     float* d_hs = nullptr;
     float* d_o = nullptr;
-    int32_t* h_ids = nullptr;  // pinned
+    float* d_os = nullptr;     // shared-expert outputs [cap_T][d]
+    unsigned long long* h_pub = nullptr;  // mapped pinned [cap_T * k]: seq << 32 | id
+    unsigned long long* h_pub_dev = nullptr;
+    std::vector<int32_t> h_ids;           // ids of the current call, read from h_pub
+    float* d_part = nullptr;
+    size_t part_floats = 0;
+    unsigned* d_fcount = nullptr;
+    size_t n_fcount = 0;
+    uint32_t err_generation = 0;  // the context's value when the counters were last known zero
     std::vector<int32_t> offsets, perm;
     moe_stats stats{};
     std::vector<WaitRec> waits;
@@ -153,7 +172,7 @@ namespace {
 
 moe_status check_shapes(const moe_shapes* s) {
     if (!s) return set_error(MOE_EINVAL, "shapes is NULL");
-    if (s->d_model < 64 || s->d_model > kMaxDModel || s->d_model % 256 != 0)
+    if (s->d_model < 256 || s->d_model > kMaxDModel || s->d_model % 256 != 0)
         return set_error(MOE_EINVAL, "d_model %d must be a multiple of 256 in [256, %d]", s->d_model, kMaxDModel);
     if (s->d_ff < 64 || s->d_ff % 64 != 0 || s->d_ff > kMaxDModel)
         return set_error(MOE_EINVAL, "d_ff %d must be a multiple of 64 in [64, %d]", s->d_ff, kMaxDModel);
@@ -170,44 +189,60 @@ moe_status check_shapes(const moe_shapes* s) {
 
 void free_scratch(moe_layer* L) {
     cudaFree(L->d_logits);
-    cudaFree(L->d_counters);
+    cudaFree(L->d_rcount);
     cudaFree(L->d_ids);
     cudaFree(L->d_gates);
     cudaFree(L->d_h);
     cudaFree(L->d_hs);
     cudaFree(L->d_o);
-    cudaFreeHost(L->h_ids);
+    cudaFree(L->d_os);
+    cudaFree(L->d_part);
+    cudaFree(L->d_fcount);
+    cudaFreeHost(L->h_pub);
     L->d_logits = nullptr;
-    L->d_counters = nullptr;
+    L->d_rcount = nullptr;
     L->d_ids = nullptr;
     L->d_gates = nullptr;
-    L->d_h = L->d_hs = L->d_o = nullptr;
-    L->h_ids = nullptr;
+    L->d_h = L->d_hs = L->d_o = L->d_os = L->d_part = nullptr;
+    L->d_fcount = nullptr;
+    L->h_pub = L->h_pub_dev = nullptr;
+    L->part_floats = L->n_fcount = 0;
     L->cap_T = 0;
 }
 
 // Scratch for up to T tokens per call (grows; never shrinks).
 moe_status ensure_scratch(moe_layer* L, int T) {
     if (T <= L->cap_T) return MOE_OK;
-    if (L->ev_done) CUDA_TRY(cudaEventSynchronize(L->ev_done));  // old buffers may still be in use
+    if (L->ev_done) CUDA_TRY(cudaEventSynchronize(L->ev_done));  // the old buffers may still be in use
     free_scratch(L);
     const moe_shapes& s = L->sh;
     const size_t pairs = (size_t)T * s.top_k;
     const int blocks = (T + 7) / 8;
+    const int routed_items = (int)std::min<size_t>(256, pairs);
+    const int shared_items = (T + kFfnMaxNT - 1) / kFfnMaxNT;
+    L->part_floats = ffn_max_partial_floats(s.d_model, shared_items, s.d_ff_shared, routed_items, s.d_ff);
+    L->n_fcount = ffn_max_counters(s.d_model, shared_items, s.d_ff_shared, routed_items, s.d_ff);
     bool ok = cudaMalloc(&L->d_logits, sizeof(float) * T * s.n_experts) == cudaSuccess &&
-              cudaMalloc(&L->d_counters, sizeof(unsigned) * blocks) == cudaSuccess &&
-              cudaMemset(L->d_counters, 0, sizeof(unsigned) * blocks) == cudaSuccess &&
+              cudaMalloc(&L->d_rcount, sizeof(unsigned) * blocks) == cudaSuccess &&
+              cudaMemset(L->d_rcount, 0, sizeof(unsigned) * blocks) == cudaSuccess &&
               cudaMalloc(&L->d_ids, sizeof(int32_t) * pairs) == cudaSuccess &&
               cudaMalloc(&L->d_gates, sizeof(float) * pairs) == cudaSuccess &&
               cudaMalloc(&L->d_h, sizeof(float) * pairs * s.d_ff) == cudaSuccess &&
               cudaMalloc(&L->d_hs, sizeof(float) * (size_t)T * s.d_ff_shared) == cudaSuccess &&
               cudaMalloc(&L->d_o, sizeof(float) * pairs * s.d_model) == cudaSuccess &&
-              cudaHostAlloc(&L->h_ids, sizeof(int32_t) * pairs, cudaHostAllocDefault) == cudaSuccess;
+              cudaMalloc(&L->d_os, sizeof(float) * (size_t)T * s.d_model) == cudaSuccess &&
+              cudaMalloc(&L->d_part, sizeof(float) * L->part_floats) == cudaSuccess &&
+              cudaMalloc(&L->d_fcount, sizeof(unsigned) * L->n_fcount) == cudaSuccess &&
+              cudaMemset(L->d_fcount, 0, sizeof(unsigned) * L->n_fcount) == cudaSuccess &&
+              cudaHostAlloc(&L->h_pub, sizeof(unsigned long long) * pairs, cudaHostAllocMapped) == cudaSuccess &&
+              cudaHostGetDevicePointer(&L->h_pub_dev, L->h_pub, 0) == cudaSuccess;
     if (!ok) {
         cudaGetLastError();
         free_scratch(L);
         return set_error(MOE_ENOMEM, "scratch allocation for %d tokens failed", T);
     }
+    memset(L->h_pub, 0, sizeof(unsigned long long) * pairs);
+    L->h_ids.assign(pairs, 0);
     L->cap_T = T;
     return MOE_OK;
 }
@@ -232,6 +267,7 @@ struct Prof {
     cudaStream_t s;
     ProfRec r{};
     Prof(moe_ctx* c, cudaStream_t st, int kind, double bytes, double flops) : C(c), s(st) {
+        ++C->launches;
         if (!C->profiling) return;
         r.kind = kind;
         r.bytes = bytes;
@@ -262,25 +298,38 @@ void drain_prof(moe_ctx* C) {
     C->prof.clear();
 }
 
+// Exposed copy time: how long the routed-expert kernel had misses still
+// landing after it started (zero when every copy finished before it).
 void drain_waits(moe_layer* L) {
     for (WaitRec& w : L->waits) {
-        cudaEventSynchronize(w.b);
+        cudaEventSynchronize(w.copies_done);
+        cudaEventSynchronize(w.ffn_start);
         float ms = 0;
-        cudaEventElapsedTime(&ms, w.a, w.b);
-        L->stats.exposed_copy_us += 1000.0 * ms;
-        L->ctx->timing_pool.push_back(w.a);
-        L->ctx->timing_pool.push_back(w.b);
+        if (cudaEventElapsedTime(&ms, w.ffn_start, w.copies_done) == cudaSuccess && ms > 0)
+            L->stats.exposed_copy_us += 1000.0 * ms;
+        cudaGetLastError();
+        L->ctx->timing_pool.push_back(w.ffn_start);
+        L->ctx->timing_pool.push_back(w.copies_done);
     }
     L->waits.clear();
 }
 
-double qbytes(int N, int K) { return (double)qmat_bytes(N, K); }
+moe_status check_err_word(moe_ctx* C) {
+    if (const unsigned ew = *(volatile unsigned*)C->err_host) {
+        *(volatile unsigned*)C->err_host = 0;
+        ++C->err_generation;  // a kernel that gave up may have left counters non-zero
+        return set_error(MOE_ETIMEOUT, "a bounded device wait expired in an earlier kernel (code %u)", ew);
+    }
+    return MOE_OK;
+}
 
-// Issue the copies of one cache step's misses. Slot misses land in their
-// slots and record the slot's ready event; bypassed experts land in staging,
-// in miss order, and share one ready event. On failure the failed slot is
-// emptied so that the table never claims an expert whose bytes are missing.
-moe_status issue_miss_copies(moe_layer* L, const StepResult& r, bool with_bypass, int* n_bypass_staged) {
+// Issue the copies of one cache step's misses. A slot miss lands in its slot,
+// a bypass in the next staging entry; after each copy the copy stream writes
+// `epoch` into the matching ready flag (slot s -> flag s, staging entry b ->
+// flag S + b). On failure every slot this step filled but whose copy is not
+// known good is emptied, so the table never claims bytes that are missing.
+moe_status issue_miss_copies(moe_layer* L, const StepResult& r, bool with_bypass, uint32_t epoch,
+                             std::vector<int>* ready_of_miss) {
     moe_ctx* C = L->ctx;
     int nb = 0;
     if (with_bypass && r.bypass > 0) {
@@ -288,10 +337,12 @@ moe_status issue_miss_copies(moe_layer* L, const StepResult& r, bool with_bypass
         if (st != MOE_OK) return st;
         CUDA_TRY(cudaStreamWaitEvent(C->copy_stream, C->staging_free, 0));
     }
+    if (ready_of_miss) ready_of_miss->assign(r.miss_experts.size(), -1);
     for (size_t i = 0; i < r.miss_experts.size(); ++i) {
         const int e = r.miss_experts[i], slot = r.miss_slots[i];
         if (slot < 0 && !with_bypass) continue;
         uint8_t* dst = slot >= 0 ? L->d_slots + (size_t)slot * L->ebytes : C->staging + (size_t)nb * L->ebytes;
+        const int flag = slot >= 0 ? slot : L->S + nb;
         bool fail = false;
         if (C->fail_copy_at >= 0 && C->copies_issued == C->fail_copy_at) {
             fail = true;
@@ -301,129 +352,92 @@ moe_status issue_miss_copies(moe_layer* L, const StepResult& r, bool with_bypass
         cudaError_t ce = fail ? cudaErrorUnknown
                               : cudaMemcpyAsync(dst, L->h_pool + (size_t)e * L->ebytes, L->ebytes,
                                                 cudaMemcpyHostToDevice, C->copy_stream);
-        if (ce != cudaSuccess) {
+        CUresult cr = CUDA_SUCCESS;
+        if (ce == cudaSuccess)
+            cr = C->write_value((CUstream)C->copy_stream, (CUdeviceptr)(L->d_ready + flag), epoch, 0);
+        if (ce != cudaSuccess || cr != CUDA_SUCCESS) {
             if (!fail) cudaGetLastError();
-            // empty every slot this step filled but whose copy is not known good
             for (size_t j = i; j < r.miss_experts.size(); ++j)
                 if (r.miss_slots[j] >= 0) L->cache.evict(r.miss_slots[j]);
             return set_error(MOE_ECOPY, "copy of expert %d (slot %d) failed: %s", e, slot,
-                             fail ? "injected failure" : cudaGetErrorString(ce));
+                             fail ? "injected failure" : ce != cudaSuccess ? cudaGetErrorString(ce) : "flag write");
         }
         L->stats.bytes_h2d += L->ebytes;
-        if (slot >= 0)
-            CUDA_TRY(cudaEventRecord(L->slot_ready[slot], C->copy_stream));
-        else
-            ++nb;
+        if (ready_of_miss) (*ready_of_miss)[i] = flag;
+        if (slot < 0) ++nb;
     }
-    if (nb > 0) CUDA_TRY(cudaEventRecord(L->ev_bypass, C->copy_stream));
-    if (n_bypass_staged) *n_bypass_staged = nb;
     return MOE_OK;
-}
-
-template <class List>
-bool add_item(List& l, const uint8_t* w, const int32_t* perm, int b, int e_) {
-    constexpr int MAXI = sizeof(l.w) / sizeof(l.w[0]);
-    constexpr int MAXP = sizeof(l.pair) / sizeof(l.pair[0]);
-    if (l.n_items >= MAXI || l.begin[l.n_items] + (e_ - b) > MAXP) return false;
-    l.w[l.n_items] = w;
-    int p = l.begin[l.n_items];
-    for (int i = b; i < e_; ++i) l.pair[p++] = (int16_t)perm[i];
-    ++l.n_items;
-    l.begin[l.n_items] = (int16_t)p;
-    return true;
 }
 
 struct Item {
     const uint8_t* w;
-    int b, e;  // pair range in perm
+    int b, e;              // pair range in perm, or pair ids themselves when perm is null
+    const int32_t* perm;
+    int ready;             // ready-flag index, -1 if resident
+    int fam;               // 0 shared expert, 1 routed expert
 };
 
-// Gate/up and down for a set of experts, packed into as few work lists as fit.
 template <class List>
-moe_status launch_items(moe_layer* L, const uint16_t* x, const std::vector<Item>& items, cudaStream_t s) {
-    moe_ctx* C = L->ctx;
+bool add_item(List& l, const Item& x) {
+    constexpr int MAXI = sizeof(l.item) / sizeof(l.item[0]);
+    constexpr int MAXP = sizeof(l.pair) / sizeof(l.pair[0]);
+    if (l.n_items >= MAXI) return false;
+    int pb = l.n_items ? l.item[l.n_items - 1].pb + l.item[l.n_items - 1].np : 0;
+    if (pb + (x.e - x.b) > MAXP) return false;
+    FfnItem& it = l.item[l.n_items++];
+    it.w = x.w;
+    it.pb = (int16_t)pb;
+    it.np = (int16_t)(x.e - x.b);
+    it.ready = (int16_t)x.ready;
+    it.pad = 0;
+    for (int i = x.b; i < x.e; ++i) l.pair[pb++] = x.perm ? (int16_t)x.perm[i] : (int16_t)i;
+    return true;
+}
+
+// Fused FFN launches covering `items` (family 0 first); the combine runs in the last.
+template <class List>
+moe_status launch_items(moe_layer* L, const std::vector<Item>& items, FfnArgs a, cudaStream_t s) {
     const moe_shapes& sh = L->sh;
-    const double egu = 2 * qbytes(sh.d_ff, sh.d_model), edn = qbytes(sh.d_model, sh.d_ff);
+    const int combine = a.combine;
     size_t i = 0;
     while (i < items.size()) {
         List l{};
-        l.begin[0] = 0;
-        while (i < items.size() && add_item(l, items[i].w, L->perm.data(), items[i].b, items[i].e)) ++i;
-        if (l.n_items == 0) return set_error(MOE_EINVAL, "expert with too many pairs for one work list");
-        const double np = l.begin[l.n_items];
-        {
-            Prof p(C, s, K_ROUTED_GU, l.n_items * egu, 2.0 * np * 2 * sh.d_ff * sh.d_model);
-            CUDA_TRY(launch_gateup(x, sh.d_model, sh.d_ff, sh.act, sh.top_k, l, L->d_h, s));
+        l.epoch = L->epoch;
+        size_t j = i;
+        int n_fam[2] = {0, 0};
+        double bytes = 0, flops = 0;
+        while (j < items.size() && add_item(l, items[j])) {
+            ++n_fam[items[j].fam];
+            bytes += items[j].fam == 0 ? (double)L->shared_bytes : (double)L->ebytes;
+            flops += 6.0 * (items[j].e - items[j].b) * sh.d_model * (items[j].fam == 0 ? sh.d_ff_shared : sh.d_ff);
+            ++j;
         }
+        if (j == i) return set_error(MOE_EINVAL, "an expert with too many pairs for one work list");
+        a.fam[0].n_items = n_fam[0];
+        a.fam[1].n_items = n_fam[1];
+        a.combine = (j == items.size()) ? combine : 0;
         {
-            Prof p(C, s, K_ROUTED_DN, l.n_items * edn, 2.0 * np * sh.d_ff * sh.d_model);
-            CUDA_TRY(launch_down(L->d_h, sh.d_ff, sh.d_model, l, L->d_o, s));
+            Prof p(L->ctx, s, K_FFN, bytes, flops);
+            CUDA_TRY(launch_ffn(a, l, s));
         }
-        L->stats.bytes_resident += (uint64_t)(l.n_items * (egu + edn));
+        L->stats.bytes_resident += (uint64_t)bytes;
+        i = j;
     }
     return MOE_OK;
 }
 
-moe_status launch_items_any(moe_layer* L, const uint16_t* x, const std::vector<Item>& items, cudaStream_t s) {
+moe_status launch_items_any(moe_layer* L, const std::vector<Item>& items, const FfnArgs& a, cudaStream_t s) {
     if (items.empty()) return MOE_OK;
     int pairs = 0;
     for (const Item& it : items) pairs += it.e - it.b;
-    if ((int)items.size() <= 16 && pairs <= 64) return launch_items<SmallList>(L, x, items, s);
-    return launch_items<LargeList>(L, x, items, s);
-}
-
-// Routed experts: hits first, then (after the ready events) misses.
-moe_status run_routed(moe_layer* L, const uint16_t* x, int T, int nb_staged, cudaStream_t s) {
-    moe_ctx* C = L->ctx;
-    const moe_shapes& sh = L->sh;
-    const int npairs = T * sh.top_k;
-    L->offsets.resize(sh.n_experts + 1);
-    L->perm.resize(npairs);
-    group_pairs(L->h_ids, npairs, sh.n_experts, L->offsets.data(), L->perm.data());
-    std::vector<Item> hit, miss;
-    std::vector<int> miss_slots;
-    int bypass_i = 0;
-    size_t mi = 0;
-    for (int e : L->step.distinct) {
-        int slot = -1;
-        bool is_miss = false;
-        while (mi < L->step.miss_experts.size() && L->step.miss_experts[mi] < e) ++mi;
-        if (mi < L->step.miss_experts.size() && L->step.miss_experts[mi] == e) {
-            is_miss = true;
-            slot = L->step.miss_slots[mi];
-        } else {
-            slot = L->cache.slot_of(e);
-        }
-        const uint8_t* w;
-        if (slot >= 0) {
-            w = L->d_slots + (size_t)slot * L->ebytes;
-        } else {
-            if (bypass_i >= nb_staged) return set_error(MOE_ESTATE, "bypassed expert %d has no staging", e);
-            w = C->staging + (size_t)bypass_i * L->ebytes;
-            ++bypass_i;
-        }
-        (is_miss ? miss : hit).push_back(Item{w, L->offsets[e], L->offsets[e + 1]});
-        if (is_miss && slot >= 0) miss_slots.push_back(slot);
-    }
-    moe_status st = launch_items_any(L, x, hit, s);
-    if (st != MOE_OK) return st;
-    if (!miss.empty()) {
-        WaitRec w{C->timing_event(), C->timing_event()};
-        CUDA_TRY(cudaEventRecord(w.a, s));
-        for (int slot : miss_slots) CUDA_TRY(cudaStreamWaitEvent(s, L->slot_ready[slot], 0));
-        if (nb_staged > 0) CUDA_TRY(cudaStreamWaitEvent(s, L->ev_bypass, 0));
-        CUDA_TRY(cudaEventRecord(w.b, s));
-        L->waits.push_back(w);
-        st = launch_items_any(L, x, miss, s);
-        if (st != MOE_OK) return st;
-    }
-    return MOE_OK;
+    if ((int)items.size() <= 24 && pairs <= 96) return launch_items<FfnSmall>(L, items, a, s);
+    return launch_items<FfnLarge>(L, items, a, s);
 }
 
 moe_status route_into(moe_layer* L, const uint16_t* x, int T, const float* zbias, int32_t* ids, float* gates,
-                      cudaStream_t s) {
+                      bool publish, cudaStream_t s) {
     RouterParams p{x, T, L->sh.d_model, L->sh.n_experts, L->sh.top_k, L->d_router_codes, L->d_router_sb, zbias,
-                   L->d_logits, L->d_counters, ids, gates};
+                   L->d_logits, L->d_rcount, ids, gates, publish ? L->h_pub_dev : nullptr, L->seq};
     Prof pr(L->ctx, s, K_ROUTER, (double)L->router_bytes + 2.0 * T * L->sh.d_model,
             2.0 * T * L->sh.n_experts * L->sh.d_model);
     CUDA_TRY(launch_router(p, s));
@@ -431,29 +445,94 @@ moe_status route_into(moe_layer* L, const uint16_t* x, int T, const float* zbias
     return MOE_OK;
 }
 
-template <class List>
-moe_status shared_expert_t(moe_layer* L, const uint16_t* x, int T, float* y, cudaStream_t s) {
+// The experts of one call: the shared expert on every token (family 0), then
+// the routed experts - hits first, then misses in miss order - and the
+// combine y = shared + sum_r g_r o_r.
+moe_status run_experts(moe_layer* L, const uint16_t* x, int T, float* y, const std::vector<int>& ready_of_miss,
+                       cudaEvent_t copies_done, cudaStream_t s) {
+    moe_ctx* C = L->ctx;
     const moe_shapes& sh = L->sh;
-    List l{};
-    l.n_items = 1;
-    l.w[0] = L->d_shared;
-    l.begin[0] = 0;
-    l.begin[1] = (int16_t)T;
-    for (int t = 0; t < T; ++t) l.pair[t] = (int16_t)t;
-    {
-        Prof p(L->ctx, s, K_SHARED_GU, 2 * qbytes(sh.d_ff_shared, sh.d_model), 4.0 * T * sh.d_ff_shared * sh.d_model);
-        CUDA_TRY(launch_gateup(x, sh.d_model, sh.d_ff_shared, sh.act, 1, l, L->d_hs, s));
+    const int npairs = T * sh.top_k;
+    L->offsets.resize(sh.n_experts + 1);
+    L->perm.resize(npairs);
+    group_pairs(L->h_ids.data(), npairs, sh.n_experts, L->offsets.data(), L->perm.data());
+    std::vector<Item> items, miss;
+    for (int t0 = 0; t0 < T; t0 += kFfnMaxNT)
+        items.push_back(Item{L->d_shared, t0, std::min(T, t0 + kFfnMaxNT), nullptr, -1, 0});
+    int nb = 0;
+    size_t mi = 0;
+    for (int e : L->step.distinct) {
+        while (mi < L->step.miss_experts.size() && L->step.miss_experts[mi] < e) ++mi;
+        const bool is_miss = mi < L->step.miss_experts.size() && L->step.miss_experts[mi] == e;
+        const int slot = is_miss ? L->step.miss_slots[mi] : L->cache.slot_of(e);
+        const uint8_t* w;
+        if (slot >= 0) {
+            w = L->d_slots + (size_t)slot * L->ebytes;
+        } else {
+            w = C->staging + (size_t)nb * L->ebytes;
+            ++nb;
+        }
+        const int ready = is_miss ? ready_of_miss[mi] : -1;
+        for (int b = L->offsets[e]; b < L->offsets[e + 1]; b += kFfnMaxNT)
+            (is_miss ? miss : items)
+                .push_back(Item{w, b, std::min(b + kFfnMaxNT, (int)L->offsets[e + 1]), L->perm.data(), ready, 1});
     }
-    {
-        Prof p(L->ctx, s, K_SHARED_DN, qbytes(sh.d_model, sh.d_ff_shared), 2.0 * T * sh.d_ff_shared * sh.d_model);
-        CUDA_TRY(launch_down(L->d_hs, sh.d_ff_shared, sh.d_model, l, y, s));
+    items.insert(items.end(), miss.begin(), miss.end());
+    FfnArgs a{};
+    a.x = x;
+    a.d = sh.d_model;
+    a.act = sh.act;
+    a.fam[0] = FfnFam{0, sh.d_ff_shared, 1, 1, 1, 1, L->d_hs, L->d_os};
+    a.fam[1] = FfnFam{0, sh.d_ff, sh.top_k, 1, 1, 1, L->d_h, L->d_o};
+    a.gates = L->d_gates;
+    a.combine_base = L->d_os;
+    a.y = y;
+    a.T = T;
+    a.k = sh.top_k;
+    a.combine = 1;
+    a.partials = L->d_part;
+    a.partial_floats = L->part_floats;
+    a.counters = L->d_fcount;
+    a.n_counters = L->n_fcount;
+    a.ready = L->d_ready;
+    a.err = C->err_dev;
+    a.trace = nullptr;
+    WaitRec w{};
+    if (copies_done) {
+        w.ffn_start = C->timing_event();
+        w.copies_done = copies_done;
+        CUDA_TRY(cudaEventRecord(w.ffn_start, s));
     }
-    L->stats.bytes_resident += L->shared_bytes;
-    return MOE_OK;
+    moe_status st = launch_items_any(L, items, a, s);
+    if (copies_done) L->waits.push_back(w);
+    return st;
 }
 
-moe_status shared_expert(moe_layer* L, const uint16_t* x, int T, float* y, cudaStream_t s) {
-    return T <= 64 ? shared_expert_t<SmallList>(L, x, T, y, s) : shared_expert_t<LargeList>(L, x, T, y, s);
+// Wait on the host until the router of the current call has published all
+// n ids (each word carries the call number in its high half).
+moe_status wait_published(moe_layer* L, int n) {
+    volatile unsigned long long* pub = L->h_pub;
+    const auto t0 = std::chrono::steady_clock::now();
+    int done = 0;
+    for (uint32_t i = 0;; ++i) {
+        while (done < n) {
+            const unsigned long long v = pub[done];
+            if ((uint32_t)(v >> 32) != L->seq) break;
+            L->h_ids[done] = (int32_t)(uint32_t)v;
+            ++done;
+        }
+        if (done == n) return MOE_OK;
+        if ((i & 1023) == 1023) {
+            const double el = std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count();
+            if (el > kHostWaitLimitS) return set_error(MOE_ETIMEOUT, "routing was not published within %.0f s", el);
+            cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return set_error(MOE_ECUDA, "while waiting for routing: %s", cudaGetErrorString(e));
+        }
+    }
+}
+
+double us_since(std::chrono::steady_clock::time_point t) {
+    return std::chrono::duration<double, std::micro>(std::chrono::steady_clock::now() - t).count();
 }
 
 // One call of at most kPrefillChunk tokens.
@@ -462,33 +541,49 @@ moe_status forward_chunk(moe_layer* L, const uint16_t* x, int T, const float* zb
     moe_ctx* C = L->ctx;
     const moe_shapes& sh = L->sh;
     const int npairs = T * sh.top_k;
+    auto t0 = std::chrono::steady_clock::now();
     CUDA_TRY(cudaStreamWaitEvent(s, L->ev_done, 0));
-    moe_status st = route_into(L, x, T, zbias, L->d_ids, L->d_gates, s);
+    CUDA_TRY(cudaStreamWaitEvent(s, L->ev_pending, 0));
+    if (L->err_generation != C->err_generation) {
+        // an earlier kernel abandoned a wait: restore the all-zero counters
+        CUDA_TRY(cudaMemsetAsync(L->d_fcount, 0, sizeof(unsigned) * L->n_fcount, s));
+        CUDA_TRY(cudaMemsetAsync(L->d_rcount, 0, sizeof(unsigned) * ((L->cap_T + 7) / 8), s));
+        L->err_generation = C->err_generation;
+    }
+    ++L->seq;
+    moe_status st = route_into(L, x, T, zbias, L->d_ids, L->d_gates, true, s);
     if (st != MOE_OK) return st;
-    CUDA_TRY(cudaMemcpyAsync(L->h_ids, L->d_ids, sizeof(int32_t) * npairs, cudaMemcpyDeviceToHost, s));
-    CUDA_TRY(cudaEventRecord(L->ev_ids, s));
-    st = shared_expert(L, x, T, y, s);  // overlaps the host step and the miss copies
+    L->stats.host_issue_us += us_since(t0);
+    t0 = std::chrono::steady_clock::now();
+    st = wait_published(L, npairs);
+    L->stats.host_wait_us += us_since(t0);
     if (st != MOE_OK) return st;
-    CUDA_TRY(cudaEventSynchronize(L->ev_ids));
-    if (!L->cache.step(L->h_ids, npairs, L->step)) return set_error(MOE_ESTATE, "router produced an invalid id");
+    t0 = std::chrono::steady_clock::now();
+    st = check_err_word(C);
+    if (st != MOE_OK) return st;
+    if (!L->cache.step(L->h_ids.data(), npairs, L->step))
+        return set_error(MOE_ESTATE, "router produced an invalid id");
     L->stats.steps += 1;
     L->stats.hits += L->step.hits;
     L->stats.misses += L->step.miss_experts.size();
     L->stats.bypass += L->step.bypass;
-    int nb = 0;
-    st = issue_miss_copies(L, L->step, true, &nb);
+    const uint32_t epoch = ++L->epoch;
+    std::vector<int> ready_of_miss;
+    st = issue_miss_copies(L, L->step, true, epoch, &ready_of_miss);
     if (st != MOE_OK) return st;
-    st = run_routed(L, x, T, nb, s);
-    if (st != MOE_OK) return st;
-    {
-        Prof p(C, s, K_COMBINE, 4.0 * npairs * sh.d_model + 8.0 * T * sh.d_model, 2.0 * npairs * sh.d_model);
-        CUDA_TRY(launch_combine(L->d_o, L->d_gates, T, sh.top_k, sh.d_model, y, s));
+    cudaEvent_t copies_done = nullptr;
+    if (!L->step.miss_experts.empty()) {
+        copies_done = C->timing_event();
+        CUDA_TRY(cudaEventRecord(copies_done, C->copy_stream));
     }
+    st = run_experts(L, x, T, y, ready_of_miss, copies_done, s);
+    if (st != MOE_OK) return st;
     if (ids_out) CUDA_TRY(cudaMemcpyAsync(ids_out, L->d_ids, sizeof(int32_t) * npairs, cudaMemcpyDeviceToDevice, s));
     if (gates_out)
         CUDA_TRY(cudaMemcpyAsync(gates_out, L->d_gates, sizeof(float) * npairs, cudaMemcpyDeviceToDevice, s));
     CUDA_TRY(cudaEventRecord(L->ev_done, s));
-    if (nb > 0) CUDA_TRY(cudaEventRecord(C->staging_free, s));
+    if (L->step.bypass > 0) CUDA_TRY(cudaEventRecord(C->staging_free, s));
+    L->stats.host_issue_us += us_since(t0);
     return MOE_OK;
 }
 
@@ -523,12 +618,24 @@ extern "C" moe_status moe_ctx_create(int device, moe_ctx** out) {
     moe_ctx* C = new (std::nothrow) moe_ctx();
     if (!C) return set_error(MOE_ENOMEM, "out of host memory");
     C->device = device;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+        cudaGetLastError();
+        delete C;
+        return set_error(MOE_ECUDA, "cuStreamWriteValue32 is not available");
+    }
+    C->write_value = reinterpret_cast<WriteValue32>(fn);
     if (cudaStreamCreateWithFlags(&C->copy_stream, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaEventCreateWithFlags(&C->staging_free, cudaEventDisableTiming) != cudaSuccess) {
+        cudaEventCreateWithFlags(&C->staging_free, cudaEventDisableTiming) != cudaSuccess ||
+        cudaHostAlloc(&C->err_host, sizeof(unsigned), cudaHostAllocMapped) != cudaSuccess ||
+        cudaHostGetDevicePointer(&C->err_dev, C->err_host, 0) != cudaSuccess) {
         cudaGetLastError();
         delete C;
         return set_error(MOE_ECUDA, "stream/event creation failed");
     }
+    *C->err_host = 0;
     *out = C;
     return MOE_OK;
 }
@@ -540,6 +647,7 @@ extern "C" void moe_ctx_destroy(moe_ctx* C) {
     drain_prof(C);
     for (cudaEvent_t e : C->timing_pool) cudaEventDestroy(e);
     cudaFree(C->staging);
+    cudaFreeHost(C->err_host);
     cudaEventDestroy(C->staging_free);
     cudaStreamDestroy(C->copy_stream);
     delete C;
@@ -561,11 +669,10 @@ extern "C" void moe_layer_destroy(moe_layer* L) {
     cudaFree(L->d_router_sb);
     cudaFree(L->d_shared);
     cudaFree(L->d_slots);
+    cudaFree(L->d_ready);
     cudaFreeHost(L->h_pool);
-    for (cudaEvent_t e : L->slot_ready) cudaEventDestroy(e);
-    if (L->ev_ids) cudaEventDestroy(L->ev_ids);
     if (L->ev_done) cudaEventDestroy(L->ev_done);
-    if (L->ev_bypass) cudaEventDestroy(L->ev_bypass);
+    if (L->ev_pending) cudaEventDestroy(L->ev_pending);
     delete L;
 }
 
@@ -588,10 +695,13 @@ extern "C" moe_status moe_layer_create(moe_ctx* C, const moe_shapes* s, const mo
     L->ebytes = expert_blob_bytes(s->d_model, s->d_ff);
     L->shared_bytes = expert_blob_bytes(s->d_model, s->d_ff_shared);
     L->router_bytes = (size_t)s->n_experts * s->d_model + (size_t)s->n_experts * (s->d_model / 64) * 4;
+    const size_t n_flags = (size_t)slots + s->n_experts;
     bool ok = cudaMalloc(&L->d_router_codes, (size_t)s->n_experts * s->d_model) == cudaSuccess &&
               cudaMalloc(&L->d_router_sb, (size_t)s->n_experts * (s->d_model / 64) * 4) == cudaSuccess &&
               cudaMalloc(&L->d_shared, L->shared_bytes) == cudaSuccess &&
               cudaMalloc(&L->d_slots, (size_t)slots * L->ebytes) == cudaSuccess &&
+              cudaMalloc(&L->d_ready, n_flags * sizeof(uint32_t)) == cudaSuccess &&
+              cudaMemset(L->d_ready, 0, n_flags * sizeof(uint32_t)) == cudaSuccess &&
               cudaHostAlloc(&L->h_pool, (size_t)s->n_experts * L->ebytes, cudaHostAllocDefault) == cudaSuccess;
     if (!ok) {
         cudaGetLastError();
@@ -599,12 +709,8 @@ extern "C" moe_status moe_layer_create(moe_ctx* C, const moe_shapes* s, const mo
         return set_error(MOE_ENOMEM, "layer allocation failed (%zu B pinned pool, %zu B slots)",
                          (size_t)s->n_experts * L->ebytes, (size_t)slots * L->ebytes);
     }
-    L->slot_ready.resize(slots, nullptr);
-    for (int i = 0; i < slots; ++i)
-        if (cudaEventCreateWithFlags(&L->slot_ready[i], cudaEventDisableTiming) != cudaSuccess) ok = false;
-    ok = ok && cudaEventCreateWithFlags(&L->ev_ids, cudaEventDisableTiming) == cudaSuccess &&
-         cudaEventCreateWithFlags(&L->ev_done, cudaEventDisableTiming) == cudaSuccess &&
-         cudaEventCreateWithFlags(&L->ev_bypass, cudaEventDisableTiming) == cudaSuccess;
+    ok = cudaEventCreateWithFlags(&L->ev_done, cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&L->ev_pending, cudaEventDisableTiming) == cudaSuccess;
     if (!ok) {
         cudaGetLastError();
         moe_layer_destroy(L);
@@ -623,7 +729,7 @@ extern "C" moe_status moe_layer_set_weights(moe_layer* L, const moe_host_weights
     CUDA_TRY(cudaSetDevice(L->ctx->device));
     const moe_shapes& s = L->sh;
     const int d = s.d_model, I = s.d_ff, Is = s.d_ff_shared, E = s.n_experts;
-    if (L->ev_done) CUDA_TRY(cudaEventSynchronize(L->ev_done));
+    CUDA_TRY(cudaEventSynchronize(L->ev_done));
     CUDA_TRY(cudaStreamSynchronize(L->ctx->copy_stream));
     // router: codes as they are, (scale, bias) interleaved
     std::vector<uint32_t> sb((size_t)E * (d / 64));
@@ -671,7 +777,7 @@ extern "C" moe_status moe_route(moe_layer* L, const void* x, int32_t T, const fl
         if (st != MOE_OK) return st;
         CUDA_TRY(cudaStreamWaitEvent(s, L->ev_done, 0));
         st = route_into(L, static_cast<const uint16_t*>(x) + (size_t)t0 * L->sh.d_model, tc, zbias,
-                        ids + (size_t)t0 * L->sh.top_k, gates + (size_t)t0 * L->sh.top_k, s);
+                        ids + (size_t)t0 * L->sh.top_k, gates + (size_t)t0 * L->sh.top_k, false, s);
         if (st != MOE_OK) return st;
         CUDA_TRY(cudaEventRecord(L->ev_done, s));
     }
@@ -690,7 +796,9 @@ extern "C" moe_status moe_cache_step(moe_layer* L, const int32_t* ids, int32_t n
     L->stats.bypass += L->step.bypass;
     // slots being overwritten may still be read by this layer's earlier kernels
     CUDA_TRY(cudaStreamWaitEvent(L->ctx->copy_stream, L->ev_done, 0));
-    moe_status st = issue_miss_copies(L, L->step, false, nullptr);
+    moe_status st = issue_miss_copies(L, L->step, false, ++L->epoch, nullptr);
+    // the next forward treats these experts as resident: it waits for the copies first
+    cudaError_t e = cudaEventRecord(L->ev_pending, L->ctx->copy_stream);
     if (slot_of)
         for (int i = 0; i < n_ids; ++i) slot_of[i] = L->cache.slot_of(ids[i]);
     for (size_t i = 0; i < L->step.miss_experts.size(); ++i) {
@@ -698,6 +806,7 @@ extern "C" moe_status moe_cache_step(moe_layer* L, const int32_t* ids, int32_t n
         if (miss_slots) miss_slots[i] = L->step.miss_slots[i];
     }
     if (n_miss) *n_miss = (int32_t)L->step.miss_experts.size();
+    if (st == MOE_OK && e != cudaSuccess) return set_error(MOE_ECUDA, "event record failed: %s", cudaGetErrorString(e));
     return st;
 }
 
@@ -771,6 +880,12 @@ extern "C" moe_status moe_ctx_reset_kernel_times(moe_ctx* C) {
     cudaSetDevice(C->device);
     drain_prof(C);
     for (auto& a : C->acc) a = moe_ctx::Acc{};
+    return MOE_OK;
+}
+
+extern "C" moe_status moe_ctx_launches(moe_ctx* C, uint64_t* out) {
+    if (!C || !out) return set_error(MOE_EINVAL, "moe_ctx_launches: bad arguments");
+    *out = C->launches;
     return MOE_OK;
 }
 

@@ -80,21 +80,7 @@ MOE_HD inline size_t expert_blob_bytes(int d, int inter) { return 2 * qmat_bytes
 // Repack one canonical matrix into the tiled blob format at dst.
 void repack_qmatrix(const moe_qmatrix& m, int N, int K, uint8_t* dst);
 
-// ---- kernel work lists -------------------------------------------------------
-//
-// A list of distinct experts ("items") and, per item, the (token, rank) pairs
-// it serves. Pair p reads input row p / x_div (x_div is a launch argument:
-// k for the routed gate/up, 1 otherwise) and writes output row p.
-
-template <int MAXI, int MAXP>
-struct WorkList {
-    int n_items;
-    const uint8_t* w[MAXI];   // expert blob base (slot, staging or shared)
-    int16_t begin[MAXI + 1];  // pair ranges within pair[]
-    int16_t pair[MAXP];
-};
-using SmallList = WorkList<16, 64>;
-using LargeList = WorkList<256, 1024>;
+// ---- router -----------------------------------------------------------------
 
 struct RouterParams {
     const uint16_t* x;  // [T][d] bf16
@@ -103,23 +89,90 @@ struct RouterParams {
     const uint32_t* sb;    // [E][d/64] (scale | bias << 16)
     const float* zbias;    // [E] or null
     float* logits;         // scratch [T][E]
-    unsigned* counters;    // scratch, one per token block, zero between launches
-    int32_t* ids;          // [T][k]
-    float* gates;          // [T][k]
+    unsigned* counters;    // scratch, ceil(T/8) entries, zero between launches
+    int32_t* ids;          // [T][k] device
+    float* gates;          // [T][k] device
+    unsigned long long* host_ids;  // [T][k] mapped pinned host memory (seq << 32 | id), or null
+    uint32_t seq;
 };
 
 cudaError_t launch_router(const RouterParams& p, cudaStream_t s);
 
-// h[pair][inter] = act(Wg x) * (Wu x) for every pair of every item.
-template <class L>
-cudaError_t launch_gateup(const uint16_t* x, int d, int inter, int act, int x_div, const L& list, float* h,
-                          cudaStream_t s);
-
-// out[pair][d] = Wd h[pair] for every pair of every item (down region of the blob).
-template <class L>
-cudaError_t launch_down(const float* h, int inter, int d, const L& list, float* out, cudaStream_t s);
-
 // y[t][n] += sum_{r<k} gates[t][r] * o[t*k + r][n], added in rank order.
 cudaError_t launch_combine(const float* o, const float* gates, int T, int k, int d, float* y, cudaStream_t s);
+
+// ---- fused expert FFN ----------------------------------------------------------
+//
+// A list of expert "items", each with at most kFfnMaxNT (token, rank) pairs.
+// Items come in two families, family 0 first: the shared expert (its pairs
+// are token indices) and the routed experts (pair p = t * k + r). Pair p of
+// family f reads x row p / x_div and writes row p of the family's h and out.
+// An item whose bytes are still being copied names a ready flag (index into
+// `ready`) that must reach the list's epoch before its weights are read; -1
+// means resident.
+
+constexpr int kFfnMaxNT = 8;
+constexpr int kFfnFams = 2;
+
+struct FfnItem {
+    const uint8_t* w;  // expert blob: gate | up | down in the tiled layout
+    int16_t pb, np;    // pair range within pair[]
+    int16_t ready;     // ready-flag index, -1 if resident
+    int16_t pad;
+};
+
+template <int MAXI, int MAXP>
+struct FfnList {
+    int n_items;
+    uint32_t epoch;
+    FfnItem item[MAXI];
+    int16_t pair[MAXP];
+};
+using FfnSmall = FfnList<24, 96>;
+using FfnLarge = FfnList<256, 1024>;
+
+struct FfnFam {
+    int n_items;   // consecutive items of the list; family 0 first
+    int inter;     // intermediate size
+    int x_div;     // x row of pair p is p / x_div
+    int kc1, kc2;  // K-chunks per gate/up and per down tile (set by the launcher)
+    int tpj;       // down tiles per job (set by the launcher)
+    float* h;      // scratch [pairs][inter]
+    float* out;    // down outputs [pairs][d]
+};
+
+struct FfnArgs {
+    const uint16_t* x;  // [T][d] bf16
+    int d, act;
+    FfnFam fam[kFfnFams];
+    // combine (when `combine`): once every item of the launch has finished an
+    // output tile, y[t] = base[t] + sum_r gates[t][r] * fam[1].out[t*k + r],
+    // ranks in order, where base = combine_base (e.g. the shared expert's
+    // outputs) or, when that is null, y itself
+    const float* gates;  // [T][k]
+    const float* combine_base;
+    float* y;  // [T][d]
+    int T, k, combine;
+    float* partials;
+    size_t partial_floats;
+    unsigned* counters;  // zero between launches; each launch leaves them zero
+    size_t n_counters;
+    const uint32_t* ready;
+    unsigned* err;
+    int xs_stride;  // set by the launcher: inputs per row of the staged-input buffer
+    // optional diagnostics: per CTA, %globaltimer at kFfnTracePoints moments
+    // (start, first weights landed, last gate/up done, down inputs ready,
+    // last down done, end); null = off
+    unsigned long long* trace;
+};
+constexpr int kFfnTracePoints = 6;
+
+// Scratch a launch over these families may need (the launcher never exceeds it).
+size_t ffn_max_partial_floats(int d, int n_shared, int inter_shared, int n_routed, int inter_routed);
+size_t ffn_max_counters(int d, int n_shared, int inter_shared, int n_routed, int inter_routed);
+
+// One cooperative launch computing the FFN of every item (and the combine).
+template <class L>
+cudaError_t launch_ffn(const FfnArgs& a, const L& list, cudaStream_t s);
 
 }  // namespace moe

@@ -99,6 +99,8 @@ typedef struct {
     uint64_t bytes_h2d;      /* bytes copied host -> device for misses */
     uint64_t bytes_resident; /* weight bytes the layer's kernels read from HBM */
     double exposed_copy_us;
+    double host_wait_us;     /* host time spent waiting for the routing to be published */
+    double host_issue_us;    /* host time in the cache step, copy issue and kernel launches */
 } moe_stats;
 
 /* ---- context ------------------------------------------------------------ */
@@ -222,14 +224,19 @@ const char* moe_last_error(void);
 
 /* Per-kernel device time, measured with CUDA events recorded around each
  * launch on the launching stream while profiling is on (off by default; it
- * adds event records to the stream). kind: 0 router, 1 shared gate/up,
- * 2 shared down, 3 routed gate/up, 4 routed down, 5 combine, 6 grouped GEMM
- * gate/up, 7 grouped GEMM down. Returns launches, total milliseconds and
- * the algorithmic bytes and flops of those launches. Waits for the events. */
+ * adds event records to the stream). kind: 0 router + top-k, 1 expert FFN
+ * (shared and routed experts and the combine), 2 combine, 3 prefill grouped
+ * GEMM gate/up, 4 prefill grouped GEMM down. Returns launches, total
+ * milliseconds and the algorithmic bytes and flops of those launches. Waits
+ * for the events. */
 moe_status moe_ctx_set_profiling(moe_ctx* ctx, int32_t on);
 moe_status moe_ctx_kernel_times(moe_ctx* ctx, int32_t kind, uint64_t* launches, double* total_ms,
                                 double* bytes, double* flops);
 moe_status moe_ctx_reset_kernel_times(moe_ctx* ctx);
+
+/* Number of kernels the context's layers have launched since its creation
+ * (every launch is counted, profiling or not). */
+moe_status moe_ctx_launches(moe_ctx* ctx, uint64_t* out);
 
 /* Fault injection on the host, for tests of the failure path: the nth miss
  * copy issued from now on (0 = the next one) is reported as failed instead of

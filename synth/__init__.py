@@ -175,16 +175,20 @@ def expert_bytes(s: Shapes) -> int:
 # generation
 
 
-def _matrix(seed, layer, sub, t_codes, t_scale, n, k, bits=4, lo=0.005, hi=0.02, div=1.0, bias_mult=-8.0):
+def _matrix(seed, layer, sub, t_codes, t_scale, n, k, bits=4, lo=0.005, hi=0.02, div=1.0, bias_mult=-8.0,
+            out=None):
+    """One quantised matrix; writes into out=(codes, scale, bias) when given."""
     lib = _load()
+    if out is None:
+        codes = np.empty((n, k // 2 if bits == 4 else k), np.uint8)
+        scale = np.empty((n, k // 64), np.uint16)
+        bias = np.empty((n, k // 64), np.uint16)
+    else:
+        codes, scale, bias = out
     if bits == 4:
-        codes = np.empty((n, k // 2), np.uint8)
         lib.synth_codes_u4(key(seed, t_codes, layer, sub), n * k, _ptr(codes))
     else:
-        codes = np.empty((n, k), np.uint8)
         lib.synth_codes_u8(key(seed, t_codes, layer, sub), n * k, _ptr(codes))
-    scale = np.empty((n, k // 64), np.uint16)
-    bias = np.empty((n, k // 64), np.uint16)
     lib.synth_scale_bias_f16(key(seed, t_scale, layer, sub), n * (k // 64), lo, hi, div, bias_mult,
                              _ptr(scale), _ptr(bias))
     return codes, scale, bias
@@ -196,18 +200,19 @@ def router_weights(s: Shapes, layer: int, seed: int = 0):
                    div=float(np.sqrt(s.d_model)), bias_mult=-128.0)
 
 
-def ffn_weights(s: Shapes, layer: int, expert: int, seed: int = 0, shared: bool = False):
+def ffn_weights(s: Shapes, layer: int, expert: int, seed: int = 0, shared: bool = False, out=None):
     """One gated FFN: (gate, up, down) triples of (codes, scale, bias).
 
     Routed expert e uses stream sub-index e; the shared expert uses the shared
-    tensor ids with sub-index 0.
+    tensor ids with sub-index 0. out: optional preallocated triples to fill.
     """
     off = T_SHARED_OFFSET if shared else 0
     inter = s.d_ff_shared if shared else s.d_ff
     sub = 0 if shared else expert
-    g = _matrix(seed, layer, sub, T_GATE_CODES + off, T_GATE_SCALE + off, inter, s.d_model)
-    u = _matrix(seed, layer, sub, T_UP_CODES + off, T_UP_SCALE + off, inter, s.d_model)
-    dn = _matrix(seed, layer, sub, T_DOWN_CODES + off, T_DOWN_SCALE + off, s.d_model, inter)
+    o = out or (None, None, None)
+    g = _matrix(seed, layer, sub, T_GATE_CODES + off, T_GATE_SCALE + off, inter, s.d_model, out=o[0])
+    u = _matrix(seed, layer, sub, T_UP_CODES + off, T_UP_SCALE + off, inter, s.d_model, out=o[1])
+    dn = _matrix(seed, layer, sub, T_DOWN_CODES + off, T_DOWN_SCALE + off, s.d_model, inter, out=o[2])
     return g, u, dn
 
 
@@ -235,23 +240,28 @@ class LayerWeights:
                 (self.down_codes[e], self.down_scale[e], self.down_bias[e]))
 
 
-def layer_weights(s: Shapes, layer: int, seed: int = 0, threads: int | None = None) -> LayerWeights:
+def layer_weights(s: Shapes, layer: int, seed: int = 0, threads: int | None = None,
+                  reuse: LayerWeights | None = None) -> LayerWeights:
+    """All weights of one layer. reuse: a LayerWeights of the same shapes whose
+    routed arrays are overwritten (saves the allocation of ~1 GB per layer)."""
     E, d, I = s.n_experts, s.d_model, s.d_ff
-    gc = np.empty((E, I, d // 2), np.uint8)
-    gs = np.empty((E, I, d // 64), np.uint16)
-    gb = np.empty_like(gs)
-    uc = np.empty_like(gc)
-    us = np.empty_like(gs)
-    ub = np.empty_like(gs)
-    dc = np.empty((E, d, I // 2), np.uint8)
-    ds = np.empty((E, d, I // 64), np.uint16)
-    db = np.empty_like(ds)
+    if reuse is not None and reuse.shapes == s:
+        gc, gs, gb = reuse.gate_codes, reuse.gate_scale, reuse.gate_bias
+        uc, us, ub = reuse.up_codes, reuse.up_scale, reuse.up_bias
+        dc, ds, db = reuse.down_codes, reuse.down_scale, reuse.down_bias
+    else:
+        gc = np.empty((E, I, d // 2), np.uint8)
+        gs = np.empty((E, I, d // 64), np.uint16)
+        gb = np.empty_like(gs)
+        uc = np.empty_like(gc)
+        us = np.empty_like(gs)
+        ub = np.empty_like(gs)
+        dc = np.empty((E, d, I // 2), np.uint8)
+        ds = np.empty((E, d, I // 64), np.uint16)
+        db = np.empty_like(ds)
 
     def one(e):
-        (a, b, c), (p, q, r), (x, y, z) = ffn_weights(s, layer, e, seed)
-        gc[e], gs[e], gb[e] = a, b, c
-        uc[e], us[e], ub[e] = p, q, r
-        dc[e], ds[e], db[e] = x, y, z
+        ffn_weights(s, layer, e, seed, out=((gc[e], gs[e], gb[e]), (uc[e], us[e], ub[e]), (dc[e], ds[e], db[e])))
 
     nthreads = threads or min(32, os.cpu_count() or 1)
     if E > 1 and nthreads > 1:
