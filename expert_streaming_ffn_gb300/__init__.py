@@ -70,6 +70,7 @@ SIGNATURES = [
     ("moe_layer_set_weights", _i32, [_vp, _P(moe_host_weights)]),
     ("moe_expert_bytes", _sz, [_P(moe_shapes)]),
     ("moe_route", _i32, [_vp, _vp, _i32, _vp, _vp, _vp, _vp]),
+    ("moe_route_noalloc", _i32, [_vp, _vp, _i32, _vp, _vp, _vp, _vp]),
     ("moe_cache_step", _i32, [_vp, _vp, _i32, _vp, _vp, _vp, _vp]),
     ("moe_forward", _i32, [_vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp]),
     ("moe_layer_stats", _i32, [_vp, _P(moe_stats)]),
@@ -204,6 +205,13 @@ def moe_route(layer: int, x, top_k: int, zbias=None, ids=None, gates=None, strea
     _check(load().moe_route(layer, _dptr(x), T, _dptr(zbias), _dptr(ids), _dptr(gates), _stream(stream)),
            "moe_route")
     return ids, gates
+
+
+def moe_route_noalloc(layer: int, x, zbias, ids, gates, stream=None):
+    """moe_route into caller-provided CUDA buffers, with no allocation anywhere:
+    x bf16 [T][d], ids int32 [T][k], gates f32 [T][k] (T <= 64)."""
+    _check(load().moe_route_noalloc(layer, _dptr(x), x.shape[0], _dptr(zbias), _dptr(ids), _dptr(gates),
+                                    _stream(stream)), "moe_route_noalloc")
 
 
 def moe_cache_step(layer: int, ids) -> dict:

@@ -27,6 +27,7 @@
 
 #include <algorithm>
 #include <chrono>
+#include <mutex>
 #include <new>
 #include <thread>
 #include <vector>
@@ -892,5 +893,75 @@ extern "C" moe_status moe_ctx_launches(moe_ctx* C, uint64_t* out) {
 extern "C" moe_status moe_ctx_inject_copy_failure(moe_ctx* C, int64_t nth) {
     if (!C) return set_error(MOE_EINVAL, "ctx is NULL");
     C->fail_copy_at = nth < 0 ? -1 : C->copies_issued + nth;
+    return MOE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// moe_route_noalloc: the router with library-owned static scratch.
+//
+// For callers that cannot allocate: a decode loop on a fixed memory budget,
+// or one that cannot take the device-wide synchronisation of the cudaFree in
+// ensure_scratch's growth path. The scratch below is sized once at compile
+// time; the entry point never calls cudaMalloc, cudaFree or any routine that
+// allocates. Every layer on a device shares it, so overlapping calls race.
+
+namespace {
+
+constexpr int kNoAllocMaxT = 64;
+constexpr int kNoAllocLogits = 16384;                                // fp32 logits, T * n_experts
+constexpr int kNoAllocCounters = (kNoAllocMaxT + 7) / 8;            // one per block of 8 tokens
+constexpr int kNoAllocMaxDevices = 64;
+
+// Zero at load; the router's last block per token block puts its counter back to zero.
+static __device__ __align__(256) float g_noalloc_logits[kNoAllocLogits];
+static __device__ __align__(256) unsigned g_noalloc_counters[kNoAllocCounters];
+
+struct NoAllocScratch {
+    float* logits = nullptr;
+    unsigned* counters = nullptr;
+};
+std::mutex g_noalloc_mu;
+NoAllocScratch g_noalloc[kNoAllocMaxDevices];
+
+// Device addresses of the scratch on `device`, looked up once per device with
+// that device current.
+moe_status noalloc_scratch(int device, NoAllocScratch* out) {
+    if (device < 0 || device >= kNoAllocMaxDevices)
+        return set_error(MOE_EINVAL, "moe_route_noalloc: device %d out of [0, %d)", device, kNoAllocMaxDevices);
+    std::lock_guard<std::mutex> g(g_noalloc_mu);
+    NoAllocScratch& sc = g_noalloc[device];
+    if (!sc.logits) {
+        void* l = nullptr;
+        void* c = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&l, g_noalloc_logits);
+        if (e == cudaSuccess) e = cudaGetSymbolAddress(&c, g_noalloc_counters);
+        if (e != cudaSuccess)
+            return set_error(MOE_ECUDA, "moe_route_noalloc: scratch lookup failed: %s", cudaGetErrorString(e));
+        sc.logits = static_cast<float*>(l);
+        sc.counters = static_cast<unsigned*>(c);
+    }
+    *out = sc;
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" moe_status moe_route_noalloc(moe_layer* L, const void* x, int32_t T, const float* zbias, int32_t* ids,
+                                        float* gates, void* stream) {
+    if (!L || !x || !ids || !gates || T < 1) return set_error(MOE_EINVAL, "moe_route_noalloc: bad arguments");
+    if (!L->loaded) return set_error(MOE_ESTATE, "moe_route_noalloc before moe_layer_set_weights");
+    if (T > kNoAllocMaxT || (long)T * L->sh.n_experts > kNoAllocLogits)
+        return set_error(MOE_EINVAL,
+                         "moe_route_noalloc: T = %d with %d experts exceeds the static scratch "
+                         "(T <= %d and T * n_experts <= %d)",
+                         T, L->sh.n_experts, kNoAllocMaxT, kNoAllocLogits);
+    CUDA_TRY(cudaSetDevice(L->ctx->device));
+    NoAllocScratch sc;
+    moe_status st = noalloc_scratch(L->ctx->device, &sc);
+    if (st != MOE_OK) return st;
+    RouterParams p{static_cast<const uint16_t*>(x), T, L->sh.d_model, L->sh.n_experts, L->sh.top_k,
+                   L->d_router_codes, L->d_router_sb, zbias, sc.logits, sc.counters, ids, gates, nullptr, 0};
+    CUDA_TRY(launch_router(p, (cudaStream_t)stream));
+    ++L->ctx->launches;
     return MOE_OK;
 }

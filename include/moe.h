@@ -149,6 +149,30 @@ size_t moe_expert_bytes(const moe_shapes* shapes);
 moe_status moe_route(moe_layer* layer, const void* x_bf16, int32_t T, const float* zbias, int32_t* ids,
                      float* gates, void* stream);
 
+/* moe_route without any device allocation. The pages have no counterpart:
+ * this entry point exists for callers that must not allocate, such as a
+ * decode loop that holds a fixed memory budget, or one that cannot afford the
+ * device-wide synchronisation that a cudaFree inside moe_route's scratch
+ * growth would add. It computes exactly what moe_route computes, with the
+ * same kernel and the same fixed summation order, but its scratch (the fp32
+ * logits and the per-token-block arrival counters) lives in a statically
+ * sized device array of the library instead of the layer's own buffers.
+ * Limits: 1 <= T <= 64 and T * n_experts <= 16384 (64 KiB of fp32 logits);
+ * larger calls fail with MOE_EINVAL before anything is enqueued.
+ * Zero state: the counters must be zero when a call starts. They are zero
+ * when the library is loaded, and every call leaves them at zero.
+ * The first call on a device looks up the scratch's device address and
+ * sets the router kernel's shared-memory attribute, so make it before any
+ * stream capture. Later calls only enqueue the one router kernel.
+ * Overlapping calls race: the scratch is shared by every layer on a device,
+ * so two calls that may run at the same time (other streams, other threads)
+ * corrupt each other's logits. Calls ordered on one stream are safe.
+ * Arguments, layouts and outputs as for moe_route.
+ * Errors: MOE_EINVAL (bad arguments or over the limits), MOE_ESTATE (no
+ * weights), MOE_ECUDA (the set-up lookup or the launch failed). */
+moe_status moe_route_noalloc(moe_layer* layer, const void* x_bf16, int32_t T, const float* zbias, int32_t* ids,
+                             float* gates, void* stream);
+
 /* One expert-cache step over n_ids expert ids (host int32, duplicates
  * allowed): LFU/LRU lookup ([P1] §8.3 flow) in which distinct ids are taken
  * in ascending order; hits are counted (LFU: use_count += 1; LRU: stamped
