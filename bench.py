@@ -158,6 +158,24 @@ def gpu_bus_id(dev: int) -> str | None:
         return None
 
 
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu record, or None
+    when the kernel's source has changed since the counters were taken."""
+    import hashlib
+
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f).get(kernel)
+        if not rec:
+            return None
+        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != rec["source_sha256"]:
+                return None
+        return rec["dram_bytes_per_launch"]
+    except (OSError, ValueError, KeyError):
+        return None
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -381,7 +399,8 @@ def run_ours(args, world, rank, local):
         "resident_GB_per_token": resident / args.steps / 1e9,
         "hbm_GBs_all_kernels": all_bytes / (all_ms * 1e-3) / 1e9 if all_ms else None,
         "roofline": {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(name),
+                     "algorithmic_bytes_per_launch": by / n_l if n_l else None,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                      else "fallback 6.8 TB/s"},
         "kernels": kernels,
