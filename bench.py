@@ -414,8 +414,51 @@ def run_ours(args, world, rank, local):
     print(json.dumps(out), flush=True)
 
 
+def _prefill_pass(ctx, dev, stream, layers, xs, y):
+    """One pass of every layer's prompt (8 chunks of 128) with per-kernel events."""
+    import torch
+
+    import expert_streaming_ffn_gb300 as moe
+
+    moe.moe_ctx_set_profiling(ctx, True)
+    moe.moe_ctx_reset_kernel_times(ctx)
+    for h in layers:
+        moe.moe_layer_reset_stats(h)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    ev0.record(stream)
+    for h, x in zip(layers, xs):
+        moe.moe_forward(h, x, y=y)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    kt = moe.moe_ctx_kernel_times(ctx)
+    moe.moe_ctx_set_profiling(ctx, False)
+    return ev0.elapsed_time(ev1), kt, [moe.moe_layer_stats(h) for h in layers]
+
+
+def _gemm_summary(kt, peaks):
+    out = {}
+    for k in ("gemm_gateup", "gemm_down"):
+        n, ms, by, fl = kt[k]
+        if n == 0 or ms <= 0:
+            continue
+        tf = fl / (ms * 1e-3) / 1e12
+        gbs = by / (ms * 1e-3) / 1e9
+        out[k] = {"launches": n, "ms": round(ms, 4), "TFLOPs": round(tf, 2), "GB_s": round(gbs, 1),
+                  "frac_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+                  "frac_hbm_peak": round(gbs / peaks["hbm_gbs"], 4)}
+    return out
+
+
 def run_prefill(args, ctx, dev, stream, seed):
-    """prefill_2816: 8 chunks of 128 tokens per layer on a few fresh layers."""
+    """prefill_2816: a 1024-token prompt as 8 chunks of 128 tokens per layer.
+
+    Three runs: (1) streaming, as configured (16-slot LFU, misses copied from
+    pinned host memory); (2) all-resident (256 slots, prompt run once to fill
+    the slots, then timed), which times the grouped GEMMs on weights already in
+    HBM; (3) the shared-expert GEMM alone (a layer of the same d and shared
+    expert with a single 64-wide routed expert), the dense contraction the
+    tensor-core roofline applies to."""
     import torch
 
     import expert_streaming_ffn_gb300 as moe
@@ -425,44 +468,35 @@ def run_prefill(args, ctx, dev, stream, seed):
     s = wl.shapes
     P = args.prefill_layers
     prompt = wl.tokens * wl.steps  # 1024
-    layers = []
-    w = None
-    for l in range(P):
-        w = synth.layer_weights(s, l, seed, reuse=w)
-        h = moe.moe_layer_create(ctx, s, wl.cache_slots, wl.policy)
-        moe.moe_layer_set_weights(h, w)
-        layers.append(h)
+    peaks, _ = measured_peaks()
+    y = torch.empty((prompt, s.d_model), dtype=torch.float32, device=dev)
     xs = [torch.from_numpy(synth.tokens(s, l, 0, prompt, wl.rms_normalise, seed).view(np.int16))
           .view(torch.bfloat16).to(dev) for l in range(P)]
-    y = torch.empty((prompt, s.d_model), dtype=torch.float32, device=dev)
-    # warm-up on a separate layer-sized call to load kernels, then reset caches
-    moe.moe_forward(layers[0], xs[0][:128], y=y[:128])
-    torch.cuda.synchronize(dev)
-    w = synth.layer_weights(s, 0, seed, reuse=w)
-    moe.moe_layer_set_weights(layers[0], w)
-    moe.moe_ctx_set_profiling(ctx, True)
-    moe.moe_ctx_reset_kernel_times(ctx)
-    for h in layers:
-        moe.moe_layer_reset_stats(h)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize(dev)
-    ev0.record(stream)
+
+    def make(shapes, slots, l, w):
+        w = synth.layer_weights(shapes, l, seed, reuse=w)
+        h = moe.moe_layer_create(ctx, shapes, slots, wl.policy)
+        moe.moe_layer_set_weights(h, w)
+        return h, w
+
+    # (1) streaming
+    layers, w = [], None
     for l in range(P):
-        moe.moe_forward(layers[l], xs[l], y=y)
-    ev1.record(stream)
+        h, w = make(s, wl.cache_slots, l, w)
+        layers.append(h)
+    moe.moe_forward(layers[0], xs[0][:128], y=y[:128])  # load the kernels
     torch.cuda.synchronize(dev)
-    ms = ev0.elapsed_time(ev1)
-    kt = moe.moe_ctx_kernel_times(ctx)
-    moe.moe_ctx_set_profiling(ctx, False)
-    stats = [moe.moe_layer_stats(h) for h in layers]
+    moe.moe_layer_destroy(layers[0])  # a fresh cache for the timed pass
+    layers[0], w = make(s, wl.cache_slots, 0, w)
+    ms, kt, stats = _prefill_pass(ctx, dev, stream, layers, xs, y)
     for h in layers:
         moe.moe_layer_destroy(h)
-    expert_kinds = ("expert_ffn", "gemm_gateup", "gemm_down")
-    fl = sum(kt[k][3] for k in expert_kinds)
-    kms = sum(kt[k][1] for k in expert_kinds)
+    kinds = ("gemm_gateup", "gemm_down", "pf_gather", "combine", "router")
+    kms = sum(kt[k][1] for k in ("gemm_gateup", "gemm_down"))
+    fl = sum(kt[k][3] for k in ("gemm_gateup", "gemm_down"))
     hits = sum(x["hits"] for x in stats)
     misses = sum(x["misses"] for x in stats)
-    return {
+    out = {
         "workload": "prefill_2816", "layers_measured": P, "prompt_tokens": prompt, "chunk": wl.tokens,
         "tok_s_per_layer": prompt * P / (ms * 1e-3),
         "tok_s_30_layers": prompt / (ms * 1e-3 / P * 30),
@@ -471,10 +505,27 @@ def run_prefill(args, ctx, dev, stream, seed):
         "hit_rate": hits / (hits + misses) if hits + misses else None,
         "h2d_GB": sum(x["bytes_h2d"] for x in stats) / 1e9,
         "exposed_copy_ms": sum(x["exposed_copy_us"] for x in stats) / 1e3,
-        "kernels": {k: {"launches": v[0], "ms": round(v[1], 3),
-                        "TFLOPs": round(v[3] / (v[1] * 1e-3) / 1e12, 2) if v[1] > 0 else None}
-                    for k, v in kt.items() if v[0] > 0},
+        "kernels": {k: {"launches": kt[k][0], "ms": round(kt[k][1], 3)} for k in kinds if kt[k][0] > 0},
     }
+
+    # (2) all-resident: 256 slots, filled by a first pass
+    h, w = make(s, s.n_experts, 0, w)
+    _prefill_pass(ctx, dev, stream, [h], xs[:1], y)
+    ms2, kt2, st2 = _prefill_pass(ctx, dev, stream, [h], xs[:1], y)
+    moe.moe_layer_destroy(h)
+    out["all_resident"] = {"tok_s_per_layer": prompt / (ms2 * 1e-3), "wall_ms": ms2,
+                           "hit_rate": st2[0]["hits"] / max(1, st2[0]["hits"] + st2[0]["misses"]),
+                           "kernels": _gemm_summary(kt2, peaks)}
+
+    # (3) the shared-expert GEMM: 128 x 2816 x 2816 (gate, up) and 128 x 2816 x 2816 (down) per chunk
+    s3 = synth.Shapes(s.d_model, 1, 1, 64, s.d_ff_shared, s.act)
+    h, _ = make(s3, 1, 0, None)
+    _prefill_pass(ctx, dev, stream, [h], xs[:1], y)
+    ms3, kt3, _ = _prefill_pass(ctx, dev, stream, [h], xs[:1], y)
+    moe.moe_layer_destroy(h)
+    out["shared_gemm"] = {"shape": f"{prompt}x{s.d_model}x{s.d_ff_shared} in chunks of {wl.tokens}",
+                          "wall_ms": ms3, "kernels": _gemm_summary(kt3, peaks)}
+    return out
 
 
 def main():

@@ -46,17 +46,41 @@ moe_status set_error(moe_status s, const char* fmt, ...) {
     return s;
 }
 
+// One 32-bit word of 8 codes (elements k0..k7 of the canonical row, byte j =
+// k_2j | k_2j+1 << 4) in the device order: nibble i holds element
+// [0,2,4,6,1,3,5,7][i], so that masking with 0x000F000F (and the same on the
+// word shifted by 4, 8, 12) yields the consecutive pairs (k0,k1), (k2,k3),
+// (k4,k5), (k6,k7) in the two halves of a 32-bit register.
+uint32_t device_nibble_order(const uint8_t* b) {
+    uint32_t k[8];
+    for (int j = 0; j < 4; ++j) {
+        k[2 * j] = b[j] & 15u;
+        k[2 * j + 1] = b[j] >> 4;
+    }
+    static const int order[8] = {0, 2, 4, 6, 1, 3, 5, 7};
+    uint32_t w = 0;
+    for (int i = 0; i < 8; ++i) w |= k[order[i]] << (4 * i);
+    return w;
+}
+
+// Device layout of one [N][K] int4 matrix: 32-row tiles, each a run of K/64
+// records, one per group of 64 inputs. Record (rt, g), at (rt * K/64 + g) *
+// 1152: the codes of chunk 2g for rows rt*32 + lane (16 bytes per lane), the
+// codes of chunk 2g+1 likewise, then one word per lane: fp16 scale | fp16 bias
+// << 16. So a row tile's consecutive groups are one contiguous copy.
 void repack_qmatrix(const moe_qmatrix& m, int N, int K, uint8_t* dst) {
-    const int C = K / 32, G = K / 64;
-    uint8_t* codes = dst;
-    uint32_t* sb = reinterpret_cast<uint32_t*>(dst + (size_t)N * (size_t)K / 2);
+    const int G = K / 64;
     for (int n = 0; n < N; ++n) {
         const int rt = n >> 5, lane = n & 31;
         const uint8_t* src = m.codes + (size_t)n * (size_t)(K / 2);
-        for (int c = 0; c < C; ++c) memcpy(codes + (((size_t)rt * C + c) * 32 + lane) * 16, src + (size_t)c * 16, 16);
         for (int g = 0; g < G; ++g) {
+            uint8_t* rec = dst + ((size_t)rt * G + g) * 1152;
+            for (int h = 0; h < 2; ++h) {
+                uint32_t* o = reinterpret_cast<uint32_t*>(rec + h * 512 + lane * 16);
+                for (int w = 0; w < 4; ++w) o[w] = device_nibble_order(src + (size_t)(2 * g + h) * 16 + 4 * w);
+            }
             const size_t i = (size_t)n * G + g;
-            sb[((size_t)rt * G + g) * 32 + lane] = (uint32_t)m.scale[i] | ((uint32_t)m.bias[i] << 16);
+            reinterpret_cast<uint32_t*>(rec + 1024)[lane] = (uint32_t)m.scale[i] | ((uint32_t)m.bias[i] << 16);
         }
     }
 }
@@ -76,7 +100,7 @@ using namespace moe;
 namespace {
 
 constexpr int kKinds = 8;
-enum Kind { K_ROUTER = 0, K_FFN = 1, K_COMBINE = 2, K_GEMM_GU = 3, K_GEMM_DN = 4 };
+enum Kind { K_ROUTER = 0, K_FFN = 1, K_COMBINE = 2, K_GEMM_GU = 3, K_GEMM_DN = 4, K_GATHER = 5 };
 constexpr double kHostWaitLimitS = 10.0;  // longest the host waits for the routing of one call
 
 using WriteValue32 = CUresult (*)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
@@ -159,6 +183,15 @@ struct moe_layer {
     std::vector<int32_t> h_ids;           // ids of the current call, read from h_pub
     float* d_part = nullptr;
     size_t part_floats = 0;
+    // prefill (T > kDecodeMaxT): fp16 token rows (x of the shared expert
+    // [cap_T][d], then x gathered per sorted pair [pairs][d]), fp16 h (shared
+    // [cap_T][d_ff_shared], then routed [pairs][d_ff]), and the item/pair
+    // table (pinned host copy and its device twin)
+    __half* d_x16 = nullptr;
+    __half* d_h16 = nullptr;
+    uint8_t* d_pf = nullptr;
+    uint8_t* h_pf = nullptr;
+    size_t pf_bytes = 0;
     unsigned* d_fcount = nullptr;
     size_t n_fcount = 0;
     uint32_t err_generation = 0;  // the context's value when the counters were last known zero
@@ -199,6 +232,13 @@ void free_scratch(moe_layer* L) {
     cudaFree(L->d_os);
     cudaFree(L->d_part);
     cudaFree(L->d_fcount);
+    cudaFree(L->d_x16);
+    cudaFree(L->d_h16);
+    cudaFree(L->d_pf);
+    cudaFreeHost(L->h_pf);
+    L->d_x16 = L->d_h16 = nullptr;
+    L->d_pf = L->h_pf = nullptr;
+    L->pf_bytes = 0;
     cudaFreeHost(L->h_pub);
     L->d_logits = nullptr;
     L->d_rcount = nullptr;
@@ -237,6 +277,14 @@ moe_status ensure_scratch(moe_layer* L, int T) {
               cudaMemset(L->d_fcount, 0, sizeof(unsigned) * L->n_fcount) == cudaSuccess &&
               cudaHostAlloc(&L->h_pub, sizeof(unsigned long long) * pairs, cudaHostAllocMapped) == cudaSuccess &&
               cudaHostGetDevicePointer(&L->h_pub_dev, L->h_pub, 0) == cudaSuccess;
+    if (ok && T > kDecodeMaxT) {
+        const size_t items = 1 + std::min<size_t>(s.n_experts, pairs);
+        L->pf_bytes = items * sizeof(PfItem) + pairs * sizeof(int32_t);
+        ok = cudaMalloc(&L->d_x16, sizeof(__half) * ((size_t)T + pairs) * s.d_model) == cudaSuccess &&
+             cudaMalloc(&L->d_h16, sizeof(__half) * ((size_t)T * s.d_ff_shared + pairs * s.d_ff)) == cudaSuccess &&
+             cudaMalloc(&L->d_pf, L->pf_bytes) == cudaSuccess &&
+             cudaHostAlloc(&L->h_pf, L->pf_bytes, cudaHostAllocDefault) == cudaSuccess;
+    }
     if (!ok) {
         cudaGetLastError();
         free_scratch(L);
@@ -509,6 +557,100 @@ moe_status run_experts(moe_layer* L, const uint16_t* x, int T, float* y, const s
     return st;
 }
 
+// The experts of a prefill chunk (T > kDecodeMaxT) as grouped GEMMs on the
+// tensor cores: every token row of an expert in one item (the shared expert
+// over all T tokens; each routed expert over its pairs, sorted by expert),
+// then gate/up, down into y (shared) and o (routed), and the combine
+// y += sum_r g_r o_r. Hits come before misses in the job order, so the
+// resident experts run while the copies land.
+moe_status run_experts_prefill(moe_layer* L, const uint16_t* x, int T, float* y,
+                               const std::vector<int>& ready_of_miss, cudaEvent_t copies_done, cudaStream_t s) {
+    moe_ctx* C = L->ctx;
+    const moe_shapes& sh = L->sh;
+    const int k = sh.top_k, d = sh.d_model, P = T * k;
+    if (T > kPfMaxN || !L->d_pf) return set_error(MOE_EINVAL, "prefill chunk of %d tokens (at most %d)", T, kPfMaxN);
+    L->offsets.resize(sh.n_experts + 1);
+    L->perm.resize(P);
+    group_pairs(L->h_ids.data(), P, sh.n_experts, L->offsets.data(), L->perm.data());
+    PfItem* items = reinterpret_cast<PfItem*>(L->h_pf);
+    int n = 0;
+    items[n++] = PfItem{L->d_shared, 0, T, -1, 0};
+    std::vector<PfItem> miss;
+    int nb = 0;
+    size_t mi = 0;
+    double bytes = (double)L->shared_bytes;
+    for (int e : L->step.distinct) {
+        while (mi < L->step.miss_experts.size() && L->step.miss_experts[mi] < e) ++mi;
+        const bool is_miss = mi < L->step.miss_experts.size() && L->step.miss_experts[mi] == e;
+        const int slot = is_miss ? L->step.miss_slots[mi] : L->cache.slot_of(e);
+        const uint8_t* w = slot >= 0 ? L->d_slots + (size_t)slot * L->ebytes : C->staging + (size_t)(nb++) * L->ebytes;
+        const PfItem it{w, L->offsets[e], L->offsets[e + 1] - L->offsets[e], is_miss ? ready_of_miss[mi] : -1, 0};
+        if (it.np > kPfMaxN) return set_error(MOE_EINVAL, "expert %d has %d rows in one chunk", e, it.np);
+        if (is_miss)
+            miss.push_back(it);
+        else
+            items[n++] = it;
+        bytes += (double)L->ebytes;
+    }
+    for (const PfItem& it : miss) items[n++] = it;
+    const size_t item_bytes = sizeof(PfItem) * (1 + std::min<size_t>(sh.n_experts, P));
+    int32_t* pair_h = reinterpret_cast<int32_t*>(L->h_pf + item_bytes);
+    std::copy(L->perm.begin(), L->perm.end(), pair_h);
+    CUDA_TRY(cudaMemcpyAsync(L->d_pf, L->h_pf, L->pf_bytes, cudaMemcpyHostToDevice, s));
+
+    PfArgs a{};
+    a.items = reinterpret_cast<const PfItem*>(L->d_pf);
+    a.n_items = n;
+    a.n_fam0 = 1;
+    a.d = d;
+    a.act = sh.act;
+    a.T = T;
+    a.k = k;
+    a.inter[0] = sh.d_ff_shared;
+    a.inter[1] = sh.d_ff;
+    a.pair = reinterpret_cast<const int32_t*>(L->d_pf + item_bytes);
+    __half* xs = L->d_x16;
+    __half* xg = xs + (size_t)T * d;
+    a.h[0] = L->d_h16;
+    a.h[1] = L->d_h16 + (size_t)T * sh.d_ff_shared;
+    a.out[0] = y;
+    a.out[1] = L->d_o;
+    a.ready = L->d_ready;
+    a.epoch = L->epoch;
+    a.err = C->err_dev;
+    const int rows[2] = {T, P};
+    WaitRec wr{};
+    if (copies_done) {
+        wr.ffn_start = C->timing_event();
+        wr.copies_done = copies_done;
+        CUDA_TRY(cudaEventRecord(wr.ffn_start, s));
+    }
+    {
+        Prof p(C, s, K_GATHER, 2.0 * (T + P) * d * 2, 0);
+        CUDA_TRY(launch_pf_gather(x, T, d, a.pair, P, k, xs, xg, s));
+    }
+    const double rows_shared = T, rows_routed = P;
+    const double fl_gu = 4.0 * d * (rows_shared * sh.d_ff_shared + rows_routed * sh.d_ff);
+    const double fl_dn = 2.0 * d * (rows_shared * sh.d_ff_shared + rows_routed * sh.d_ff);
+    const double by_gu = (double)L->shared_bytes * 2 / 3 + (bytes - L->shared_bytes) * 2 / 3;
+    const double by_dn = bytes - by_gu;
+    {
+        Prof p(C, s, K_GEMM_GU, by_gu, fl_gu);
+        CUDA_TRY(launch_pf_gemm(a, 1, xs, xg, rows, s));
+    }
+    {
+        Prof p(C, s, K_GEMM_DN, by_dn, fl_dn);
+        CUDA_TRY(launch_pf_gemm(a, 2, a.h[0], a.h[1], rows, s));
+    }
+    {
+        Prof p(C, s, K_COMBINE, 4.0 * ((double)P * d + 2.0 * T * d), 2.0 * P * d);
+        CUDA_TRY(launch_combine(L->d_o, L->d_gates, T, k, d, y, s));
+    }
+    L->stats.bytes_resident += (uint64_t)bytes;
+    if (copies_done) L->waits.push_back(wr);
+    return MOE_OK;
+}
+
 // Wait on the host until the router of the current call has published all
 // n ids (each word carries the call number in its high half).
 moe_status wait_published(moe_layer* L, int n) {
@@ -577,7 +719,8 @@ moe_status forward_chunk(moe_layer* L, const uint16_t* x, int T, const float* zb
         copies_done = C->timing_event();
         CUDA_TRY(cudaEventRecord(copies_done, C->copy_stream));
     }
-    st = run_experts(L, x, T, y, ready_of_miss, copies_done, s);
+    st = T > kDecodeMaxT ? run_experts_prefill(L, x, T, y, ready_of_miss, copies_done, s)
+                         : run_experts(L, x, T, y, ready_of_miss, copies_done, s);
     if (st != MOE_OK) return st;
     if (ids_out) CUDA_TRY(cudaMemcpyAsync(ids_out, L->d_ids, sizeof(int32_t) * npairs, cudaMemcpyDeviceToDevice, s));
     if (gates_out)

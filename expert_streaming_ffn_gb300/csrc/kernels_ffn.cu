@@ -49,7 +49,8 @@ constexpr int kEpi = 2;   // epilogue warps
 constexpr int kThreads = (kCons + 1 + kEpi) * 32;
 constexpr int kStages = 3;
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kStageBytes = 2 * (kCons * 1024 + kCons * 128);  // gate+up stage; a down stage uses half
+constexpr int kRecord = 1152;  // one group of 64 inputs x 32 rows: codes, then scale/bias words
+constexpr int kStageBytes = 2 * kCons * kRecord;  // gate+up stage; a down stage uses half
 constexpr int kMaxSplitJobs = 1024;
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -430,13 +431,10 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) ffn_kernel(const __
                 const size_t mat = qmat_bytes(inter, a.d);  // bytes of one of gate, up, down
                 const int two = b.phase == 1 ? 2 : 1;
                 const int K = b.phase == 1 ? a.d : inter;
-                const int N = b.phase == 1 ? inter : a.d;
                 const unsigned char* A = it.w + (b.phase == 1 ? 0 : 2 * mat);
-                const size_t ctot = (size_t)N * K / 2;
                 for (int t = 0; t < b.ntiles && ok; ++t) {
                     const int rt = b.rt0 + t;
-                    const unsigned char* ca = A + (size_t)rt * (K >> 5) * 512;
-                    const unsigned char* sa = A + ctot + (size_t)rt * (K >> 6) * 128;
+                    const unsigned char* ra = A + (size_t)rt * (K >> 6) * kRecord;  // the row tile's records
                     for (int s0 = 0; s0 < b.ng; s0 += kCons) {
                         const int ng = min(kCons, b.ng - s0);
                         const size_t g = (size_t)(b.g0 + s0);
@@ -445,14 +443,9 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) ffn_kernel(const __
                             break;
                         }
                         unsigned char* st = ring + slot * kStageBytes;
-                        ptx::mbar_arrive_expect_tx(full + slot, (uint32_t)(two * ng * (1024 + 128)));
-                        ptx::bulk_g2s(st, ca + g * 1024, ng * 1024, full + slot);
-                        ptx::bulk_g2s(st + 2 * kCons * 1024, sa + g * 128, ng * 128, full + slot);
-                        if (two == 2) {
-                            ptx::bulk_g2s(st + kCons * 1024, ca + mat + g * 1024, ng * 1024, full + slot);
-                            ptx::bulk_g2s(st + 2 * kCons * 1024 + kCons * 128, sa + mat + g * 128, ng * 128,
-                                          full + slot);
-                        }
+                        ptx::mbar_arrive_expect_tx(full + slot, (uint32_t)(two * ng * kRecord));
+                        ptx::bulk_g2s(st, ra + g * kRecord, ng * kRecord, full + slot);
+                        if (two == 2) ptx::bulk_g2s(st + kCons * kRecord, ra + mat + g * kRecord, ng * kRecord, full + slot);
                         ++issued;
                         if (++slot == kStages) {
                             slot = 0;
@@ -590,8 +583,11 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) ffn_kernel(const __
                     float sum = v0 + v1;
 #pragma unroll
                     for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
-                    *reinterpret_cast<float2*>(xme + q * xs_stride + c * 64 + 2 * lane) =
-                        make_float2(v0 * pos_scale((2 * lane) & 7), v1 * pos_scale((2 * lane + 1) & 7));
+                    // elements 2m and 2m+1 of each run of 8 sit at nibbles m and 4+m of the code word
+                    float* xo = xme + q * xs_stride + c * 64 + 8 * (lane >> 2);
+                    const int m = lane & 3;
+                    xo[m] = v0 * pos_scale(m);
+                    xo[4 + m] = v1 * pos_scale(4 + m);
                     if (lane == 0) xsme[q * cw_max + c] = sum;
                 }
             }
@@ -625,15 +621,15 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) ffn_kernel(const __
                 if (ok && active) {
                     const unsigned char* st = ring + slot * kStageBytes;
                     const float* xg = xme + c * 64;
-                    const unsigned char* cb = st + warp * 1024 + lane * 16;
-                    const unsigned char* sbp = st + 2 * kCons * 1024 + warp * 128 + lane * 4;
+                    const unsigned char* cb = st + warp * kRecord + lane * 16;  // this warp's record
+                    const unsigned char* sbp = st + warp * kRecord + 1024 + lane * 4;
                     if (mats == 2) {
                         const uint4 c0[2] = {*reinterpret_cast<const uint4*>(cb),
-                                             *reinterpret_cast<const uint4*>(cb + kCons * 1024)};
+                                             *reinterpret_cast<const uint4*>(cb + kCons * kRecord)};
                         const uint4 c1[2] = {*reinterpret_cast<const uint4*>(cb + 512),
-                                             *reinterpret_cast<const uint4*>(cb + kCons * 1024 + 512)};
+                                             *reinterpret_cast<const uint4*>(cb + kCons * kRecord + 512)};
                         const float2 fg = unpack_sb(*reinterpret_cast<const uint32_t*>(sbp));
-                        const float2 fu = unpack_sb(*reinterpret_cast<const uint32_t*>(sbp + kCons * 128));
+                        const float2 fu = unpack_sb(*reinterpret_cast<const uint32_t*>(sbp + kCons * kRecord));
                         float pr[2][NT];
                         group_dot<NT, 2>(c0, c1, xg, xs_stride, pr);
 #pragma unroll

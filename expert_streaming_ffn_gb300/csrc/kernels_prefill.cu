@@ -1,0 +1,584 @@
+// Prefill grouped GEMM of the expert-streaming MoE layer on the 5th-generation
+// tensor cores (sm_103a): tcgen05.mma with fp16 operands in shared memory and
+// fp32 accumulators in tensor memory.
+//
+//   [P1] "在 Rockchip NPU 上实现 turbo-fieldfare 风格 MoE 大模型流式推理的技术方案"
+//        §2.5 and §8.4: a prefill chunk's tokens are grouped per expert, so one
+//        fetch of an expert's weights serves every row of the chunk routed to it.
+//
+// One launch per phase. A job is one 128-row tile of one item's weight matrix
+// over all of K, against all of the item's token rows (N <= 128, padded to a
+// multiple of 16):
+//   phase 1 (gate/up): the tile interleaves 64 gate rows and the same 64 up
+//     rows (in each 32-row quarter, even rows gate and odd rows up), so the
+//     epilogue forms h = act(gate) * up from neighbouring lanes;
+//   phase 2 (down): 128 consecutive output rows.
+// Warp roles in a CTA of 512 threads (one CTA per SM, persistent over jobs):
+//   warp 0      bulk copies of the weight records (int4 codes with their
+//               scales) of 4 K-blocks per row tile at a time, into a raw ring;
+//   warp 1      TMEM allocation and, from one thread, the MMA issue;
+//   warp 2      TMA loads of the token rows (128B-swizzled fp16) per K-block;
+//   warps 4-7   epilogue, one TMEM lane quarter each;
+//   warps 8-15  dequantisation: int4 -> fp16 w = fp16(s * q + b), written into
+//               the 128B-swizzled K-major A tile.
+// Copies are few and large (a bulk copy costs its issuing thread tens of
+// nanoseconds whatever its size), and the two producers issue in parallel.
+// Every wait is bounded; on expiry the kernel records an error bit, raises an
+// abort flag that makes every other wait give up, drains its asynchronous work
+// and frees its tensor memory before it exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "moe_internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kThreads = 512;
+constexpr int kWarpLoad = 0, kWarpMma = 1, kWarpB = 2, kWarpEpi = 4, kWarpDq = 8, kDqWarps = 8;
+constexpr int kStages = 4;     // A/B ring, one K-block (64) per stage
+constexpr int kRawStages = 4;  // raw ring, kUnit K-blocks per stage
+constexpr int kUnit = 4;
+constexpr int kTileM = 128;
+constexpr int kRecord = 1152;           // 32 rows x 64 codes, then 32 scale/bias words
+constexpr int kABytes = kTileM * 128;   // 128 rows x 64 fp16, 128B-swizzled
+constexpr int kBBytes = kPfMaxN * 128;  // up to 128 token rows x 64 fp16
+constexpr int kRawBytes = 4 * kUnit * kRecord;  // 4 row tiles x kUnit records
+constexpr int kTmemCols = 2 * kPfMaxN;  // two accumulators of up to 128 fp32 columns
+// shared memory: A ring, B ring, raw ring, barriers, TMEM address; +1 KB to align
+constexpr int kSmemBytes = 1024 + kStages * (kABytes + kBBytes) + kRawStages * kRawBytes + 256;
+
+// Shared-memory matrix descriptor of a K-major operand tile whose rows are 128
+// bytes apart with the 128-byte swizzle (8-row atoms of 1024 bytes).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4)  // start address
+           | ((uint64_t)1 << 16)                // leading byte offset (unused for swizzled K-major)
+           | ((uint64_t)(1024 >> 4) << 32)      // stride byte offset: 8 rows
+           | ((uint64_t)1 << 46)                // descriptor version
+           | ((uint64_t)2 << 61);               // 128-byte swizzle
+}
+
+// Instruction descriptor: fp16 A and B, both K-major, fp32 D, M x N.
+__device__ __forceinline__ uint32_t f16_idesc(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ __half2 as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+__device__ __forceinline__ uint32_t as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+
+// Eight codes of one word (device nibble order: nibble i holds element
+// [0,2,4,6,1,3,5,7][i]) to eight fp16 weights fp16(s * q + b), elements in
+// order. (w & 0x000F000F) | 0x6400_6400 is the fp16 pair (1024 + q, 1024 + q')
+// exactly; with the mask 0x00F000F0 it is (1024 + 16 q, ...), brought back to
+// q by one exact fused multiply-add.
+__device__ __forceinline__ uint4 dequant8(uint32_t v, __half2 s2, __half2 b2) {
+    const uint32_t M = 0x64006400u;
+    const __half2 c1024 = as_h2(0x64006400u);  // (1024, 1024)
+    const __half2 inv16 = as_h2(0x2C002C00u);  // (1/16, 1/16)
+    const __half2 m64 = as_h2(0xD400D400u);    // (-64, -64)
+    const uint32_t u = v >> 8;
+    const __half2 q0 = __hsub2(as_h2((v & 0x000F000Fu) | M), c1024);
+    const __half2 q1 = __hfma2(as_h2((v & 0x00F000F0u) | M), inv16, m64);
+    const __half2 q2 = __hsub2(as_h2((u & 0x000F000Fu) | M), c1024);
+    const __half2 q3 = __hfma2(as_h2((u & 0x00F000F0u) | M), inv16, m64);
+    uint4 r;
+    r.x = as_u32(__hfma2(q0, s2, b2));
+    r.y = as_u32(__hfma2(q1, s2, b2));
+    r.z = as_u32(__hfma2(q2, s2, b2));
+    r.w = as_u32(__hfma2(q3, s2, b2));
+    return r;
+}
+
+__device__ __forceinline__ float act_fn(float z, int act) {
+    if (act == 1) return z / (1.0f + expf(-z));
+    return 0.5f * z * (1.0f + tanhf(0.7978845608028654f * (z + 0.044715f * z * z * z)));
+}
+
+struct Job {
+    int item, fam, tile;
+};
+
+struct Plan {
+    int phase;
+    int tiles[2];    // M tiles per item
+    int kblocks[2];  // K blocks of 64
+    int n_jobs, jobs0;
+};
+
+__device__ __forceinline__ Plan make_plan(const PfArgs& a, int phase) {
+    Plan p;
+    p.phase = phase;
+    for (int f = 0; f < 2; ++f) {
+        p.tiles[f] = phase == 1 ? a.inter[f] / 64 : a.d / kTileM;
+        p.kblocks[f] = phase == 1 ? a.d / 64 : a.inter[f] / 64;
+    }
+    p.jobs0 = a.n_fam0 * p.tiles[0];
+    p.n_jobs = p.jobs0 + (a.n_items - a.n_fam0) * p.tiles[1];
+    return p;
+}
+
+__device__ __forceinline__ Job decode_job(const Plan& p, const PfArgs& a, int j) {
+    Job b;
+    if (j < p.jobs0) {
+        b.fam = 0;
+        b.item = j / p.tiles[0];
+        b.tile = j - b.item * p.tiles[0];
+    } else {
+        j -= p.jobs0;
+        b.fam = 1;
+        const int i = j / p.tiles[1];
+        b.tile = j - i * p.tiles[1];
+        b.item = a.n_fam0 + i;
+    }
+    return b;
+}
+
+__device__ __forceinline__ int pad16(int n) { return n <= 16 ? 16 : (n + 15) & ~15; }
+
+__device__ __forceinline__ bool wait_flag(const uint32_t* p, uint32_t want, volatile int* abort) {
+    for (uint64_t t0 = 0;;) {
+        uint32_t v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+        if (v == want) return true;
+        if (*abort) return false;
+        const uint64_t now = ptx::globaltimer();
+        if (t0 == 0) t0 = now;
+        if (now - t0 > ptx::kWaitLimitNs) return false;
+        __nanosleep(128);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    pf_gemm_kernel(const __grid_constant__ PfArgs a, const int phase, const __grid_constant__ CUtensorMap map0,
+                   const __grid_constant__ CUtensorMap map1) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem =
+        reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    unsigned char* ringA = smem;
+    unsigned char* ringB = ringA + kStages * kABytes;
+    unsigned char* ringR = ringB + kStages * kBBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ringR + kRawStages * kRawBytes);
+    uint64_t* raw_full = bars;                // [kRawStages] records landed
+    uint64_t* raw_empty = raw_full + kRawStages;  // [kRawStages] records dequantised
+    uint64_t* b_full = raw_empty + kRawStages;    // [kStages] token rows landed
+    uint64_t* a_full = b_full + kStages;          // [kStages] A tile dequantised
+    uint64_t* ab_empty = a_full + kStages;        // [kStages] MMAs reading the stage done
+    uint64_t* acc_full = ab_empty + kStages;      // [2] accumulator complete
+    uint64_t* acc_empty = acc_full + 2;           // [2] accumulator read out
+    uint64_t* drain = acc_empty + 2;              // [1] every MMA of the CTA done
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Plan P = make_plan(a, phase);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kRawStages; ++i) {
+            ptx::mbar_init(raw_full + i, 1);
+            ptx::mbar_init(raw_empty + i, kDqWarps);
+        }
+        for (int i = 0; i < kStages; ++i) {
+            ptx::mbar_init(b_full + i, 1);
+            ptx::mbar_init(a_full + i, kDqWarps);
+            ptx::mbar_init(ab_empty + i, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(acc_full + i, 1);
+            ptx::mbar_init(acc_empty + i, 4);
+        }
+        ptx::mbar_init(drain, 1);
+        abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == kWarpMma) {
+        ptx::tmem_alloc(tmem_slot, kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    volatile int* abortp = &abort_flag;
+    auto fail = [&](unsigned bit) {
+        atomicOr(a.err, bit);
+        abort_flag = 1;
+    };
+
+    if (warp == kWarpLoad) {
+        // ---------------- weight records ----------------
+        if (lane == 0) {
+            int r = 0;
+            uint32_t ph = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int j = blockIdx.x; j < P.n_jobs && ok; j += gridDim.x) {
+                const Job b = decode_job(P, a, j);
+                const PfItem it = a.items[b.item];
+                if (it.ready >= 0 && !wait_flag(a.ready + it.ready, a.epoch, abortp)) {
+                    if (!*abortp) fail(32u);
+                    ok = false;
+                    break;
+                }
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                const int I = a.inter[b.fam];
+                const size_t mat = qmat_bytes(I, a.d);
+                const int G = (phase == 1 ? a.d : I) / 64;  // records per row tile
+                const int nkb = P.kblocks[b.fam];
+                for (int kb0 = 0; kb0 < nkb; kb0 += kUnit) {
+                    const int nu = min(kUnit, nkb - kb0);
+                    if (!ptx::mbar_wait_bounded(raw_empty + r, ph ^ 1, abortp)) {
+                        if (!*abortp) fail(32u);
+                        ok = false;
+                        break;
+                    }
+                    unsigned char* raw = ringR + r * kRawBytes;
+                    ptx::mbar_arrive_expect_tx(raw_full + r, (uint32_t)(4 * nu * kRecord));
+                    for (int t = 0; t < 4; ++t) {
+                        // row tile t of the job: phase 1 gate 2i, gate 2i+1, up 2i, up 2i+1; phase 2 down 4i+t
+                        const unsigned char* m = it.w + (phase == 1 ? (size_t)(t >> 1) * mat : 2 * mat);
+                        const int rt = phase == 1 ? 2 * b.tile + (t & 1) : 4 * b.tile + t;
+                        ptx::bulk_g2s(raw + t * kUnit * kRecord, m + ((size_t)rt * G + kb0) * kRecord, nu * kRecord,
+                                      raw_full + r);
+                    }
+                    ++issued;
+                    if (++r == kRawStages) {
+                        r = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
+            if (!ok) {
+                // let the copies already issued land before the CTA can exit
+                for (int i = 0; i < kRawStages && i < issued; ++i) {
+                    int sl = r - 1 - i;
+                    uint32_t par = ph;
+                    if (sl < 0) {
+                        sl += kRawStages;
+                        par ^= 1;
+                    }
+                    ptx::mbar_wait_bounded(raw_full + sl, par, nullptr);
+                }
+            }
+        }
+    } else if (warp == kWarpB) {
+        // ---------------- token rows ----------------
+        if (lane == 0) {
+            ptx::prefetch_tensormap(&map0);
+            ptx::prefetch_tensormap(&map1);
+            int s = 0;
+            uint32_t ph = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int j = blockIdx.x; j < P.n_jobs && ok; j += gridDim.x) {
+                const Job b = decode_job(P, a, j);
+                const PfItem it = a.items[b.item];
+                const int nb = pad16(it.np);
+                for (int kb = 0; kb < P.kblocks[b.fam]; ++kb) {
+                    if (!ptx::mbar_wait_bounded(ab_empty + s, ph ^ 1, abortp)) {
+                        if (!*abortp) fail(512u);
+                        ok = false;
+                        break;
+                    }
+                    unsigned char* bt = ringB + s * kBBytes;
+                    ptx::mbar_arrive_expect_tx(b_full + s, (uint32_t)(nb * 128));
+                    if (b.fam == 0) {
+                        ptx::tma_load_2d(bt, &map0, kb * 64, 0, b_full + s);  // one box of all the rows
+                    } else {
+                        for (int r0 = 0; r0 < nb; r0 += 16)
+                            ptx::tma_load_2d(bt + r0 * 128, &map1, kb * 64, it.pb + r0, b_full + s);
+                    }
+                    ++issued;
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
+            if (!ok) {
+                for (int i = 0; i < kStages && i < issued; ++i) {
+                    int sl = s - 1 - i;
+                    uint32_t par = ph;
+                    if (sl < 0) {
+                        sl += kStages;
+                        par ^= 1;
+                    }
+                    ptx::mbar_wait_bounded(b_full + sl, par, nullptr);
+                }
+            }
+        }
+    } else if (warp == kWarpMma) {
+        // ---------------- MMA issue ----------------
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int njob = 0;
+            for (int j = blockIdx.x; j < P.n_jobs; j += gridDim.x, ++njob) {
+                const Job b = decode_job(P, a, j);
+                const int nb = pad16(a.items[b.item].np);
+                const int buf = njob & 1;
+                const uint32_t idesc = f16_idesc(kTileM, nb);
+                const uint32_t d_tmem = tmem + buf * kPfMaxN;
+                // the epilogue must have read this accumulator's previous job
+                bool ok = ptx::mbar_wait_bounded(acc_empty + buf, ((njob >> 1) & 1) ^ 1, abortp);
+                ptx::tc_fence_after();
+                for (int kb = 0; kb < P.kblocks[b.fam]; ++kb) {
+                    ok = ok && ptx::mbar_wait_bounded(b_full + s, ph, abortp) &&
+                         ptx::mbar_wait_bounded(a_full + s, ph, abortp);
+                    if (ok) {
+                        ptx::tc_fence_after();
+                        const uint64_t ad = sw128_desc(ptx::smem_addr(ringA + s * kABytes));
+                        const uint64_t bd = sw128_desc(ptx::smem_addr(ringB + s * kBBytes));
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)  // K = 16 per MMA: +32 bytes in the swizzled row
+                            ptx::mma_f16_ss(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+                        ptx::mma_commit(ab_empty + s);
+                    }
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
+                if (ok) {
+                    ptx::mma_commit(acc_full + buf);
+                } else if (!*abortp) {
+                    fail(128u);
+                }
+            }
+            // every MMA issued by this thread has completed once this arrives
+            ptx::mma_commit(drain);
+            ptx::mbar_wait_bounded(drain, 0, nullptr);
+        }
+    } else if (warp >= kWarpEpi && warp < kWarpEpi + 4) {
+        // ---------------- epilogue ----------------
+        const int q = warp - kWarpEpi;  // TMEM lanes 32q .. 32q + 31
+        int njob = 0;
+        for (int j = blockIdx.x; j < P.n_jobs; j += gridDim.x, ++njob) {
+            const Job b = decode_job(P, a, j);
+            const PfItem it = a.items[b.item];
+            const int nb = pad16(it.np);
+            const int buf = njob & 1;
+            if (!__all_sync(kFull, ptx::mbar_wait_bounded(acc_full + buf, (njob >> 1) & 1, abortp))) {
+                if (lane == 0 && !*abortp) fail(256u);
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * kPfMaxN;
+            if (phase == 1) {
+                const int I = a.inter[b.fam];
+                const int irow = 64 * b.tile + 16 * q + (lane >> 1);
+                __half* hb = a.h[b.fam];
+                for (int c = 0; c < nb; c += 16) {
+                    uint32_t v[16];
+                    ptx::tmem_ld16(taddr + c, v);
+                    ptx::tmem_ld_wait();
+                    // even lanes hold gate rows, odd lanes the matching up rows:
+                    // the even lane finishes columns c..c+7, the odd lane c+8..c+15
+                    const bool odd = lane & 1;
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) {
+                        const float mine = __uint_as_float(odd ? v[m + 8] : v[m]);
+                        const float other = __shfl_xor_sync(kFull, __uint_as_float(odd ? v[m] : v[m + 8]), 1);
+                        const float g = odd ? other : mine, u = odd ? mine : other;
+                        const int col = c + m + (odd ? 8 : 0);
+                        if (col < it.np) hb[(size_t)(it.pb + col) * I + irow] = __float2half_rn(act_fn(g, a.act) * u);
+                    }
+                }
+            } else {
+                const int n = kTileM * b.tile + 32 * q + lane;
+                for (int c = 0; c < nb; c += 16) {
+                    uint32_t v[16];
+                    ptx::tmem_ld16(taddr + c, v);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) {
+                        const int col = c + m;
+                        if (col >= it.np) break;
+                        const size_t row = b.fam == 0 ? (size_t)col : (size_t)a.pair[it.pb + col];
+                        a.out[b.fam][row * a.d + n] = __uint_as_float(v[m]);
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(acc_empty + buf);
+        }
+    } else if (warp >= kWarpDq) {
+        // ---------------- dequantisation ----------------
+        const int t = threadIdx.x - kWarpDq * 32;  // 0..255: A row t / 2, half t % 2 of the K-block
+        const int rho = t >> 1, hh = t & 1;
+        int tile_raw, rlane;
+        if (phase == 1) {
+            const int qq = rho >> 5, l = rho & 31;
+            const int wrow = 16 * qq + (l >> 1);  // row within the 64 gate (or up) rows of the tile
+            tile_raw = (l & 1) * 2 + (wrow >> 5);
+            rlane = wrow & 31;
+        } else {
+            tile_raw = rho >> 5;
+            rlane = rho & 31;
+        }
+        const int codes_off = tile_raw * kUnit * kRecord + hh * 512 + rlane * 16;
+        const int sb_off = tile_raw * kUnit * kRecord + 1024 + rlane * 4;
+        int r = 0, s = 0;
+        uint32_t rph = 0, ph = 0;
+        for (int j = blockIdx.x; j < P.n_jobs; j += gridDim.x) {
+            const Job b = decode_job(P, a, j);
+            const int nkb = P.kblocks[b.fam];
+            for (int kb0 = 0; kb0 < nkb; kb0 += kUnit) {
+                const int nu = min(kUnit, nkb - kb0);
+                const bool have = ptx::mbar_wait_bounded(raw_full + r, rph, abortp);
+                if (!have && lane == 0 && !*abortp) fail(64u);
+                const unsigned char* raw = ringR + r * kRawBytes;
+                for (int u = 0; u < nu; ++u) {
+                    // the A stage is free once the MMAs that read it are done
+                    const bool free_a = have && ptx::mbar_wait_bounded(ab_empty + s, ph ^ 1, abortp);
+                    if (free_a) {
+                        const uint4 cw = *reinterpret_cast<const uint4*>(raw + codes_off + u * kRecord);
+                        const uint32_t sbw = *reinterpret_cast<const uint32_t*>(raw + sb_off + u * kRecord);
+                        const __half2 s2 = __half2half2(__ushort_as_half((unsigned short)(sbw & 0xFFFFu)));
+                        const __half2 b2 = __half2half2(__ushort_as_half((unsigned short)(sbw >> 16)));
+                        unsigned char* arow = ringA + s * kABytes + rho * 128;
+                        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            const int chunk = 4 * hh + w;  // 16-byte chunk (8 elements) of the 128-byte row
+                            *reinterpret_cast<uint4*>(arow + ((chunk ^ (rho & 7)) << 4)) = dequant8(words[w], s2, b2);
+                        }
+                        ptx::fence_proxy_async_smem();  // generic-proxy writes, read next by the tensor core
+                    } else if (have && lane == 0 && !*abortp) {
+                        fail(64u);
+                    }
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(a_full + s);
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(raw_empty + r);
+                if (++r == kRawStages) {
+                    r = 0;
+                    rph ^= 1;
+                }
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+__global__ void pf_gather_kernel(const uint16_t* __restrict__ x, int T, int d, const int32_t* __restrict__ pair,
+                                 int P, int k, __half* __restrict__ xs, __half* __restrict__ xg) {
+    const int per_row = d / 8;
+    const long n = (long)(T + P) * per_row;
+    for (long i = blockIdx.x * (long)blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+        const int r = (int)(i / per_row), c = (int)(i - (long)r * per_row);
+        const int tok = r < T ? r : pair[r - T] / k;
+        const uint4 v = *reinterpret_cast<const uint4*>(x + (size_t)tok * d + c * 8);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const float lo = __uint_as_float(w[m] << 16), hi = __uint_as_float(w[m] & 0xffff0000u);
+            o[m] = as_u32(__floats2half2_rn(lo, hi));
+        }
+        __half* dst = r < T ? xs + (size_t)r * d : xg + (size_t)(r - T) * d;
+        *reinterpret_cast<uint4*>(dst + c * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+    static EncodeTiled fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// fp16 [rows][cols] row-major, boxes of 64 columns x box_rows rows, 128-byte swizzle.
+cudaError_t encode_rows(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) {
+    EncodeTiled fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    if ((reinterpret_cast<uintptr_t>(base) & 15) || cols % 64 || rows < 1) return cudaErrorInvalidValue;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+int num_sms() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 1;
+    }
+    return n;
+}
+
+}  // namespace
+
+cudaError_t launch_pf_gather(const uint16_t* x, int T, int d, const int32_t* pair, int P, int k, __half* xs,
+                             __half* xg, cudaStream_t s) {
+    const long n = (long)(T + P) * (d / 8);
+    const int blocks = (int)std::min<long>((n + 255) / 256, 4L * num_sms());
+    pf_gather_kernel<<<blocks, 256, 0, s>>>(x, T, d, pair, P, k, xs, xg);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pf_gemm(const PfArgs& a, int phase, const void* b0, const void* b1, const int rows[2],
+                           cudaStream_t s) {
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(pf_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    if ((phase != 1 && phase != 2) || a.n_items < 1 || a.n_fam0 < 0 || a.n_fam0 > a.n_items || a.d % kTileM ||
+        a.inter[0] % 64 || a.inter[1] % 64)
+        return cudaErrorInvalidValue;
+    CUtensorMap m0, m1;
+    const int k0 = phase == 1 ? a.d : a.inter[0], k1 = phase == 1 ? a.d : a.inter[1];
+    // family 0 is the shared expert over every token row: one box of all of them
+    if (rows[0] != a.T || a.T < 1 || a.T > kPfMaxN) return cudaErrorInvalidValue;
+    const int box0 = a.T <= 16 ? 16 : (a.T + 15) & ~15;
+    cudaError_t e = encode_rows(&m0, b0, rows[0], k0, box0);
+    if (e == cudaSuccess) e = encode_rows(&m1, b1, std::max(rows[1], 1), k1, 16);
+    if (e != cudaSuccess) return e;
+    const int tiles0 = phase == 1 ? a.inter[0] / 64 : a.d / kTileM;
+    const int tiles1 = phase == 1 ? a.inter[1] / 64 : a.d / kTileM;
+    const int jobs = a.n_fam0 * tiles0 + (a.n_items - a.n_fam0) * tiles1;
+    const int grid = std::min(jobs, num_sms());
+    pf_gemm_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, phase, m0, m1);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -5,6 +5,7 @@
 //   [P3] "BigMoeOnEdge：端侧 MoE 专家流式推理原理与实测"
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -174,5 +175,49 @@ size_t ffn_max_counters(int d, int n_shared, int inter_shared, int n_routed, int
 // One cooperative launch computing the FFN of every item (and the combine).
 template <class L>
 cudaError_t launch_ffn(const FfnArgs& a, const L& list, cudaStream_t s);
+
+// ---- prefill grouped GEMM (tcgen05) -------------------------------------------
+//
+// A prefill chunk's experts as two grouped GEMMs on the tensor cores:
+// gate/up (h = act(W_g x) * W_u x for every item and token) and down
+// (o = W_d h). Weights are dequantised to fp16 by producer warps; the token
+// rows (x converted to fp16, or h in fp16) are loaded by TMA; accumulators
+// are fp32 in tensor memory. An item is one expert and up to kPfMaxN rows:
+// family 0 is the shared expert over every token (rows 0..T-1), family 1 a
+// routed expert over its pairs, which occupy the sorted positions
+// pb..pb+np-1 (sorted position -> pair index in `pair`).
+
+constexpr int kPfMaxN = 128;
+
+struct PfItem {
+    const uint8_t* w;  // expert blob: gate | up | down in the tiled layout
+    int32_t pb, np;    // first row and row count (sorted positions, or tokens for family 0)
+    int32_t ready;     // ready-flag index, -1 if resident
+    int32_t pad;
+};
+
+struct PfArgs {
+    const PfItem* items;  // device, n_items entries, family 0 first
+    int n_items, n_fam0;
+    int d, act, T, k;
+    int inter[2];         // intermediate size per family
+    const int32_t* pair;  // device [P]: sorted position -> pair index t*k + r
+    __half* h[2];         // gate/up output, fp16: family 0 [T][inter0], family 1 [P][inter1]
+    float* out[2];        // down output, fp32: family 0 -> [T][d] by token, family 1 -> [T*k][d] by pair
+    const uint32_t* ready;
+    uint32_t epoch;
+    unsigned* err;
+};
+
+// Converts the chunk's token rows to fp16 for the gate/up B operand:
+// xs[t] = x[t] for t < T and xg[i] = x[pair[i] / k] for i < P.
+cudaError_t launch_pf_gather(const uint16_t* x, int T, int d, const int32_t* pair, int P, int k, __half* xs,
+                             __half* xg, cudaStream_t s);
+
+// phase 1: gate/up (B rows from xs / xg, K = d); phase 2: down (B rows from
+// h[0] / h[1], K = inter). `rows[f]` is the number of rows of family f's B
+// matrix (T for family 0, P for family 1).
+cudaError_t launch_pf_gemm(const PfArgs& a, int phase, const void* b0, const void* b1, const int rows[2],
+                           cudaStream_t s);
 
 }  // namespace moe

@@ -250,7 +250,8 @@ const char* moe_last_error(void);
  * launch on the launching stream while profiling is on (off by default; it
  * adds event records to the stream). kind: 0 router + top-k, 1 expert FFN
  * (shared and routed experts and the combine), 2 combine, 3 prefill grouped
- * GEMM gate/up, 4 prefill grouped GEMM down. Returns launches, total
+ * GEMM gate/up, 4 prefill grouped GEMM down, 5 prefill token-row conversion
+ * to fp16. Returns launches, total
  * milliseconds and the algorithmic bytes and flops of those launches. Waits
  * for the events. */
 moe_status moe_ctx_set_profiling(moe_ctx* ctx, int32_t on);
