@@ -13,14 +13,16 @@
 //     rows (in each 32-row quarter, even rows gate and odd rows up), so the
 //     epilogue forms h = act(gate) * up from neighbouring lanes;
 //   phase 2 (down): 128 consecutive output rows.
-// Warp roles in a CTA of 512 threads (one CTA per SM, persistent over jobs):
-//   warp 0      bulk copies of the weight records (int4 codes with their
-//               scales) of 4 K-blocks per row tile at a time, into a raw ring;
-//   warp 1      TMEM allocation and, from one thread, the MMA issue;
-//   warp 2      TMA loads of the token rows (128B-swizzled fp16) per K-block;
+// Warp roles in a CTA of 576 threads (one CTA per SM, persistent over jobs):
+//   warps 0-3   MMA issue, one thread each (one thread issues a tcgen05.mma
+//               only every ~125 cycles, a third of the tensor pipe's rate for
+//               these small tiles); warp 0 also allocates TMEM;
 //   warps 4-7   epilogue, one TMEM lane quarter each;
 //   warps 8-15  dequantisation: int4 -> fp16 w = fp16(s * q + b), written into
-//               the 128B-swizzled K-major A tile.
+//               the 128B-swizzled K-major A tile;
+//   warp 16     bulk copies of the weight records (int4 codes with their
+//               scales) of 4 K-blocks per row tile at a time, into a raw ring;
+//   warp 17     TMA loads of the token rows (128B-swizzled fp16).
 // Copies are few and large (a bulk copy costs its issuing thread tens of
 // nanoseconds whatever its size), and the two producers issue in parallel.
 // Every wait is bounded; on expiry the kernel records an error bit, raises an
@@ -40,9 +42,11 @@ namespace moe {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kThreads = 512;
-constexpr int kWarpLoad = 0, kWarpMma = 1, kWarpB = 2, kWarpEpi = 4, kWarpDq = 8, kDqWarps = 8;
-constexpr int kStages = 4;     // A/B ring, one K-block (64) per stage
+constexpr int kThreads = 576;
+// warps 0-3 issue MMAs (one thread each), 4-7 epilogue, 8-15 dequantise, 16 and 17 load
+constexpr int kIssuers = 4, kWarpEpi = 4, kWarpDq = 8, kDqWarps = 8, kWarpLoad = 16, kWarpB = 17;
+constexpr int kStages = 4;     // A ring, one K-block (64) per stage
+constexpr int kSlotsB = 4;     // B ring: a slot holds as many K-blocks of the job's rows as fit in 16 KB
 constexpr int kRawStages = 4;  // raw ring, kUnit K-blocks per stage
 constexpr int kUnit = 4;
 constexpr int kTileM = 128;
@@ -50,9 +54,16 @@ constexpr int kRecord = 1152;           // 32 rows x 64 codes, then 32 scale/bia
 constexpr int kABytes = kTileM * 128;   // 128 rows x 64 fp16, 128B-swizzled
 constexpr int kBBytes = kPfMaxN * 128;  // up to 128 token rows x 64 fp16
 constexpr int kRawBytes = 4 * kUnit * kRecord;  // 4 row tiles x kUnit records
-constexpr int kTmemCols = 2 * kPfMaxN;  // two accumulators of up to 128 fp32 columns
+// Two accumulator buffers of 256 fp32 columns. A job's K-blocks are dealt to
+// nI issuers in turn (nI = 4 for up to 64 token rows, else 2), each issuer
+// accumulating into its own 256/nI columns of the buffer; the epilogue sums them.
+constexpr int kTmemCols = 512;
+// With fewer A stages than issuers, runs of jobs whose K-block count is not a
+// multiple of the issuer count stalled until the bounded waits expired (seen
+// with 4 issuers over 3 stages and 11 K-blocks per job); keep them at least equal.
+static_assert(kStages >= kIssuers, "the A ring needs at least one stage per MMA issuer");
 // shared memory: A ring, B ring, raw ring, barriers, TMEM address; +1 KB to align
-constexpr int kSmemBytes = 1024 + kStages * (kABytes + kBBytes) + kRawStages * kRawBytes + 256;
+constexpr int kSmemBytes = 1024 + kStages * kABytes + kSlotsB * kBBytes + kRawStages * kRawBytes + 256;
 
 // Shared-memory matrix descriptor of a K-major operand tile whose rows are 128
 // bytes apart with the 128-byte swizzle (8-row atoms of 1024 bytes).
@@ -162,14 +173,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     unsigned char* ringA = smem;
     unsigned char* ringB = ringA + kStages * kABytes;
-    unsigned char* ringR = ringB + kStages * kBBytes;
+    unsigned char* ringR = ringB + kSlotsB * kBBytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(ringR + kRawStages * kRawBytes);
-    uint64_t* raw_full = bars;                // [kRawStages] records landed
+    uint64_t* raw_full = bars;                    // [kRawStages] records landed
     uint64_t* raw_empty = raw_full + kRawStages;  // [kRawStages] records dequantised
-    uint64_t* b_full = raw_empty + kRawStages;    // [kStages] token rows landed
-    uint64_t* a_full = b_full + kStages;          // [kStages] A tile dequantised
-    uint64_t* ab_empty = a_full + kStages;        // [kStages] MMAs reading the stage done
-    uint64_t* acc_full = ab_empty + kStages;      // [2] accumulator complete
+    uint64_t* b_full = raw_empty + kRawStages;    // [kSlotsB] token rows landed
+    uint64_t* b_empty = b_full + kSlotsB;         // [kSlotsB] MMAs reading the slot done
+    uint64_t* a_full = b_empty + kSlotsB;         // [kStages] A tile dequantised
+    uint64_t* a_empty = a_full + kStages;         // [kStages] MMAs reading the stage done
+    uint64_t* acc_full = a_empty + kStages;       // [2] accumulator complete
     uint64_t* acc_empty = acc_full + 2;           // [2] accumulator read out
     uint64_t* drain = acc_empty + 2;              // [1] every MMA of the CTA done
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -183,20 +195,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(raw_full + i, 1);
             ptx::mbar_init(raw_empty + i, kDqWarps);
         }
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < kSlotsB; ++i) {
             ptx::mbar_init(b_full + i, 1);
+            ptx::mbar_init(b_empty + i, kIssuers);
+        }
+        for (int i = 0; i < kStages; ++i) {
             ptx::mbar_init(a_full + i, kDqWarps);
-            ptx::mbar_init(ab_empty + i, 1);
+            ptx::mbar_init(a_empty + i, 1);
         }
         for (int i = 0; i < 2; ++i) {
-            ptx::mbar_init(acc_full + i, 1);
+            ptx::mbar_init(acc_full + i, kIssuers);
             ptx::mbar_init(acc_empty + i, 4);
         }
-        ptx::mbar_init(drain, 1);
+        ptx::mbar_init(drain, kIssuers);
         abort_flag = 0;
         ptx::fence_mbar_init();
     }
-    if (warp == kWarpMma) {
+    if (warp == 0) {
         ptx::tmem_alloc(tmem_slot, kTmemCols);
         ptx::tmem_relinquish();
     }
@@ -208,6 +223,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto fail = [&](unsigned bit) {
         atomicOr(a.err, bit);
         abort_flag = 1;
+    };
+    // diagnostics: the first kPfFailRecords expired waits of the launch, as
+    // (block << 48 | warp << 40 | what << 32 | job << 16 | K-block), what =
+    // 1 raw_empty, 2 b_empty, 3 acc_empty, 4 b_full, 5 a_full, 6 acc_full, 7 raw_full, 8 a_empty
+    auto record = [&](int what, int job, int kb) {
+        if (!a.trace) return;
+        unsigned long long* rec = a.trace + kPfTraceKb * kPfTracePoints;
+        const unsigned k = atomicAdd(reinterpret_cast<unsigned*>(rec), 1u);
+        if (k < kPfFailRecords)
+            rec[1 + k] = ((unsigned long long)blockIdx.x << 48) | ((unsigned long long)warp << 40) |
+                         ((unsigned long long)what << 32) | ((unsigned long long)(job & 0xFFFF) << 16) | (kb & 0xFFFF);
     };
 
     if (warp == kWarpLoad) {
@@ -232,7 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int nkb = P.kblocks[b.fam];
                 for (int kb0 = 0; kb0 < nkb; kb0 += kUnit) {
                     const int nu = min(kUnit, nkb - kb0);
-                    if (!ptx::mbar_wait_bounded(raw_empty + r, ph ^ 1, abortp)) {
+                    if (!ptx::mbar_wait_sleep(raw_empty + r, ph ^ 1, abortp)) {
+                        record(1, j, kb0);
                         if (!*abortp) fail(32u);
                         ok = false;
                         break;
@@ -279,69 +306,106 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Job b = decode_job(P, a, j);
                 const PfItem it = a.items[b.item];
                 const int nb = pad16(it.np);
-                for (int kb = 0; kb < P.kblocks[b.fam]; ++kb) {
-                    if (!ptx::mbar_wait_bounded(ab_empty + s, ph ^ 1, abortp)) {
+                const int kpb = kPfMaxN / nb;  // K-blocks per slot
+                const int nkb = P.kblocks[b.fam];
+                for (int kb0 = 0; kb0 < nkb; kb0 += kpb) {
+                    const int nk = min(kpb, nkb - kb0);
+                    if (!ptx::mbar_wait_sleep(b_empty + s, ph ^ 1, abortp)) {
+                        record(2, j, kb0);
                         if (!*abortp) fail(512u);
                         ok = false;
                         break;
                     }
                     unsigned char* bt = ringB + s * kBBytes;
-                    ptx::mbar_arrive_expect_tx(b_full + s, (uint32_t)(nb * 128));
-                    if (b.fam == 0) {
-                        ptx::tma_load_2d(bt, &map0, kb * 64, 0, b_full + s);  // one box of all the rows
-                    } else {
-                        for (int r0 = 0; r0 < nb; r0 += 16)
-                            ptx::tma_load_2d(bt + r0 * 128, &map1, kb * 64, it.pb + r0, b_full + s);
+                    ptx::mbar_arrive_expect_tx(b_full + s, (uint32_t)(nk * nb * 128));
+                    for (int kk = 0; kk < nk; ++kk) {
+                        unsigned char* dst = bt + kk * nb * 128;
+                        const int x = (kb0 + kk) * 64;
+                        if (b.fam == 0) {
+                            ptx::tma_load_2d(dst, &map0, x, 0, b_full + s);  // one box of all the rows
+                        } else {
+                            for (int r0 = 0; r0 < nb; r0 += 16)
+                                ptx::tma_load_2d(dst + r0 * 128, &map1, x, it.pb + r0, b_full + s);
+                        }
                     }
                     ++issued;
-                    if (++s == kStages) {
+                    if (++s == kSlotsB) {
                         s = 0;
                         ph ^= 1;
                     }
                 }
             }
             if (!ok) {
-                for (int i = 0; i < kStages && i < issued; ++i) {
+                for (int i = 0; i < kSlotsB && i < issued; ++i) {
                     int sl = s - 1 - i;
                     uint32_t par = ph;
                     if (sl < 0) {
-                        sl += kStages;
+                        sl += kSlotsB;
                         par ^= 1;
                     }
                     ptx::mbar_wait_bounded(b_full + sl, par, nullptr);
                 }
             }
         }
-    } else if (warp == kWarpMma) {
+    } else if (warp < kIssuers) {
         // ---------------- MMA issue ----------------
         if (lane == 0) {
-            int s = 0;
-            uint32_t ph = 0;
+            const int i = warp;  // this issuer
+            int s = 0, sb = 0;
+            uint32_t ph = 0, bph = 0;
             int njob = 0;
             for (int j = blockIdx.x; j < P.n_jobs; j += gridDim.x, ++njob) {
                 const Job b = decode_job(P, a, j);
                 const int nb = pad16(a.items[b.item].np);
+                const int kpb = kPfMaxN / nb;
+                const int nkb = P.kblocks[b.fam];
+                const int nI = nb <= 64 ? 4 : 2;
                 const int buf = njob & 1;
                 const uint32_t idesc = f16_idesc(kTileM, nb);
-                const uint32_t d_tmem = tmem + buf * kPfMaxN;
+                const uint32_t d_tmem = tmem + buf * 256 + i * (256 / nI);
                 // the epilogue must have read this accumulator's previous job
-                bool ok = ptx::mbar_wait_bounded(acc_empty + buf, ((njob >> 1) & 1) ^ 1, abortp);
+                bool ok = ptx::mbar_wait_sleep(acc_empty + buf, ((njob >> 1) & 1) ^ 1, abortp);
+                if (!ok) record(3, j, 0);
                 ptx::tc_fence_after();
-                for (int kb = 0; kb < P.kblocks[b.fam]; ++kb) {
-                    ok = ok && ptx::mbar_wait_bounded(b_full + s, ph, abortp) &&
-                         ptx::mbar_wait_bounded(a_full + s, ph, abortp);
-                    if (ok) {
-                        ptx::tc_fence_after();
-                        const uint64_t ad = sw128_desc(ptx::smem_addr(ringA + s * kABytes));
-                        const uint64_t bd = sw128_desc(ptx::smem_addr(ringB + s * kBBytes));
+                bool first = true;
+                for (int kb = 0; kb < nkb; ++kb) {
+                    const int kk = kb % kpb;  // K-block within the B slot
+                    // Every issuer sees each round of a slot filled before it
+                    // arrives on the slot's release, owner of a K-block in it or
+                    // not: an arrival may then only count toward that round.
+                    if (kk == 0 && ok && !ptx::mbar_wait_bounded(b_full + sb, bph, abortp)) {
+                        ok = false;
+                        record(4, j, kb);
+                    }
+                    if (i < nI && kb % nI == i) {
+                        if (ok && !ptx::mbar_wait_bounded(a_full + s, ph, abortp)) {
+                            ok = false;
+                            record(5, j, kb);
+                        }
+                        const bool trace = a.trace && blockIdx.x == 0 && njob == 0 && kb < kPfTraceKb;
+                        if (trace) a.trace[3 * kPfTraceKb + kb] = ptx::globaltimer();
+                        if (ok) {
+                            ptx::tc_fence_after();
+                            const uint64_t ad = sw128_desc(ptx::smem_addr(ringA + s * kABytes));
+                            const uint64_t bd = sw128_desc(ptx::smem_addr(ringB + sb * kBBytes + kk * nb * 128));
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)  // K = 16 per MMA: +32 bytes in the swizzled row
-                            ptx::mma_f16_ss(d_tmem, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
-                        ptx::mma_commit(ab_empty + s);
+                            for (int k = 0; k < 4; ++k)  // K = 16 per MMA: +32 bytes in the swizzled row
+                                ptx::mma_f16_ss(d_tmem, ad + 2 * k, bd + 2 * k, idesc, !(first && k == 0));
+                            first = false;
+                            ptx::mma_commit(a_empty + s);
+                            if (trace) a.trace[4 * kPfTraceKb + kb] = ptx::globaltimer();
+                        }
                     }
                     if (++s == kStages) {
                         s = 0;
                         ph ^= 1;
+                    }
+                    if (kk == kpb - 1 || kb == nkb - 1) {  // last K-block of the slot: every issuer arrives
+                        if (ok) ptx::mma_commit(b_empty + sb);
+                        if (++sb == kSlotsB) {
+                            sb = 0;
+                            bph ^= 1;
+                        }
                     }
                 }
                 if (ok) {
@@ -363,20 +427,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             const PfItem it = a.items[b.item];
             const int nb = pad16(it.np);
             const int buf = njob & 1;
-            if (!__all_sync(kFull, ptx::mbar_wait_bounded(acc_full + buf, (njob >> 1) & 1, abortp))) {
+            if (!__all_sync(kFull, ptx::mbar_wait_sleep(acc_full + buf, (njob >> 1) & 1, abortp))) {
+                if (lane == 0) record(6, j, 0);
                 if (lane == 0 && !*abortp) fail(256u);
                 break;
             }
             ptx::tc_fence_after();
-            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * kPfMaxN;
+            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * 256;
+            const int nI = nb <= 64 ? 4 : 2;
+            const int used = min(nI, P.kblocks[b.fam]);  // issuers that accumulated anything
+            // v = the sum of the issuers' accumulators for 16 columns from c, in issuer order
+            auto load_sum = [&](int c, uint32_t (&v)[16]) {
+                ptx::tmem_ld16(taddr + c, v);
+                for (int i = 1; i < used; ++i) {
+                    uint32_t w[16];
+                    ptx::tmem_ld16(taddr + i * (256 / nI) + c, w);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) v[m] = __float_as_uint(__uint_as_float(v[m]) + __uint_as_float(w[m]));
+                }
+                ptx::tmem_ld_wait();
+            };
             if (phase == 1) {
                 const int I = a.inter[b.fam];
                 const int irow = 64 * b.tile + 16 * q + (lane >> 1);
                 __half* hb = a.h[b.fam];
                 for (int c = 0; c < nb; c += 16) {
                     uint32_t v[16];
-                    ptx::tmem_ld16(taddr + c, v);
-                    ptx::tmem_ld_wait();
+                    load_sum(c, v);
                     // even lanes hold gate rows, odd lanes the matching up rows:
                     // the even lane finishes columns c..c+7, the odd lane c+8..c+15
                     const bool odd = lane & 1;
@@ -393,8 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int n = kTileM * b.tile + 32 * q + lane;
                 for (int c = 0; c < nb; c += 16) {
                     uint32_t v[16];
-                    ptx::tmem_ld16(taddr + c, v);
-                    ptx::tmem_ld_wait();
+                    load_sum(c, v);
 #pragma unroll
                     for (int m = 0; m < 16; ++m) {
                         const int col = c + m;
@@ -426,17 +503,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sb_off = tile_raw * kUnit * kRecord + 1024 + rlane * 4;
         int r = 0, s = 0;
         uint32_t rph = 0, ph = 0;
-        for (int j = blockIdx.x; j < P.n_jobs; j += gridDim.x) {
+        const bool tracer = a.trace && blockIdx.x == 0 && t == 0;
+        const bool wtracer = a.trace && blockIdx.x == 0 && lane == 0;
+        for (int j = blockIdx.x, njob = 0; j < P.n_jobs; j += gridDim.x, ++njob) {
             const Job b = decode_job(P, a, j);
             const int nkb = P.kblocks[b.fam];
             for (int kb0 = 0; kb0 < nkb; kb0 += kUnit) {
                 const int nu = min(kUnit, nkb - kb0);
-                const bool have = ptx::mbar_wait_bounded(raw_full + r, rph, abortp);
+                const bool have = ptx::mbar_wait_sleep(raw_full + r, rph, abortp);
+                if (!have && lane == 0) record(7, j, kb0);
                 if (!have && lane == 0 && !*abortp) fail(64u);
                 const unsigned char* raw = ringR + r * kRawBytes;
                 for (int u = 0; u < nu; ++u) {
+                    const bool trace = tracer && njob == 0 && kb0 + u < kPfTraceKb;
+                    if (trace) a.trace[0 * kPfTraceKb + kb0 + u] = ptx::globaltimer();
                     // the A stage is free once the MMAs that read it are done
-                    const bool free_a = have && ptx::mbar_wait_bounded(ab_empty + s, ph ^ 1, abortp);
+                    const bool free_a = have && ptx::mbar_wait_bounded(a_empty + s, ph ^ 1, abortp);
+                    if (trace) a.trace[1 * kPfTraceKb + kb0 + u] = ptx::globaltimer();
                     if (free_a) {
                         const uint4 cw = *reinterpret_cast<const uint4*>(raw + codes_off + u * kRecord);
                         const uint32_t sbw = *reinterpret_cast<const uint32_t*>(raw + sb_off + u * kRecord);
@@ -450,11 +533,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             *reinterpret_cast<uint4*>(arow + ((chunk ^ (rho & 7)) << 4)) = dequant8(words[w], s2, b2);
                         }
                         ptx::fence_proxy_async_smem();  // generic-proxy writes, read next by the tensor core
-                    } else if (have && lane == 0 && !*abortp) {
-                        fail(64u);
+                    } else if (have && lane == 0) {
+                        record(8, j, kb0 + u);
+                        if (!*abortp) fail(64u);
                     }
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(a_full + s);
+                    if (trace) a.trace[2 * kPfTraceKb + kb0 + u] = ptx::globaltimer();
+                    if (wtracer && njob == 0 && kb0 + u < kPfTraceKb)
+                        a.trace[(5 + warp - kWarpDq) * kPfTraceKb + kb0 + u] = ptx::globaltimer();
                     if (++s == kStages) {
                         s = 0;
                         ph ^= 1;
@@ -472,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == kWarpMma) {
+    if (warp == 0) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, kTmemCols);
     }

@@ -207,7 +207,16 @@ struct PfArgs {
     const uint32_t* ready;
     uint32_t epoch;
     unsigned* err;
+    // optional diagnostics: block 0 records %globaltimer for the first
+    // kPfTraceKb K-blocks of its first job at kPfTracePoints moments (raw
+    // records landed, A stage free, A stage written, MMA inputs ready, MMAs
+    // committed, then A stage written by each of the 8 dequantising warps);
+    // null = off
+    unsigned long long* trace;
 };
+constexpr int kPfTraceKb = 64;
+constexpr int kPfTracePoints = 13;
+constexpr int kPfFailRecords = 31;  // after the trace points: a count, then records
 
 // Converts the chunk's token rows to fp16 for the gate/up B operand:
 // xs[t] = x[t] for t < T and xg[i] = x[pair[i] / k] for i < P.
