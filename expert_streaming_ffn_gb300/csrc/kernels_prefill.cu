@@ -13,16 +13,17 @@
 //     rows (in each 32-row quarter, even rows gate and odd rows up), so the
 //     epilogue forms h = act(gate) * up from neighbouring lanes;
 //   phase 2 (down): 128 consecutive output rows.
-// Warp roles in a CTA of 576 threads (one CTA per SM, persistent over jobs):
+// Warp roles in a CTA of 832 threads (one CTA per SM, persistent over jobs):
 //   warps 0-3   MMA issue, one thread each (one thread issues a tcgen05.mma
 //               only every ~125 cycles, a third of the tensor pipe's rate for
 //               these small tiles); warp 0 also allocates TMEM;
 //   warps 4-7   epilogue, one TMEM lane quarter each;
-//   warps 8-15  dequantisation: int4 -> fp16 w = fp16(s * q + b), written into
-//               the 128B-swizzled K-major A tile;
-//   warp 16     bulk copies of the weight records (int4 codes with their
+//   warps 8-23  dequantisation in two groups of 8 warps that take alternate
+//               K-blocks: int4 -> fp16 w = fp16(s * q + b), written into the
+//               128B-swizzled K-major A tile;
+//   warp 24     bulk copies of the weight records (int4 codes with their
 //               scales) of 4 K-blocks per row tile at a time, into a raw ring;
-//   warp 17     TMA loads of the token rows (128B-swizzled fp16).
+//   warp 25     TMA loads of the token rows (128B-swizzled fp16).
 // Copies are few and large (a bulk copy costs its issuing thread tens of
 // nanoseconds whatever its size), and the two producers issue in parallel.
 // Every wait is bounded; on expiry the kernel records an error bit, raises an
@@ -42,9 +43,10 @@ namespace moe {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kThreads = 576;
-// warps 0-3 issue MMAs (one thread each), 4-7 epilogue, 8-15 dequantise, 16 and 17 load
-constexpr int kIssuers = 4, kWarpEpi = 4, kWarpDq = 8, kDqWarps = 8, kWarpLoad = 16, kWarpB = 17;
+constexpr int kThreads = 832;
+// warps 0-3 issue MMAs (one thread each), 4-7 epilogue, 8-23 dequantise (two
+// groups of 8, alternate K-blocks), 24 and 25 load
+constexpr int kIssuers = 4, kWarpEpi = 4, kWarpDq = 8, kDqWarps = 8, kDqGroups = 2, kWarpLoad = 24, kWarpB = 25;
 constexpr int kStages = 4;     // A ring, one K-block (64) per stage
 constexpr int kSlotsB = 4;     // B ring: a slot holds as many K-blocks of the job's rows as fit in 16 KB
 constexpr int kRawStages = 4;  // raw ring, kUnit K-blocks per stage
@@ -62,6 +64,7 @@ constexpr int kTmemCols = 512;
 // multiple of the issuer count stalled until the bounded waits expired (seen
 // with 4 issuers over 3 stages and 11 K-blocks per job); keep them at least equal.
 static_assert(kStages >= kIssuers, "the A ring needs at least one stage per MMA issuer");
+static_assert(kStages % kDqGroups == 0, "each dequantising group owns whole A stages");
 // shared memory: A ring, B ring, raw ring, barriers, TMEM address; +1 KB to align
 constexpr int kSmemBytes = 1024 + kStages * kABytes + kSlotsB * kBBytes + kRawStages * kRawBytes + 256;
 
@@ -193,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < kRawStages; ++i) {
             ptx::mbar_init(raw_full + i, 1);
-            ptx::mbar_init(raw_empty + i, kDqWarps);
+            ptx::mbar_init(raw_empty + i, kDqGroups * kDqWarps);
         }
         for (int i = 0; i < kSlotsB; ++i) {
             ptx::mbar_init(b_full + i, 1);
@@ -265,6 +268,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     unsigned char* raw = ringR + r * kRawBytes;
+                    // diagnostics: when block 0 issues each unit of its first two jobs (slot 1 of kb0's row)
+                    if (a.trace && blockIdx.x == 0 && issued < kPfTraceKb / kUnit)
+                        a.trace[0 * kPfTraceKb + issued * kUnit + 1] = ptx::globaltimer();
                     ptx::mbar_arrive_expect_tx(raw_full + r, (uint32_t)(4 * nu * kRecord));
                     for (int t = 0; t < 4; ++t) {
                         // row tile t of the job: phase 1 gate 2i, gate 2i+1, up 2i, up 2i+1; phase 2 down 4i+t
@@ -373,12 +379,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // Every issuer sees each round of a slot filled before it
                     // arrives on the slot's release, owner of a K-block in it or
                     // not: an arrival may then only count toward that round.
-                    if (kk == 0 && ok && !ptx::mbar_wait_bounded(b_full + sb, bph, abortp)) {
+                    if (kk == 0 && ok && !ptx::mbar_wait_sleep(b_full + sb, bph, abortp)) {
                         ok = false;
                         record(4, j, kb);
                     }
                     if (i < nI && kb % nI == i) {
-                        if (ok && !ptx::mbar_wait_bounded(a_full + s, ph, abortp)) {
+                        if (ok && !ptx::mbar_wait_sleep(a_full + s, ph, abortp)) {
                             ok = false;
                             record(5, j, kb);
                         }
@@ -485,9 +491,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(acc_empty + buf);
         }
-    } else if (warp >= kWarpDq) {
+    } else if (warp >= kWarpDq && warp < kWarpDq + kDqGroups * kDqWarps) {
         // ---------------- dequantisation ----------------
-        const int t = threadIdx.x - kWarpDq * 32;  // 0..255: A row t / 2, half t % 2 of the K-block
+        // group g takes the K-blocks whose running index is g mod 2, i.e. the A
+        // stages g and g + 2; within a group, thread t has A row t / 2, half t % 2
+        const int grp = (warp - kWarpDq) / kDqWarps, wg = (warp - kWarpDq) % kDqWarps;
+        const int t = wg * 32 + lane;
         const int rho = t >> 1, hh = t & 1;
         int tile_raw, rlane;
         if (phase == 1) {
@@ -501,9 +510,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int codes_off = tile_raw * kUnit * kRecord + hh * 512 + rlane * 16;
         const int sb_off = tile_raw * kUnit * kRecord + 1024 + rlane * 4;
+        const int swz = rho & 7;
         int r = 0, s = 0;
         uint32_t rph = 0, ph = 0;
-        const bool tracer = a.trace && blockIdx.x == 0 && t == 0;
+        const bool tracer = a.trace && blockIdx.x == 0 && grp == 0 && t == 0;
         const bool wtracer = a.trace && blockIdx.x == 0 && lane == 0;
         for (int j = blockIdx.x, njob = 0; j < P.n_jobs; j += gridDim.x, ++njob) {
             const Job b = decode_job(P, a, j);
@@ -514,34 +524,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!have && lane == 0) record(7, j, kb0);
                 if (!have && lane == 0 && !*abortp) fail(64u);
                 const unsigned char* raw = ringR + r * kRawBytes;
-                for (int u = 0; u < nu; ++u) {
-                    const bool trace = tracer && njob == 0 && kb0 + u < kPfTraceKb;
-                    if (trace) a.trace[0 * kPfTraceKb + kb0 + u] = ptx::globaltimer();
-                    // the A stage is free once the MMAs that read it are done
-                    const bool free_a = have && ptx::mbar_wait_bounded(a_empty + s, ph ^ 1, abortp);
-                    if (trace) a.trace[1 * kPfTraceKb + kb0 + u] = ptx::globaltimer();
-                    if (free_a) {
-                        const uint4 cw = *reinterpret_cast<const uint4*>(raw + codes_off + u * kRecord);
-                        const uint32_t sbw = *reinterpret_cast<const uint32_t*>(raw + sb_off + u * kRecord);
-                        const __half2 s2 = __half2half2(__ushort_as_half((unsigned short)(sbw & 0xFFFFu)));
-                        const __half2 b2 = __half2half2(__ushort_as_half((unsigned short)(sbw >> 16)));
-                        unsigned char* arow = ringA + s * kABytes + rho * 128;
-                        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+                // this group's K-blocks of the unit: stage s + u is ours when (s + u) % 2 == grp
+                const int u0 = ((s & 1) == grp) ? 0 : 1;
+                uint4 cw[2];
+                uint32_t sbw[2];
 #pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            const int chunk = 4 * hh + w;  // 16-byte chunk (8 elements) of the 128-byte row
-                            *reinterpret_cast<uint4*>(arow + ((chunk ^ (rho & 7)) << 4)) = dequant8(words[w], s2, b2);
-                        }
-                        ptx::fence_proxy_async_smem();  // generic-proxy writes, read next by the tensor core
-                    } else if (have && lane == 0) {
-                        record(8, j, kb0 + u);
-                        if (!*abortp) fail(64u);
+                for (int m = 0; m < 2; ++m) {
+                    const int u = u0 + 2 * m;
+                    if (have && u < nu) {
+                        cw[m] = *reinterpret_cast<const uint4*>(raw + codes_off + u * kRecord);
+                        sbw[m] = *reinterpret_cast<const uint32_t*>(raw + sb_off + u * kRecord);
                     }
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(a_full + s);
-                    if (trace) a.trace[2 * kPfTraceKb + kb0 + u] = ptx::globaltimer();
-                    if (wtracer && njob == 0 && kb0 + u < kPfTraceKb)
-                        a.trace[(5 + warp - kWarpDq) * kPfTraceKb + kb0 + u] = ptx::globaltimer();
+                }
+                for (int u = 0; u < nu; ++u) {
+                    if (((s & 1) == grp)) {
+                        const int m = (u - u0) >> 1;
+                        const bool trace = tracer && njob == 0 && kb0 + u < kPfTraceKb;
+                        if (trace) a.trace[0 * kPfTraceKb + kb0 + u] = ptx::globaltimer();
+                        // the A stage is free once the MMAs that read it are done
+                        const bool free_a = have && ptx::mbar_wait_sleep(a_empty + s, ph ^ 1, abortp);
+                        if (trace) a.trace[1 * kPfTraceKb + kb0 + u] = ptx::globaltimer();
+                        if (free_a) {
+                            const uint4 c = m ? cw[1] : cw[0];
+                            const uint32_t w = m ? sbw[1] : sbw[0];
+                            const __half2 s2 = __half2half2(__ushort_as_half((unsigned short)(w & 0xFFFFu)));
+                            const __half2 b2 = __half2half2(__ushort_as_half((unsigned short)(w >> 16)));
+                            unsigned char* arow = ringA + s * kABytes + rho * 128;
+                            const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)  // 16-byte chunk 4 hh + q (8 elements) of the 128-byte row
+                                *reinterpret_cast<uint4*>(arow + (((4 * hh + q) ^ swz) << 4)) = dequant8(words[q], s2, b2);
+                            ptx::fence_proxy_async_smem();  // generic-proxy writes, read next by the tensor core
+                        } else if (have && lane == 0) {
+                            record(8, j, kb0 + u);
+                            if (!*abortp) fail(64u);
+                        }
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(a_full + s);
+                        if (trace) a.trace[2 * kPfTraceKb + kb0 + u] = ptx::globaltimer();
+                        if (wtracer && njob == 0 && kb0 + u < kPfTraceKb)
+                            a.trace[(5 + wg) * kPfTraceKb + kb0 + u] = ptx::globaltimer();
+                    }
                     if (++s == kStages) {
                         s = 0;
                         ph ^= 1;
