@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (testing only)")
     ap.add_argument("--prefill-layers", type=int, default=2)
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="run only the prefill leg and print its JSON (for profiling; not the bench line)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -533,6 +535,18 @@ def main():
     world, rank, local = dist_init()
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.prefill_only:
+        import torch
+
+        import expert_streaming_ffn_gb300 as moe
+
+        torch.cuda.set_device(local)
+        moe.load()
+        ctx = moe.moe_ctx_create(local)
+        out = run_prefill(args, ctx, torch.device("cuda", local), torch.cuda.current_stream(), 1000 * rank)
+        moe.moe_ctx_destroy(ctx)
+        if rank == 0:
+            print(json.dumps({"prefill": out}), flush=True)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

@@ -167,6 +167,9 @@ struct moe_layer {
     StepResult step;
     cudaEvent_t ev_done = nullptr;     // end of the layer's last call
     cudaEvent_t ev_pending = nullptr;  // copies issued by moe_cache_step
+    bool pending = false;              // ev_pending recorded since the last forward
+    cudaStream_t last_stream = nullptr;  // stream of the last call that recorded ev_done
+    bool have_last_stream = false;
     bool loaded = false;
     // scratch, sized for cap_T tokens per call
     int cap_T = 0;
@@ -685,8 +688,13 @@ moe_status forward_chunk(moe_layer* L, const uint16_t* x, int T, const float* zb
     const moe_shapes& sh = L->sh;
     const int npairs = T * sh.top_k;
     auto t0 = std::chrono::steady_clock::now();
-    CUDA_TRY(cudaStreamWaitEvent(s, L->ev_done, 0));
-    CUDA_TRY(cudaStreamWaitEvent(s, L->ev_pending, 0));
+    // the layer's previous call and any copies moe_cache_step issued come first;
+    // a call on the stream that recorded ev_done is already ordered after it
+    if (!L->have_last_stream || L->last_stream != s) CUDA_TRY(cudaStreamWaitEvent(s, L->ev_done, 0));
+    if (L->pending) {
+        CUDA_TRY(cudaStreamWaitEvent(s, L->ev_pending, 0));
+        L->pending = false;
+    }
     if (L->err_generation != C->err_generation) {
         // an earlier kernel abandoned a wait: restore the all-zero counters
         CUDA_TRY(cudaMemsetAsync(L->d_fcount, 0, sizeof(unsigned) * L->n_fcount, s));
@@ -726,6 +734,8 @@ moe_status forward_chunk(moe_layer* L, const uint16_t* x, int T, const float* zb
     if (gates_out)
         CUDA_TRY(cudaMemcpyAsync(gates_out, L->d_gates, sizeof(float) * npairs, cudaMemcpyDeviceToDevice, s));
     CUDA_TRY(cudaEventRecord(L->ev_done, s));
+    L->last_stream = s;
+    L->have_last_stream = true;
     if (L->step.bypass > 0) CUDA_TRY(cudaEventRecord(C->staging_free, s));
     L->stats.host_issue_us += us_since(t0);
     return MOE_OK;
@@ -924,6 +934,8 @@ extern "C" moe_status moe_route(moe_layer* L, const void* x, int32_t T, const fl
                         ids + (size_t)t0 * L->sh.top_k, gates + (size_t)t0 * L->sh.top_k, false, s);
         if (st != MOE_OK) return st;
         CUDA_TRY(cudaEventRecord(L->ev_done, s));
+        L->last_stream = s;
+        L->have_last_stream = true;
     }
     return MOE_OK;
 }
@@ -943,6 +955,7 @@ extern "C" moe_status moe_cache_step(moe_layer* L, const int32_t* ids, int32_t n
     moe_status st = issue_miss_copies(L, L->step, false, ++L->epoch, nullptr);
     // the next forward treats these experts as resident: it waits for the copies first
     cudaError_t e = cudaEventRecord(L->ev_pending, L->ctx->copy_stream);
+    L->pending = true;
     if (slot_of)
         for (int i = 0; i < n_ids; ++i) slot_of[i] = L->cache.slot_of(ids[i]);
     for (size_t i = 0; i < L->step.miss_experts.size(); ++i) {

@@ -197,10 +197,12 @@ moe_status moe_cache_step(moe_layer* layer, const int32_t* ids, int32_t n_ids, i
  *   after their ready events) -> y[t] = shared(x_t) + sum_{r<k} gate[t][r] *
  *   FFN_{ids[t][r]}(x_t), the routed terms added in rank order.
  *   FFN_e(x) = W_down,e (act(W_gate,e x) * (W_up,e x)); fp32 accumulation.
- * T <= 64 runs the decode path (fused dequant GEMV kernels); larger T runs as
- * prefill in chunks of 128 tokens, each chunk routed, cached and grouped by
- * expert before the grouped expert GEMMs ([P1] §2.5, §8.4). Bypassed experts
- * are streamed into the context's staging arena.
+ * T <= 64 runs the decode path (fused dequant GEMV kernels, fp32 arithmetic);
+ * larger T runs as prefill in chunks of 128 tokens, each chunk routed, cached
+ * and grouped by expert before the grouped expert GEMMs on the tensor cores
+ * ([P1] §2.5, §8.4), whose operands are fp16 (weights fp16(s*q + b), x, and h
+ * rounded to fp16) with fp32 accumulation. Bypassed experts are streamed into
+ * the context's staging arena.
  * x: device bf16 [T][d_model]; zbias: device f32 [E] or NULL; y: device f32
  * [T][d_model]. Optional ids_out (device int32 [T][k]) and gates_out (device
  * f32 [T][k]) receive the routing; pass NULL to skip.
