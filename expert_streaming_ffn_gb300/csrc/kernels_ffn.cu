@@ -435,8 +435,11 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) ffn_kernel(const __
                 for (int t = 0; t < b.ntiles && ok; ++t) {
                     const int rt = b.rt0 + t;
                     const unsigned char* ra = A + (size_t)rt * (K >> 6) * kRecord;  // the row tile's records
-                    for (int s0 = 0; s0 < b.ng; s0 += kCons) {
-                        const int ng = min(kCons, b.ng - s0);
+                    // a gate/up stage holds kCons groups of both matrices, a down
+                    // stage 2 kCons groups of one
+                    const int gps = two == 2 ? kCons : 2 * kCons;
+                    for (int s0 = 0; s0 < b.ng; s0 += gps) {
+                        const int ng = min(gps, b.ng - s0);
                         const size_t g = (size_t)(b.g0 + s0);
                         if (!ptx::mbar_wait_bounded(empty + slot, phase, abortp)) {
                             ok = false;
@@ -609,9 +612,10 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) ffn_kernel(const __
             for (int m = 0; m < 2; ++m)
 #pragma unroll
                 for (int q = 0; q < NT; ++q) tot[m][q] = 0.0f;
-            for (int s0 = 0; s0 < b.ng; s0 += kCons) {
+            const int gps = mats == 2 ? kCons : 2 * kCons;  // groups per stage
+            for (int s0 = 0; s0 < b.ng; s0 += gps) {
                 const bool active = s0 + warp < b.ng;
-                const int c = s0 / kCons;  // this warp's staged group slot
+                const int c = s0 / kCons;  // this warp's staged group slot (down: c and c + 1)
                 const bool ok = ptx::mbar_wait_bounded(full + slot, phase, abortp);
                 if (tr && warp == 0 && lane == 0 && tr[1] == 0) tr[1] = ptx::globaltimer();
                 if (!ok && lane == 0) {
@@ -639,13 +643,18 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) ffn_kernel(const __
                             tot[1][q] += fmaf(fu.x, pr[1][q], fu.y * xq);
                         }
                     } else {
-                        const uint4 c0[1] = {*reinterpret_cast<const uint4*>(cb)};
-                        const uint4 c1[1] = {*reinterpret_cast<const uint4*>(cb + 512)};
-                        const float2 f = unpack_sb(*reinterpret_cast<const uint32_t*>(sbp));
-                        float pr[1][NT];
-                        group_dot<NT, 1>(c0, c1, xg, xs_stride, pr);
+                        // this warp's groups of the stage: s0 + warp and s0 + kCons + warp
+                        for (int hh = 0; hh < 2 && s0 + hh * kCons + warp < b.ng; ++hh) {
+                            const unsigned char* cbh = cb + hh * kCons * kRecord;
+                            const uint4 c0[1] = {*reinterpret_cast<const uint4*>(cbh)};
+                            const uint4 c1[1] = {*reinterpret_cast<const uint4*>(cbh + 512)};
+                            const float2 f = unpack_sb(*reinterpret_cast<const uint32_t*>(sbp + hh * kCons * kRecord));
+                            float pr[1][NT];
+                            group_dot<NT, 1>(c0, c1, xg + hh * 64, xs_stride, pr);
 #pragma unroll
-                        for (int q = 0; q < NT; ++q) tot[0][q] += fmaf(f.x, pr[0][q], f.y * xsme[q * cw_max + c]);
+                            for (int q = 0; q < NT; ++q)
+                                tot[0][q] += fmaf(f.x, pr[0][q], f.y * xsme[q * cw_max + c + hh]);
+                        }
                     }
                 }
                 __syncwarp();
