@@ -73,6 +73,7 @@ SIGNATURES = [
     ("moe_route_noalloc", _i32, [_vp, _vp, _i32, _vp, _vp, _vp, _vp]),
     ("moe_cache_step", _i32, [_vp, _vp, _i32, _vp, _vp, _vp, _vp]),
     ("moe_forward", _i32, [_vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp]),
+    ("moe_cache_reset", _i32, [_vp]),
     ("moe_layer_stats", _i32, [_vp, _P(moe_stats)]),
     ("moe_layer_reset_stats", _i32, [_vp]),
     ("moe_cache_dump", _i32, [_vp, _vp, _vp]),
@@ -212,6 +213,11 @@ def moe_route_noalloc(layer: int, x, zbias, ids, gates, stream=None):
     x bf16 [T][d], ids int32 [T][k], gates f32 [T][k] (T <= 64)."""
     _check(load().moe_route_noalloc(layer, _dptr(x), x.shape[0], _dptr(zbias), _dptr(ids), _dptr(gates),
                                     _stream(stream)), "moe_route_noalloc")
+
+
+def moe_cache_reset(layer: int):
+    """Empty the layer's expert cache (slots free, counts zero)."""
+    _check(load().moe_cache_reset(layer), "moe_cache_reset")
 
 
 def moe_cache_step(layer: int, ids) -> dict:

@@ -93,7 +93,10 @@ typedef struct {
  * found no unpinned slot ([P3] "缓存管理的是专家工作集": the budget may be
  * exceeded temporarily) and are included in misses. exposed_copy_us is the
  * time the compute stream spent waiting for miss copies ([P3]
- * "读取完成后，算子才可以使用切片": overlap hides only part of the reads). */
+ * "读取完成后，算子才可以使用切片": overlap hides only part of the reads): for
+ * each call with misses, how long after the expert kernel started the last
+ * copy finished. It is measured only while kernel profiling is on
+ * (moe_ctx_set_profiling), since it needs two timed events per call. */
 typedef struct {
     uint64_t steps, hits, misses, bypass;
     uint64_t bytes_h2d;      /* bytes copied host -> device for misses */
@@ -212,6 +215,15 @@ moe_status moe_cache_step(moe_layer* layer, const int32_t* ids, int32_t n_ids, i
  * failed expert's slot is empty), MOE_ECUDA. */
 moe_status moe_forward(moe_layer* layer, const void* x_bf16, int32_t T, const float* zbias, float* y,
                        int32_t* ids_out, float* gates_out, void* stream);
+
+/* Empties the layer's expert cache: every slot becomes free and every count
+ * zero, as the per-layer slot cache of [P1] §6.2.2 is when created (and
+ * after moe_layer_set_weights). Slot contents are not touched; the next calls
+ * refill them. Orders
+ * itself after the layer's earlier calls on the host side only, so call it
+ * between calls, not while another thread uses the layer.
+ * Errors: MOE_EINVAL (layer NULL), MOE_ESTATE (no weights). */
+moe_status moe_cache_reset(moe_layer* layer);
 
 /* Counters (see moe_stats). Waits for the layer's outstanding timing events. */
 moe_status moe_layer_stats(moe_layer* layer, moe_stats* out);

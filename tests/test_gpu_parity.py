@@ -222,3 +222,20 @@ def test_injected_copy_failure_is_reported_and_recovers(ctx):
             r.forward(synth.tokens(s, 0, 20 + step, 4, False))
     finally:
         r.close()
+
+
+def test_cache_reset_empties_the_table(ctx):
+    s = synth.SHAPES_TINY
+    r = Rig(ctx, s, 0, 4)
+    try:
+        for step in range(3):
+            r.forward(synth.tokens(s, 0, 30 + step, 4, False))
+        moe.moe_cache_reset(r.h)
+        se, cnt = moe.moe_cache_dump(r.h, 4)
+        assert (se == -1).all() and (cnt == 0).all()
+        # from here the library must follow a fresh oracle cache
+        r.cache = oracle.Cache(s.n_experts, 4, moe.LFU)
+        for step in range(3):
+            r.forward(synth.tokens(s, 0, 40 + step, 4, False))
+    finally:
+        r.close()
