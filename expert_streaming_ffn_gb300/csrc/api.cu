@@ -85,6 +85,24 @@ void repack_qmatrix(const moe_qmatrix& m, int N, int K, uint8_t* dst) {
     }
 }
 
+void repack_down(const moe_qmatrix& m, int N, int K, uint8_t* dst) {
+    const int G = K / 64, RT = N / 32;
+    uint8_t* sb = dst + down_codes_bytes(N, K);
+    for (int n = 0; n < N; ++n) {
+        const int rt = n >> 5, lane = n & 31;
+        const uint8_t* src = m.codes + (size_t)n * (size_t)(K / 2);
+        for (int c = 0; c < K / 32; ++c) {
+            uint32_t* o = reinterpret_cast<uint32_t*>(dst + (((size_t)c * RT + rt) * 32 + lane) * 16);
+            for (int w = 0; w < 4; ++w) o[w] = device_nibble_order(src + (size_t)c * 16 + 4 * w);
+        }
+        for (int g = 0; g < G; ++g) {
+            const size_t i = (size_t)n * G + g;
+            reinterpret_cast<uint32_t*>(sb)[((size_t)g * RT + rt) * 32 + lane] =
+                (uint32_t)m.scale[i] | ((uint32_t)m.bias[i] << 16);
+        }
+    }
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -182,15 +200,10 @@ struct moe_layer {
     unsigned* d_rcount = nullptr;  // router block counters
     int32_t* d_ids = nullptr;
     float* d_gates = nullptr;
-    float* d_h = nullptr;
-    float* d_hs = nullptr;
-    float* d_o = nullptr;
-    float* d_os = nullptr;     // shared-expert outputs [cap_T][d]
+    float* d_o = nullptr;      // prefill: routed-expert outputs by pair [cap_T * k][d]
     unsigned long long* h_pub = nullptr;  // mapped pinned [cap_T * k]: seq << 32 | id
     unsigned long long* h_pub_dev = nullptr;
     std::vector<int32_t> h_ids;           // ids of the current call, read from h_pub
-    float* d_part = nullptr;
-    size_t part_floats = 0;
     // prefill (T > kDecodeMaxT): fp16 token rows (x of the shared expert
     // [cap_T][d], then x gathered per sorted pair [pairs][d]), fp16 h (shared
     // [cap_T][d_ff_shared], then routed [pairs][d_ff]), and the item/pair
@@ -200,8 +213,6 @@ struct moe_layer {
     uint8_t* d_pf = nullptr;
     uint8_t* h_pf = nullptr;
     size_t pf_bytes = 0;
-    unsigned* d_fcount = nullptr;
-    size_t n_fcount = 0;
     uint32_t err_generation = 0;  // the context's value when the counters were last known zero
     std::vector<int32_t> offsets, perm;
     moe_stats stats{};
@@ -234,12 +245,7 @@ void free_scratch(moe_layer* L) {
     cudaFree(L->d_rcount);
     cudaFree(L->d_ids);
     cudaFree(L->d_gates);
-    cudaFree(L->d_h);
-    cudaFree(L->d_hs);
     cudaFree(L->d_o);
-    cudaFree(L->d_os);
-    cudaFree(L->d_part);
-    cudaFree(L->d_fcount);
     cudaFree(L->d_x16);
     cudaFree(L->d_h16);
     cudaFree(L->d_pf);
@@ -252,10 +258,8 @@ void free_scratch(moe_layer* L) {
     L->d_rcount = nullptr;
     L->d_ids = nullptr;
     L->d_gates = nullptr;
-    L->d_h = L->d_hs = L->d_o = L->d_os = L->d_part = nullptr;
-    L->d_fcount = nullptr;
+    L->d_o = nullptr;
     L->h_pub = L->h_pub_dev = nullptr;
-    L->part_floats = L->n_fcount = 0;
     L->cap_T = 0;
 }
 
@@ -267,22 +271,12 @@ moe_status ensure_scratch(moe_layer* L, int T) {
     const moe_shapes& s = L->sh;
     const size_t pairs = (size_t)T * s.top_k;
     const int blocks = (T + 7) / 8;
-    const int routed_items = (int)std::min<size_t>(256, pairs);
-    const int shared_items = (T + kFfnMaxNT - 1) / kFfnMaxNT;
-    L->part_floats = ffn_max_partial_floats(s.d_model, shared_items, s.d_ff_shared, routed_items, s.d_ff);
-    L->n_fcount = ffn_max_counters(s.d_model, shared_items, s.d_ff_shared, routed_items, s.d_ff);
     bool ok = cudaMalloc(&L->d_logits, sizeof(float) * T * s.n_experts) == cudaSuccess &&
               cudaMalloc(&L->d_rcount, sizeof(unsigned) * blocks) == cudaSuccess &&
               cudaMemset(L->d_rcount, 0, sizeof(unsigned) * blocks) == cudaSuccess &&
               cudaMalloc(&L->d_ids, sizeof(int32_t) * pairs) == cudaSuccess &&
               cudaMalloc(&L->d_gates, sizeof(float) * pairs) == cudaSuccess &&
-              cudaMalloc(&L->d_h, sizeof(float) * pairs * s.d_ff) == cudaSuccess &&
-              cudaMalloc(&L->d_hs, sizeof(float) * (size_t)T * s.d_ff_shared) == cudaSuccess &&
               cudaMalloc(&L->d_o, sizeof(float) * pairs * s.d_model) == cudaSuccess &&
-              cudaMalloc(&L->d_os, sizeof(float) * (size_t)T * s.d_model) == cudaSuccess &&
-              cudaMalloc(&L->d_part, sizeof(float) * L->part_floats) == cudaSuccess &&
-              cudaMalloc(&L->d_fcount, sizeof(unsigned) * L->n_fcount) == cudaSuccess &&
-              cudaMemset(L->d_fcount, 0, sizeof(unsigned) * L->n_fcount) == cudaSuccess &&
               cudaHostAlloc(&L->h_pub, sizeof(unsigned long long) * pairs, cudaHostAllocMapped) == cudaSuccess &&
               cudaHostGetDevicePointer(&L->h_pub_dev, L->h_pub, 0) == cudaSuccess;
     if (ok && T > kDecodeMaxT) {
@@ -455,11 +449,11 @@ bool add_item(List& l, const Item& x) {
     return true;
 }
 
-// Fused FFN launches covering `items` (family 0 first); the combine runs in the last.
+// Fused FFN launches covering `items` (family 0 first), each adding its
+// experts' gate-weighted outputs into y.
 template <class List>
 moe_status launch_items(moe_layer* L, const std::vector<Item>& items, FfnArgs a, cudaStream_t s) {
     const moe_shapes& sh = L->sh;
-    const int combine = a.combine;
     size_t i = 0;
     while (i < items.size()) {
         List l{};
@@ -476,7 +470,6 @@ moe_status launch_items(moe_layer* L, const std::vector<Item>& items, FfnArgs a,
         if (j == i) return set_error(MOE_EINVAL, "an expert with too many pairs for one work list");
         a.fam[0].n_items = n_fam[0];
         a.fam[1].n_items = n_fam[1];
-        a.combine = (j == items.size()) ? combine : 0;
         {
             Prof p(L->ctx, s, K_FFN, bytes, flops);
             CUDA_TRY(launch_ffn(a, l, s));
@@ -495,10 +488,12 @@ moe_status launch_items_any(moe_layer* L, const std::vector<Item>& items, const 
     return launch_items<FfnLarge>(L, items, a, s);
 }
 
+// `zero_y`, when given, is the call's [T][d] fp32 output, zeroed by the same launch.
 moe_status route_into(moe_layer* L, const uint16_t* x, int T, const float* zbias, int32_t* ids, float* gates,
-                      bool publish, cudaStream_t s) {
+                      bool publish, cudaStream_t s, float* zero_y = nullptr) {
     RouterParams p{x, T, L->sh.d_model, L->sh.n_experts, L->sh.top_k, L->d_router_codes, L->d_router_sb, zbias,
-                   L->d_logits, L->d_rcount, ids, gates, publish ? L->h_pub_dev : nullptr, L->seq};
+                   L->d_logits, L->d_rcount, ids, gates, publish ? L->h_pub_dev : nullptr, L->seq,
+                   zero_y, zero_y ? T * L->sh.d_model : 0};
     Prof pr(L->ctx, s, K_ROUTER, (double)L->router_bytes + 2.0 * T * L->sh.d_model,
             2.0 * T * L->sh.n_experts * L->sh.d_model);
     CUDA_TRY(launch_router(p, s));
@@ -543,18 +538,10 @@ moe_status run_experts(moe_layer* L, const uint16_t* x, int T, float* y, const s
     a.x = x;
     a.d = sh.d_model;
     a.act = sh.act;
-    a.fam[0] = FfnFam{0, sh.d_ff_shared, 1, 1, 1, 1, L->d_hs, L->d_os};
-    a.fam[1] = FfnFam{0, sh.d_ff, sh.top_k, 1, 1, 1, L->d_h, L->d_o};
+    a.fam[0] = FfnFam{0, sh.d_ff_shared, 1};
+    a.fam[1] = FfnFam{0, sh.d_ff, sh.top_k};
     a.gates = L->d_gates;
-    a.combine_base = L->d_os;
-    a.y = y;
-    a.T = T;
-    a.k = sh.top_k;
-    a.combine = 1;
-    a.partials = L->d_part;
-    a.partial_floats = L->part_floats;
-    a.counters = L->d_fcount;
-    a.n_counters = L->n_fcount;
+    a.y = y;  // zeroed by the router launch of this call
     a.ready = L->d_ready;
     a.err = C->err_dev;
     a.trace = nullptr;
@@ -706,12 +693,12 @@ moe_status forward_chunk(moe_layer* L, const uint16_t* x, int T, const float* zb
     }
     if (L->err_generation != C->err_generation) {
         // an earlier kernel abandoned a wait: restore the all-zero counters
-        CUDA_TRY(cudaMemsetAsync(L->d_fcount, 0, sizeof(unsigned) * L->n_fcount, s));
         CUDA_TRY(cudaMemsetAsync(L->d_rcount, 0, sizeof(unsigned) * ((L->cap_T + 7) / 8), s));
         L->err_generation = C->err_generation;
     }
     ++L->seq;
-    moe_status st = route_into(L, x, T, zbias, L->d_ids, L->d_gates, true, s);
+    // a decode call's experts add into y, which the router launch zeroes
+    moe_status st = route_into(L, x, T, zbias, L->d_ids, L->d_gates, true, s, T <= kDecodeMaxT ? y : nullptr);
     if (st != MOE_OK) return st;
     L->stats.host_issue_us += us_since(t0);
     t0 = std::chrono::steady_clock::now();
@@ -896,7 +883,7 @@ extern "C" moe_status moe_layer_set_weights(moe_layer* L, const moe_host_weights
     std::vector<uint8_t> blob(L->shared_bytes);
     repack_qmatrix(w->shared_gate, Is, d, blob.data());
     repack_qmatrix(w->shared_up, Is, d, blob.data() + qmat_bytes(Is, d));
-    repack_qmatrix(w->shared_down, d, Is, blob.data() + 2 * qmat_bytes(Is, d));
+    repack_down(w->shared_down, d, Is, blob.data() + 2 * qmat_bytes(Is, d));
     CUDA_TRY(cudaMemcpy(L->d_shared, blob.data(), blob.size(), cudaMemcpyHostToDevice));
     // routed experts into the pinned pool, expert-major
     const size_t gc = (size_t)I * (d / 2), gs = (size_t)I * (d / 64), dc = (size_t)d * (I / 2), ds = (size_t)d * (I / 64);
@@ -907,7 +894,7 @@ extern "C" moe_status moe_layer_set_weights(moe_layer* L, const moe_host_weights
         moe_qmatrix dn{w->down.codes + e * dc, w->down.scale + e * ds, w->down.bias + e * ds};
         repack_qmatrix(g, I, d, dst);
         repack_qmatrix(u, I, d, dst + qmat_bytes(I, d));
-        repack_qmatrix(dn, d, I, dst + 2 * qmat_bytes(I, d));
+        repack_down(dn, d, I, dst + 2 * qmat_bytes(I, d));
     };
     unsigned nth = std::max(1u, std::min(16u, std::thread::hardware_concurrency()));
     std::vector<std::thread> pool;

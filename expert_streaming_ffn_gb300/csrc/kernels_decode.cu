@@ -118,6 +118,11 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(const RouterP
     const int runs = p.d >> 4;
     const int vec = p.d >> 3;
     const bool has_row = e < p.E;
+    if (p.zero) {
+        const int nb = gridDim.x * gridDim.y * blockDim.x;
+        for (int i = (blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x; i < p.zero_n; i += nb)
+            p.zero[i] = 0.0f;
+    }
     const uint8_t* row = p.codes + (size_t)(has_row ? e : 0) * p.d;
     const uint32_t* sbrow = p.sb + (size_t)(has_row ? e : 0) * (p.d >> 6);
     // Lane l owns runs c = l + 32 i (16 inputs each), walked in increasing c.

@@ -21,8 +21,9 @@
 //   warps 8-23  dequantisation in two groups of 8 warps that take alternate
 //               K-blocks: int4 -> fp16 w = fp16(s * q + b), written into the
 //               128B-swizzled K-major A tile;
-//   warp 24     bulk copies of the weight records (int4 codes with their
-//               scales) of 4 K-blocks per row tile at a time, into a raw ring;
+//   warp 24     bulk copies of the weight codes and scales of 4 K-blocks of
+//               the job's row tiles at a time, into a raw ring (gate/up in
+//               the tiled record format, down column-sliced);
 //   warp 25     TMA loads of the token rows (128B-swizzled fp16).
 // Copies are few and large (a bulk copy costs its issuing thread tens of
 // nanoseconds whatever its size), and the two producers issue in parallel.
@@ -241,62 +242,89 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kWarpLoad) {
         // ---------------- weight records ----------------
-        if (lane == 0) {
-            int r = 0;
-            uint32_t ph = 0;
-            int issued = 0;
-            bool ok = true;
-            for (int j = blockIdx.x; j < P.n_jobs && ok; j += gridDim.x) {
-                const Job b = decode_job(P, a, j);
-                const PfItem it = a.items[b.item];
-                if (it.ready >= 0 && !wait_flag(a.ready + it.ready, a.epoch, abortp)) {
-                    if (!*abortp) fail(32u);
+        // Lane 0 waits and arms the stage; the copies of a stage are issued by
+        // several lanes at once (a bulk copy costs its thread tens of ns).
+        int r = 0;
+        uint32_t ph = 0;
+        int issued = 0;
+        bool ok = true;
+        for (int j = blockIdx.x; j < P.n_jobs && ok; j += gridDim.x) {
+            const Job b = decode_job(P, a, j);
+            const PfItem it = a.items[b.item];
+            if (lane == 0 && it.ready >= 0 && !wait_flag(a.ready + it.ready, a.epoch, abortp)) {
+                if (!*abortp) fail(32u);
+                ok = false;
+            }
+            ok = __shfl_sync(kFull, ok, 0);
+            if (!ok) break;
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            const int I = a.inter[b.fam];
+            const size_t mat = qmat_bytes(I, a.d);
+            const int nkb = P.kblocks[b.fam];
+            for (int kb0 = 0; kb0 < nkb; kb0 += kUnit) {
+                const int nu = min(kUnit, nkb - kb0);
+                bool w = true;
+                if (lane == 0) {
+                    w = ptx::mbar_wait_sleep(raw_empty + r, ph ^ 1, abortp);
+                    if (!w) {
+                        record(1, j, kb0);
+                        if (!*abortp) fail(32u);
+                    } else {
+                        // diagnostics: when block 0 issues each unit of its first jobs (slot 1 of kb0's row)
+                        if (a.trace && blockIdx.x == 0 && issued < kPfTraceKb / kUnit)
+                            a.trace[0 * kPfTraceKb + issued * kUnit + 1] = ptx::globaltimer();
+                        ptx::mbar_arrive_expect_tx(raw_full + r, (uint32_t)(4 * nu * kRecord));
+                    }
+                }
+                w = __shfl_sync(kFull, w, 0);
+                if (!w) {
                     ok = false;
                     break;
                 }
-                asm volatile("fence.proxy.async.global;" ::: "memory");
-                const int I = a.inter[b.fam];
-                const size_t mat = qmat_bytes(I, a.d);
-                const int G = (phase == 1 ? a.d : I) / 64;  // records per row tile
-                const int nkb = P.kblocks[b.fam];
-                for (int kb0 = 0; kb0 < nkb; kb0 += kUnit) {
-                    const int nu = min(kUnit, nkb - kb0);
-                    if (!ptx::mbar_wait_sleep(raw_empty + r, ph ^ 1, abortp)) {
-                        record(1, j, kb0);
-                        if (!*abortp) fail(32u);
-                        ok = false;
-                        break;
+                unsigned char* raw = ringR + r * kRawBytes;
+                if (phase == 1) {
+                    // lane t < 4: row tile t of the job (gate 2i, gate 2i+1, up 2i, up 2i+1),
+                    // records kb0 .. kb0+nu-1, into raw + t * kUnit * kRecord
+                    if (lane < 4) {
+                        const int G = a.d / 64;
+                        const unsigned char* m = it.w + (size_t)(lane >> 1) * mat;
+                        const int rt = 2 * b.tile + (lane & 1);
+                        ptx::bulk_g2s(raw + lane * kUnit * kRecord, m + ((size_t)rt * G + kb0) * kRecord,
+                                      nu * kRecord, raw_full + r);
                     }
-                    unsigned char* raw = ringR + r * kRawBytes;
-                    // diagnostics: when block 0 issues each unit of its first two jobs (slot 1 of kb0's row)
-                    if (a.trace && blockIdx.x == 0 && issued < kPfTraceKb / kUnit)
-                        a.trace[0 * kPfTraceKb + issued * kUnit + 1] = ptx::globaltimer();
-                    ptx::mbar_arrive_expect_tx(raw_full + r, (uint32_t)(4 * nu * kRecord));
-                    for (int t = 0; t < 4; ++t) {
-                        // row tile t of the job: phase 1 gate 2i, gate 2i+1, up 2i, up 2i+1; phase 2 down 4i+t
-                        const unsigned char* m = it.w + (phase == 1 ? (size_t)(t >> 1) * mat : 2 * mat);
-                        const int rt = phase == 1 ? 2 * b.tile + (t & 1) : 4 * b.tile + t;
-                        ptx::bulk_g2s(raw + t * kUnit * kRecord, m + ((size_t)rt * G + kb0) * kRecord, nu * kRecord,
+                } else {
+                    // down, column-sliced: the job's 4 row tiles are contiguous within each
+                    // 32-input chunk (2 KB of codes) and each group's scale block (512 B).
+                    // Lane c < 2 nu copies chunk 2 kb0 + c to raw + c * 2048; lane 16 + u
+                    // (u < nu) the scale block of group kb0 + u to raw + kUnit * 4096 + u * 512.
+                    const int RT = a.d / 32;
+                    const unsigned char* dn = it.w + 2 * mat;
+                    if (lane < 2 * nu)
+                        ptx::bulk_g2s(raw + lane * 2048, dn + ((size_t)(2 * kb0 + lane) * RT + 4 * b.tile) * 512, 2048,
                                       raw_full + r);
-                    }
-                    ++issued;
-                    if (++r == kRawStages) {
-                        r = 0;
-                        ph ^= 1;
-                    }
+                    else if (lane >= 16 && lane - 16 < nu)
+                        ptx::bulk_g2s(raw + kUnit * 4096 + (lane - 16) * 512,
+                                      dn + down_codes_bytes(a.d, I) + ((size_t)(kb0 + lane - 16) * RT + 4 * b.tile) * 128,
+                                      512, raw_full + r);
+                }
+                __syncwarp();
+                ++issued;
+                if (++r == kRawStages) {
+                    r = 0;
+                    ph ^= 1;
                 }
             }
-            if (!ok) {
-                // let the copies already issued land before the CTA can exit
-                for (int i = 0; i < kRawStages && i < issued; ++i) {
-                    int sl = r - 1 - i;
-                    uint32_t par = ph;
-                    if (sl < 0) {
-                        sl += kRawStages;
-                        par ^= 1;
-                    }
-                    ptx::mbar_wait_bounded(raw_full + sl, par, nullptr);
+        }
+        if (!ok && lane == 0) {
+            // let the copies already issued land before the CTA can exit
+            for (int i = 0; i < kRawStages && i < issued; ++i) {
+                int sl = r - 1 - i;
+                uint32_t par = ph;
+                if (sl < 0) {
+                    sl += kRawStages;
+                    par ^= 1;
                 }
+                ptx::mbar_wait_bounded(raw_full + sl, par, nullptr);
             }
         }
     } else if (warp == kWarpB) {
@@ -508,8 +536,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tile_raw = rho >> 5;
             rlane = rho & 31;
         }
-        const int codes_off = tile_raw * kUnit * kRecord + hh * 512 + rlane * 16;
-        const int sb_off = tile_raw * kUnit * kRecord + 1024 + rlane * 4;
+        // where this thread's 16 codes and scale word of K-block u of a raw stage sit:
+        // phase 1 records [tile][u] of kRecord bytes; phase 2 codes [u][half][tile] of
+        // 512 bytes, then scale blocks [u][tile] of 128 bytes
+        const int codes_off = phase == 1 ? tile_raw * kUnit * kRecord + hh * 512 + rlane * 16
+                                         : hh * 2048 + tile_raw * 512 + rlane * 16;
+        const int codes_step = phase == 1 ? kRecord : 4096;
+        const int sb_off = phase == 1 ? tile_raw * kUnit * kRecord + 1024 + rlane * 4
+                                      : kUnit * 4096 + tile_raw * 128 + rlane * 4;
+        const int sb_step = phase == 1 ? kRecord : 512;
         const int swz = rho & 7;
         int r = 0, s = 0;
         uint32_t rph = 0, ph = 0;
@@ -532,8 +567,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int m = 0; m < 2; ++m) {
                     const int u = u0 + 2 * m;
                     if (have && u < nu) {
-                        cw[m] = *reinterpret_cast<const uint4*>(raw + codes_off + u * kRecord);
-                        sbw[m] = *reinterpret_cast<const uint32_t*>(raw + sb_off + u * kRecord);
+                        cw[m] = *reinterpret_cast<const uint4*>(raw + codes_off + u * codes_step);
+                        sbw[m] = *reinterpret_cast<const uint32_t*>(raw + sb_off + u * sb_step);
                     }
                 }
                 for (int u = 0; u < nu; ++u) {

@@ -73,13 +73,23 @@ void group_pairs(const int32_t* ids, int n_pairs, int n_experts, int32_t* offset
 //   sb:    (scale, bias) of group g as one 32-bit word (scale in the low half)
 //          at N*K/2 + ((rt * K/64 + g) * 32 + lane) * 4.
 // An expert blob is [gate (I x d)][up (I x d)][down (d x I)]; its size equals
-// the canonical byte count, 27 * I * d / 16.
+// the canonical byte count, 27 * I * d / 16. Gate and up use this tiled
+// format, down the column-sliced one below.
 
 MOE_HD inline size_t qmat_bytes(int N, int K) { return (size_t)N * (size_t)K / 2 + (size_t)N * (size_t)K / 16; }
 MOE_HD inline size_t expert_blob_bytes(int d, int inter) { return 2 * qmat_bytes(inter, d) + qmat_bytes(d, inter); }
 
 // Repack one canonical matrix into the tiled blob format at dst.
 void repack_qmatrix(const moe_qmatrix& m, int N, int K, uint8_t* dst);
+
+// The down matrix W[N][K] (N = d, K = intermediate) is column-sliced instead,
+// so that the 32 columns one decode work unit needs are contiguous:
+//   codes: 16-byte chunk c of row n at ((c * N/32 + rt) * 32 + lane) * 16,
+//          i.e. 512-byte half-records ordered by (chunk, row tile);
+//   sb:    the word of group g of row n at N*K/2 + ((g * N/32 + rt) * 32 + lane) * 4,
+//          i.e. 128-byte blocks ordered by (group, row tile).
+// Same size as the tiled format.
+void repack_down(const moe_qmatrix& m, int N, int K, uint8_t* dst);
 
 // ---- router -----------------------------------------------------------------
 
@@ -95,6 +105,8 @@ struct RouterParams {
     float* gates;          // [T][k] device
     unsigned long long* host_ids;  // [T][k] mapped pinned host memory (seq << 32 | id), or null
     uint32_t seq;
+    float* zero;  // optional: zero_n floats set to zero by the launch (the decode output, which
+    int zero_n;   // the expert FFN then adds into)
 };
 
 cudaError_t launch_router(const RouterParams& p, cudaStream_t s);
@@ -102,21 +114,27 @@ cudaError_t launch_router(const RouterParams& p, cudaStream_t s);
 // y[t][n] += sum_{r<k} gates[t][r] * o[t*k + r][n], added in rank order.
 cudaError_t launch_combine(const float* o, const float* gates, int T, int k, int d, float* y, cudaStream_t s);
 
-// ---- fused expert FFN ----------------------------------------------------------
+// ---- fused expert FFN (decode) --------------------------------------------------
 //
 // A list of expert "items", each with at most kFfnMaxNT (token, rank) pairs.
 // Items come in two families, family 0 first: the shared expert (its pairs
-// are token indices) and the routed experts (pair p = t * k + r). Pair p of
-// family f reads x row p / x_div and writes row p of the family's h and out.
-// An item whose bytes are still being copied names a ready flag (index into
-// `ready`) that must reach the list's epoch before its weights are read; -1
-// means resident.
+// are token indices, gate 1) and the routed experts (pair p = t * k + r, gate
+// gates[p]). Pair p of family f reads x row p / x_div and adds its
+// gate-weighted FFN output into y row p / x_div. An item whose bytes are still
+// being copied names a ready flag (index into `ready`) that must reach the
+// list's epoch before its weights are read; -1 means resident.
+//
+// Device layout of an expert blob (see repack_qmatrix / repack_down):
+// gate | up (records by 32-row tile, then group of 64 inputs) | down
+// (column-sliced: the codes of 32 output rows x 32 intermediate inputs as
+// 512-byte half-records ordered by (input slice, row tile), then the
+// scale/bias words as 128-byte blocks ordered by (group, row tile)).
 
 constexpr int kFfnMaxNT = 8;
 constexpr int kFfnFams = 2;
 
 struct FfnItem {
-    const uint8_t* w;  // expert blob: gate | up | down in the tiled layout
+    const uint8_t* w;  // expert blob
     int16_t pb, np;    // pair range within pair[]
     int16_t ready;     // ready-flag index, -1 if resident
     int16_t pad;
@@ -133,48 +151,37 @@ using FfnSmall = FfnList<24, 96>;
 using FfnLarge = FfnList<256, 1024>;
 
 struct FfnFam {
-    int n_items;   // consecutive items of the list; family 0 first
-    int inter;     // intermediate size
-    int x_div;     // x row of pair p is p / x_div
-    int kc1, kc2;  // K-chunks per gate/up and per down tile (set by the launcher)
-    int tpj;       // down tiles per job (set by the launcher)
-    float* h;      // scratch [pairs][inter]
-    float* out;    // down outputs [pairs][d]
+    int n_items;  // consecutive items of the list; family 0 first
+    int inter;    // intermediate size
+    int x_div;    // x (and y) row of pair p is p / x_div
 };
 
 struct FfnArgs {
     const uint16_t* x;  // [T][d] bf16
     int d, act;
     FfnFam fam[kFfnFams];
-    // combine (when `combine`): once every item of the launch has finished an
-    // output tile, y[t] = base[t] + sum_r gates[t][r] * fam[1].out[t*k + r],
-    // ranks in order, where base = combine_base (e.g. the shared expert's
-    // outputs) or, when that is null, y itself
-    const float* gates;  // [T][k]
-    const float* combine_base;
-    float* y;  // [T][d]
-    int T, k, combine;
-    float* partials;
-    size_t partial_floats;
-    unsigned* counters;  // zero between launches; each launch leaves them zero
-    size_t n_counters;
+    const float* gates;  // [T * k], pair p's gate (family 1)
+    float* y;            // [T][d] fp32, zero on entry: every unit adds its share
     const uint32_t* ready;
     unsigned* err;
-    int xs_stride;  // set by the launcher: inputs per row of the staged-input buffer
+    int xs_stride;  // set by the launcher: staged inputs per warp and row
+    int kchunk;     // set by the launcher: gate/up groups staged at a time
     // optional diagnostics: per CTA, %globaltimer at kFfnTracePoints moments
-    // (start, first weights landed, last gate/up done, down inputs ready,
-    // last down done, end); null = off
+    // (start, first weights landed, first unit's h ready, first unit done,
+    // end); null = off
     unsigned long long* trace;
 };
-constexpr int kFfnTracePoints = 6;
+constexpr int kFfnTracePoints = 5;
 
-// Scratch a launch over these families may need (the launcher never exceeds it).
-size_t ffn_max_partial_floats(int d, int n_shared, int inter_shared, int n_routed, int inter_routed);
-size_t ffn_max_counters(int d, int n_shared, int inter_shared, int n_routed, int inter_routed);
-
-// One cooperative launch computing the FFN of every item (and the combine).
+// One launch computing, for every item, unit by unit (32 intermediate rows at
+// a time), h = act(W_g x) * (W_u x) and the matching slice of W_d h, added
+// gate-weighted into y.
 template <class L>
 cudaError_t launch_ffn(const FfnArgs& a, const L& list, cudaStream_t s);
+
+// Bytes of the down matrix of one expert in the column-sliced layout (equal to
+// qmat_bytes(d, inter)).
+MOE_HD inline size_t down_codes_bytes(int d, int inter) { return (size_t)d * (size_t)inter / 2; }
 
 // ---- prefill grouped GEMM (tcgen05) -------------------------------------------
 //

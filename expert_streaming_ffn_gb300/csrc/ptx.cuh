@@ -10,7 +10,11 @@ namespace moe {
 namespace ptx {
 
 // A wait that has not completed after this many nanoseconds is abandoned.
-constexpr uint64_t kWaitLimitNs = 200ull * 1000ull * 1000ull;
+// Waits on weights still being copied from host memory sit behind every copy
+// queued before them (a prefill chunk can queue most of a layer's experts, near
+// a gigabyte), and the host link has been seen running far below its rate for
+// a while after large pinned allocations, so the bound is generous.
+constexpr uint64_t kWaitLimitNs = 2000ull * 1000ull * 1000ull;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
