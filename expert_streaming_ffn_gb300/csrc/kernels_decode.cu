@@ -5,7 +5,7 @@
 //
 // router_kernel   8-bit router GEMV, one warp per expert row, fp32 in a fixed
 //                 order, followed, in the last block to finish a token block,
-//                 by a warp-shuffle top-k (ties to the lower expert index) and
+//                 by a warp-reduction top-k (ties to the lower expert index) and
 //                 the softmax over the k chosen logits ([P3]
 //                 "每个 token、每层都要重新路由"; [P1] §2.4 cb1). Each id is
 //                 also written to mapped host memory as one 64-bit word
@@ -49,50 +49,59 @@ __device__ __forceinline__ float bf16_at(const uint4& r, int i) {
     return (i & 1) ? bf16_hi(w) : bf16_lo(w);
 }
 
-// Top-k of one token's logits by one warp: k rounds of a warp-wide argmax
-// ordered by (logit descending, expert index ascending); lane r ends up with
-// rank r. Then gates = softmax over the k chosen logits.
+// Monotonic map of floats to unsigned keys (a < b iff key(a) < key(b)), with
+// -0 taken as +0 so that the two compare equal as floats do.
+__device__ __forceinline__ uint32_t order_key(float v) {
+    const uint32_t u = __float_as_uint(v + 0.0f);
+    return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k ^ 0x80000000u) : ~k);
+}
+
+// Top-k of one token's logits by one warp. Lane l holds the candidates of
+// experts l + 32 j as 64-bit words (key << 32 | ~e), so that a larger word is
+// a larger logit or, for equal logits, a lower expert index; it sorts them
+// once, descending. Each of the k rounds then takes the warp-wide maximum of
+// the lanes' heads (one max-reduction of the keys, one of the index part
+// among the lanes that hold that key), and the lane that owned it moves to
+// its next candidate; lane r ends up with rank r. Then gates = softmax over
+// the k chosen logits.
 template <int MAXV>
 __device__ void topk_warp(const float* logits, int E, int k, int lane, int32_t* ids, float* gates,
                           unsigned long long* host_ids, uint32_t seq) {
-    float v[MAXV];
-    uint32_t taken = 0;
+    unsigned long long c[MAXV];
 #pragma unroll
     for (int j = 0; j < MAXV; ++j) {
         const int e = lane + 32 * j;
-        if (e < E) {
-            v[j] = __ldcg(logits + e);
-        } else {
-            v[j] = -INFINITY;
-            taken |= 1u << j;
-        }
+        // beyond E: 0, below every real candidate (whose index part is nonzero)
+        c[j] = e < E ? ((unsigned long long)order_key(__ldcg(logits + e)) << 32) | (uint32_t)~e : 0ull;
     }
+    // odd-even transposition sort, descending (MAXV passes)
+#pragma unroll
+    for (int pass = 0; pass < MAXV; ++pass)
+#pragma unroll
+        for (int j = pass & 1; j + 1 < MAXV; j += 2)
+            if (c[j] < c[j + 1]) {
+                const unsigned long long t = c[j];
+                c[j] = c[j + 1];
+                c[j + 1] = t;
+            }
     float mine_v = -INFINITY;
     int mine_i = 0;
     for (int r = 0; r < k; ++r) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
+        const uint32_t hk = (uint32_t)(c[0] >> 32), hi = (uint32_t)c[0];
+        const uint32_t top = __reduce_max_sync(kFull, hk);
+        const uint32_t win = __reduce_max_sync(kFull, hk == top ? hi : 0u);  // ~e: the lowest index
+        if (hk == top && hi == win) {
+            // this lane's head was taken: move up its remaining candidates
 #pragma unroll
-        for (int j = 0; j < MAXV; ++j) {
-            const int e = lane + 32 * j;
-            if (!((taken >> j) & 1u) && (v[j] > bv || (v[j] == bv && e < bi))) {
-                bv = v[j];
-                bi = e;
-            }
+            for (int j = 0; j + 1 < MAXV; ++j) c[j] = c[j + 1];
+            c[MAXV - 1] = 0ull;
         }
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) {
-            const float ov = __shfl_xor_sync(kFull, bv, off);
-            const int oi = __shfl_xor_sync(kFull, bi, off);
-            if (ov > bv || (ov == bv && oi < bi)) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-        if (bi >= 0 && bi < E && (bi & 31) == lane) taken |= 1u << (bi >> 5);
         if (lane == r) {
-            mine_v = bv;
-            mine_i = bi;
+            mine_v = key_value(top);
+            mine_i = (int)~win;
         }
     }
     const float top = __shfl_sync(kFull, mine_v, 0);
@@ -109,12 +118,25 @@ __device__ void topk_warp(const float* logits, int E, int k, int lane, int32_t* 
     }
 }
 
+// Code byte m of a word as the float q (exact): 2^23 + q from a byte permute
+// into the magic word 0x4B000000, minus 2^23.
+__device__ __forceinline__ float byte_code(uint32_t w, int m) {
+    return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | (uint32_t)m)) - 8388608.0f;
+}
+
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+template <int TB>
 __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(const RouterParams p) {
     extern __shared__ uint4 xsm[];  // the block's token rows, [nt][d / 8] of 8 bf16 each
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x * kRouterWarps + warp;
-    const int t0 = blockIdx.y * kRouterTB;
-    const int nt = min(kRouterTB, p.T - t0);
+    const int t0 = blockIdx.y * TB;
+    const int nt = min(TB, p.T - t0);
     const int runs = p.d >> 4;
     const int vec = p.d >> 3;
     const bool has_row = e < p.E;
@@ -141,13 +163,25 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(const RouterP
         }
     };
     load_batch(0);
-    const uint4* xg = reinterpret_cast<const uint4*>(p.x + (size_t)t0 * p.d);
-    for (int i = threadIdx.x; i < nt * vec; i += blockDim.x) xsm[i] = __ldg(xg + i);
+    {
+        // the token rows, eight loads per thread in flight at a time
+        const uint4* xg = reinterpret_cast<const uint4*>(p.x + (size_t)t0 * p.d);
+        const int n = nt * vec;
+        for (int i0 = threadIdx.x; i0 < n; i0 += 8 * blockDim.x) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (i0 + u * (int)blockDim.x < n) v[u] = __ldg(xg + i0 + u * blockDim.x);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (i0 + u * (int)blockDim.x < n) xsm[i0 + u * blockDim.x] = v[u];
+        }
+    }
     __syncthreads();
     if (has_row) {
-        float acc[kRouterTB];
+        float acc[TB];
 #pragma unroll
-        for (int j = 0; j < kRouterTB; ++j) acc[j] = 0.0f;
+        for (int j = 0; j < TB; ++j) acc[j] = 0.0f;
         for (int b0 = 0; 32 * b0 < runs; b0 += kRouterBatch) {
             if (b0 > 0) load_batch(b0);
 #pragma unroll
@@ -158,9 +192,9 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(const RouterP
                 const uint32_t qw[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
                 float w[16];
 #pragma unroll
-                for (int m = 0; m < 16; ++m) w[m] = __fmaf_rn(f.x, (float)((qw[m >> 2] >> (8 * (m & 3))) & 0xFFu), f.y);
+                for (int m = 0; m < 16; ++m) w[m] = __fmaf_rn(f.x, byte_code(qw[m >> 2], m & 3), f.y);
 #pragma unroll
-                for (int j = 0; j < kRouterTB; ++j) {
+                for (int j = 0; j < TB; ++j) {
                     if (j < nt) {
                         const uint4 xa = xsm[j * vec + 2 * c], xb = xsm[j * vec + 2 * c + 1];
 #pragma unroll
@@ -172,7 +206,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(const RouterP
             }
         }
 #pragma unroll
-        for (int j = 0; j < kRouterTB; ++j) {
+        for (int j = 0; j < TB; ++j) {
             if (j < nt) {
                 float v = acc[j];
 #pragma unroll
@@ -181,17 +215,17 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(const RouterP
             }
         }
     }
-    // The last block of this token block to finish runs the top-k.
+    // The last block of this token block to finish runs the top-k. Each
+    // block's arrival is a release of its logits, and the count the last one
+    // reads an acquire of all of them.
     __shared__ int is_last;
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
-        const unsigned prev = atomicAdd(p.counters + blockIdx.y, 1u);
+        const unsigned prev = atom_add_acq_rel(p.counters + blockIdx.y, 1u);
         is_last = prev == gridDim.x - 1;
     }
     __syncthreads();
     if (!is_last) return;
-    __threadfence();
     for (int j = warp; j < nt; j += kRouterWarps) {
         const int t = t0 + j;
         unsigned long long* hid = p.host_ids ? p.host_ids + (size_t)t * p.k : nullptr;
@@ -221,14 +255,20 @@ __global__ void combine_kernel(const float* __restrict__ o, const float* __restr
 cudaError_t launch_router(const RouterParams& p, cudaStream_t s) {
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(router_kernel<kRouterTB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kRouterTB * kMaxDModel * 2);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(router_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDModel * 2);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    dim3 grid((p.E + kRouterWarps - 1) / kRouterWarps, (p.T + kRouterTB - 1) / kRouterTB);
     const size_t sm = (size_t)std::min(kRouterTB, p.T) * p.d * 2;
-    router_kernel<<<grid, kRouterWarps * 32, sm, s>>>(p);
+    if (p.T == 1) {
+        router_kernel<1><<<dim3((p.E + kRouterWarps - 1) / kRouterWarps, 1), kRouterWarps * 32, sm, s>>>(p);
+    } else {
+        dim3 grid((p.E + kRouterWarps - 1) / kRouterWarps, (p.T + kRouterTB - 1) / kRouterTB);
+        router_kernel<kRouterTB><<<grid, kRouterWarps * 32, sm, s>>>(p);
+    }
     return cudaGetLastError();
 }
 
