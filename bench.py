@@ -339,7 +339,12 @@ def run_ours(args, world, rank, local):
     moe.moe_ctx_set_profiling(ctx, False)
     exposed = sum(moe.moe_layer_stats(h)["exposed_copy_us"] for h in layers)
     peaks, peak_src = measured_peaks()
-    dom = max(kt.items(), key=lambda kv: kv[1][1])
+    # The roofline kernel: the one with the most device time among those whose
+    # duration is HBM work. The decode launch over the experts copied in by
+    # the call (expert_ffn_miss) waits for the host-to-device copies, so its
+    # time is the host link's, reported beside the roofline instead.
+    hbm_kinds = {k: v for k, v in kt.items() if k != "expert_ffn_miss" and v[0] > 0}
+    dom = max(hbm_kinds.items(), key=lambda kv: kv[1][1])
     name, (n_l, tot_ms, by, fl) = dom
     achieved = by / (tot_ms * 1e-3) / 1e9 if tot_ms > 0 else 0.0
     all_ms = sum(v[1] for v in kt.values())
@@ -423,6 +428,9 @@ def run_ours(args, world, rank, local):
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                      else "fallback 6.8 TB/s"},
         "kernels": kernels,
+        "miss_launches": ({"kernel": "expert_ffn_miss", "bound": "host link (copies of missed experts)",
+                           "launches": kt["expert_ffn_miss"][0], "ms": round(kt["expert_ffn_miss"][1], 4)}
+                          if kt.get("expert_ffn_miss", (0, 0))[1] > 0 else None),
         "prefill": prefill,
         "cpu_baseline": cpu,
         "e2e": e2e,

@@ -23,7 +23,7 @@ _lib = None
 MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA, MOE_ECOPY, MOE_ETIMEOUT, MOE_ESTATE = range(7)
 LFU, LRU = 0, 1
 GELU_TANH, SILU = 0, 1
-KERNEL_KINDS = ("router", "expert_ffn", "combine", "gemm_gateup", "gemm_down", "pf_gather")
+KERNEL_KINDS = ("router", "expert_ffn", "combine", "gemm_gateup", "gemm_down", "pf_gather", "expert_ffn_miss")
 
 
 class MoeError(RuntimeError):

@@ -24,11 +24,14 @@
 #include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
+#include <time.h>
 
 #include <algorithm>
+#include <atomic>
 #include <chrono>
 #include <mutex>
 #include <new>
+#include <string>
 #include <thread>
 #include <vector>
 
@@ -118,7 +121,7 @@ using namespace moe;
 namespace {
 
 constexpr int kKinds = 8;
-enum Kind { K_ROUTER = 0, K_FFN = 1, K_COMBINE = 2, K_GEMM_GU = 3, K_GEMM_DN = 4, K_GATHER = 5 };
+enum Kind { K_ROUTER = 0, K_FFN = 1, K_COMBINE = 2, K_GEMM_GU = 3, K_GEMM_DN = 4, K_GATHER = 5, K_FFN_MISS = 6 };
 constexpr double kHostWaitLimitS = 10.0;  // longest the host waits for the routing of one call
 // Rounds of ready-word source values kept in pinned memory. A round's entry is
 // rewritten kEpochRing calls later, long after its copies ran: every call
@@ -135,6 +138,38 @@ struct ProfRec {
 struct WaitRec {
     cudaEvent_t ffn_start, copies_done;
 };
+
+// Timeline diagnostics, on when the environment variable MOE_TRACE_FILE
+// names an output file at context creation: every launch gets a device span
+// {earliest block start, latest block end} in %globaltimer nanoseconds, and
+// the host records its own steps in CLOCK_REALTIME nanoseconds; the file is
+// written when the context is destroyed.
+constexpr int kTraceSpans = 1 << 18;
+
+struct TraceLaunch {
+    int kind, layer;
+    uint32_t seq;
+    int slot;
+    uint64_t t_host;
+};
+struct TraceHost {
+    const char* what;
+    int layer;
+    uint32_t seq;
+    uint64_t t;
+};
+
+uint64_t realtime_ns() {
+    timespec ts;
+    clock_gettime(CLOCK_REALTIME, &ts);
+    return (uint64_t)ts.tv_sec * 1000000000ull + (uint64_t)ts.tv_nsec;
+}
+
+__global__ void read_globaltimer(unsigned long long* out) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    *out = t;
+}
 
 }  // namespace
 
@@ -157,6 +192,28 @@ struct moe_ctx {
     uint32_t err_generation = 0;  // bumped whenever a kernel reported an expired wait
     long fail_copy_at = -1;  // test hook: the n-th miss copy from now reports failure
     long copies_issued = 0;
+    // timeline diagnostics (see TraceLaunch)
+    std::string trace_path;
+    unsigned long long* trace_spans = nullptr;  // device [kTraceSpans][2]
+    std::vector<TraceLaunch> trace_launches;
+    std::vector<TraceHost> trace_host;
+    struct TraceCopy {
+        cudaEvent_t a, b;
+        size_t bytes;
+        uint64_t t_host;
+    };
+    std::vector<TraceCopy> trace_copies;
+    cudaEvent_t trace_base = nullptr;
+
+    unsigned long long* trace_span(int kind, int layer, uint32_t seq) {
+        if (!trace_spans || (int)trace_launches.size() >= kTraceSpans) return nullptr;
+        const int slot = (int)trace_launches.size();
+        trace_launches.push_back(TraceLaunch{kind, layer, seq, slot, realtime_ns()});
+        return trace_spans + 2 * slot;
+    }
+    void trace_mark(const char* what, int layer, uint32_t seq) {
+        if (trace_spans) trace_host.push_back(TraceHost{what, layer, seq, realtime_ns()});
+    }
 
     cudaEvent_t timing_event() {
         if (!timing_pool.empty()) {
@@ -172,6 +229,7 @@ struct moe_ctx {
 
 struct moe_layer {
     moe_ctx* ctx = nullptr;
+    int id = 0;  // creation order within the process (diagnostics)
     moe_shapes sh{};
     int S = 0, policy = 0;
     size_t ebytes = 0, shared_bytes = 0, router_bytes = 0;
@@ -374,53 +432,105 @@ moe_status check_err_word(moe_ctx* C) {
     return MOE_OK;
 }
 
+// The ready flags of one miss: its gate/up bytes and its down bytes land
+// separately, so that its gate/up work can run while its down bytes are still
+// being copied.
+struct MissFlags {
+    int gu = -1, dn = -1;
+};
+
+// Misses per ready-flag group: a group's flag is written after the group's
+// copies, so a small call (decode) waits on one flag per part and a large one
+// (a prefill chunk) can start on its first experts while the rest still copy.
+constexpr int kFlagGroup = 8;
+
 // Issue the copies of one cache step's misses. A slot miss lands in its slot,
-// a bypass in the next staging entry; after each copy the copy stream writes
-// `epoch` into the matching ready flag (slot s -> flag s, staging entry b ->
-// flag S + b). On failure every slot this step filled but whose copy is not
-// known good is emptied, so the table never claims bytes that are missing.
+// a bypass in the next staging entry. With flags wanted (ready_of_miss), each
+// expert is copied in two parts, every miss's gate and up matrices first and
+// then every miss's down matrix, and after each group of kFlagGroup misses'
+// part the copy stream writes `epoch` into that group's flag for the part
+// (group g: flags 2g for gate/up, 2g + 1 for down). On failure every slot
+// this step filled but whose copy is not known good is emptied, so the table
+// never claims bytes that are missing.
 moe_status issue_miss_copies(moe_layer* L, const StepResult& r, bool with_bypass, uint32_t epoch,
-                             std::vector<int>* ready_of_miss) {
+                             std::vector<MissFlags>* ready_of_miss) {
     moe_ctx* C = L->ctx;
-    int nb = 0;
     L->h_epochs[epoch % kEpochRing] = epoch;
     if (with_bypass && r.bypass > 0) {
         moe_status st = ensure_staging(C, (size_t)r.bypass * L->ebytes);
         if (st != MOE_OK) return st;
         CUDA_TRY(cudaStreamWaitEvent(C->copy_stream, C->staging_free, 0));
     }
-    if (ready_of_miss) ready_of_miss->assign(r.miss_experts.size(), -1);
+    if (ready_of_miss) ready_of_miss->assign(r.miss_experts.size(), MissFlags{});
+    // the copies to make, in miss order
+    struct Copy {
+        size_t i;
+        uint8_t* dst;
+        const uint8_t* src;
+    };
+    std::vector<Copy> copies;
+    int nb = 0;
     for (size_t i = 0; i < r.miss_experts.size(); ++i) {
-        const int e = r.miss_experts[i], slot = r.miss_slots[i];
+        const int slot = r.miss_slots[i];
         if (slot < 0 && !with_bypass) continue;
-        uint8_t* dst = slot >= 0 ? L->d_slots + (size_t)slot * L->ebytes : C->staging + (size_t)nb * L->ebytes;
-        const int flag = slot >= 0 ? slot : L->S + nb;
-        bool fail = false;
-        if (C->fail_copy_at >= 0 && C->copies_issued == C->fail_copy_at) {
-            fail = true;
-            C->fail_copy_at = -1;
-        }
-        ++C->copies_issued;
-        cudaError_t ce = fail ? cudaErrorUnknown
-                              : cudaMemcpyAsync(dst, L->h_pool + (size_t)e * L->ebytes, L->ebytes,
-                                                cudaMemcpyHostToDevice, C->copy_stream);
-        // The ready word is set by a 4-byte copy queued behind the data on the
-        // same stream: on this stream it costs ~1.5 us, a stream write of the
-        // value ~3.3 us (measured).
-        if (ce == cudaSuccess)
-            ce = cudaMemcpyAsync(L->d_ready + flag, L->h_epochs + epoch % kEpochRing, sizeof(uint32_t),
-                                 cudaMemcpyHostToDevice, C->copy_stream);
-        if (ce != cudaSuccess) {
-            if (!fail) cudaGetLastError();
-            for (size_t j = i; j < r.miss_experts.size(); ++j)
-                if (r.miss_slots[j] >= 0) L->cache.evict(r.miss_slots[j]);
-            return set_error(MOE_ECOPY, "copy of expert %d (slot %d) failed: %s", e, slot,
-                             fail ? "injected failure" : cudaGetErrorString(ce));
-        }
-        L->stats.bytes_h2d += L->ebytes;
-        if (ready_of_miss) (*ready_of_miss)[i] = flag;
-        if (slot < 0) ++nb;
+        uint8_t* dst = slot >= 0 ? L->d_slots + (size_t)slot * L->ebytes : C->staging + (size_t)(nb++) * L->ebytes;
+        copies.push_back(Copy{i, dst, L->h_pool + (size_t)r.miss_experts[i] * L->ebytes});
     }
+    const bool flags = ready_of_miss != nullptr;
+    const size_t gu_bytes = 2 * qmat_bytes(L->sh.d_ff, L->sh.d_model);
+    // a flag is set by a 4-byte copy queued behind the data on the same
+    // stream: on this stream it costs ~1.5 us, a stream write of the value
+    // ~3.3 us (measured)
+    auto set_flag = [&](int flag) {
+        return cudaMemcpyAsync(L->d_ready + flag, L->h_epochs + epoch % kEpochRing, sizeof(uint32_t),
+                               cudaMemcpyHostToDevice, C->copy_stream);
+    };
+    auto fail_from = [&](size_t k, cudaError_t ce, bool injected) {
+        if (!injected) cudaGetLastError();
+        for (size_t j = copies[k].i; j < r.miss_experts.size(); ++j)
+            if (r.miss_slots[j] >= 0) L->cache.evict(r.miss_slots[j]);
+        return set_error(MOE_ECOPY, "copy of expert %d (slot %d) failed: %s", r.miss_experts[copies[k].i],
+                         r.miss_slots[copies[k].i], injected ? "injected failure" : cudaGetErrorString(ce));
+    };
+    const int parts = flags ? 2 : 1;
+    for (int part = 0; part < parts; ++part) {
+        const size_t off = part == 0 ? 0 : gu_bytes;
+        const size_t len = !flags ? L->ebytes : part == 0 ? gu_bytes : L->ebytes - gu_bytes;
+        for (size_t k = 0; k < copies.size(); ++k) {
+            bool injected = false;
+            if (part == 0) {
+                if (C->fail_copy_at >= 0 && C->copies_issued == C->fail_copy_at) {
+                    injected = true;
+                    C->fail_copy_at = -1;
+                }
+                ++C->copies_issued;
+            }
+            moe_ctx::TraceCopy tc{};
+            if (C->trace_spans && C->trace_copies.size() < (size_t)kTraceSpans) {
+                cudaEventCreate(&tc.a);
+                cudaEventCreate(&tc.b);
+                cudaEventRecord(tc.a, C->copy_stream);
+            }
+            const cudaError_t ce = injected ? cudaErrorUnknown
+                                            : cudaMemcpyAsync(copies[k].dst + off, copies[k].src + off, len,
+                                                              cudaMemcpyHostToDevice, C->copy_stream);
+            if (tc.a) {
+                cudaEventRecord(tc.b, C->copy_stream);
+                tc.bytes = len;
+                tc.t_host = realtime_ns();
+                C->trace_copies.push_back(tc);
+            }
+            if (ce != cudaSuccess) return fail_from(k, ce, injected);
+            if (!flags) continue;
+            const int g = (int)(k / kFlagGroup);
+            (*ready_of_miss)[copies[k].i] = MissFlags{2 * g, 2 * g + 1};
+            if (k + 1 == copies.size() || (k + 1) % kFlagGroup == 0) {
+                const cudaError_t fe = set_flag(2 * g + part);
+                if (fe != cudaSuccess) return fail_from(k, fe, false);
+            }
+        }
+    }
+    L->stats.bytes_h2d += (uint64_t)copies.size() * L->ebytes;
     return MOE_OK;
 }
 
@@ -428,7 +538,7 @@ struct Item {
     const uint8_t* w;
     int b, e;              // pair range in perm, or pair ids themselves when perm is null
     const int32_t* perm;
-    int ready;             // ready-flag index, -1 if resident
+    int ready, ready_dn;   // ready-flag indices of the gate/up and down bytes, -1 if resident
     int fam;               // 0 shared expert, 1 routed expert
 };
 
@@ -444,15 +554,15 @@ bool add_item(List& l, const Item& x) {
     it.pb = (int16_t)pb;
     it.np = (int16_t)(x.e - x.b);
     it.ready = (int16_t)x.ready;
-    it.pad = 0;
+    it.ready_dn = (int16_t)x.ready_dn;
     for (int i = x.b; i < x.e; ++i) l.pair[pb++] = x.perm ? (int16_t)x.perm[i] : (int16_t)i;
     return true;
 }
 
 // Fused FFN launches covering `items` (family 0 first), each adding its
-// experts' gate-weighted outputs into y.
+// experts' gate-weighted outputs into y; timed as `kind` when profiling.
 template <class List>
-moe_status launch_items(moe_layer* L, const std::vector<Item>& items, FfnArgs a, cudaStream_t s) {
+moe_status launch_items(moe_layer* L, const std::vector<Item>& items, FfnArgs a, int kind, cudaStream_t s) {
     const moe_shapes& sh = L->sh;
     size_t i = 0;
     while (i < items.size()) {
@@ -470,9 +580,10 @@ moe_status launch_items(moe_layer* L, const std::vector<Item>& items, FfnArgs a,
         if (j == i) return set_error(MOE_EINVAL, "an expert with too many pairs for one work list");
         a.fam[0].n_items = n_fam[0];
         a.fam[1].n_items = n_fam[1];
+        a.span = L->ctx->trace_span(kind, L->id, L->seq);
         {
-            Prof p(L->ctx, s, K_FFN, bytes, flops);
-            CUDA_TRY(launch_ffn(a, l, s));
+            Prof p(L->ctx, s, kind, bytes, flops);
+            CUDA_TRY(launch_ffn(a, l, s, true));
         }
         L->stats.bytes_resident += (uint64_t)bytes;
         i = j;
@@ -480,12 +591,40 @@ moe_status launch_items(moe_layer* L, const std::vector<Item>& items, FfnArgs a,
     return MOE_OK;
 }
 
-moe_status launch_items_any(moe_layer* L, const std::vector<Item>& items, const FfnArgs& a, cudaStream_t s) {
+moe_status launch_items_any(moe_layer* L, const std::vector<Item>& items, const FfnArgs& a, int kind,
+                            cudaStream_t s) {
     if (items.empty()) return MOE_OK;
     int pairs = 0;
     for (const Item& it : items) pairs += it.e - it.b;
-    if ((int)items.size() <= 24 && pairs <= 96) return launch_items<FfnSmall>(L, items, a, s);
-    return launch_items<FfnLarge>(L, items, a, s);
+    if ((int)items.size() <= 24 && pairs <= 96) return launch_items<FfnSmall>(L, items, a, kind, s);
+    return launch_items<FfnLarge>(L, items, a, kind, s);
+}
+
+FfnArgs decode_args(moe_layer* L, const uint16_t* x, float* y) {
+    const moe_shapes& sh = L->sh;
+    FfnArgs a{};
+    a.x = x;
+    a.d = sh.d_model;
+    a.act = sh.act;
+    a.fam[0] = FfnFam{0, sh.d_ff_shared, 1};
+    a.fam[1] = FfnFam{0, sh.d_ff, sh.top_k};
+    a.gates = L->d_gates;
+    a.y = y;  // zeroed by the router launch of this call
+    a.ready = L->d_ready;
+    a.err = L->ctx->err_dev;
+    a.trace = nullptr;
+    return a;
+}
+
+// The shared expert of a decode call on every token. It needs no routing, so
+// it is queued right behind the router and runs while the host reads the
+// routing, steps the cache and issues the miss copies ([P1] §8.2: the copies
+// overlap the shared expert's compute).
+moe_status run_shared(moe_layer* L, const uint16_t* x, int T, float* y, cudaStream_t s) {
+    std::vector<Item> items;
+    for (int t0 = 0; t0 < T; t0 += kFfnMaxNT)
+        items.push_back(Item{L->d_shared, t0, std::min(T, t0 + kFfnMaxNT), nullptr, -1, -1, 0});
+    return launch_items_any(L, items, decode_args(L, x, y), K_FFN, s);
 }
 
 // `zero_y`, when given, is the call's [T][d] fp32 output, zeroed by the same launch.
@@ -493,18 +632,19 @@ moe_status route_into(moe_layer* L, const uint16_t* x, int T, const float* zbias
                       bool publish, cudaStream_t s, float* zero_y = nullptr) {
     RouterParams p{x, T, L->sh.d_model, L->sh.n_experts, L->sh.top_k, L->d_router_codes, L->d_router_sb, zbias,
                    L->d_logits, L->d_rcount, ids, gates, publish ? L->h_pub_dev : nullptr, L->seq,
-                   zero_y, zero_y ? T * L->sh.d_model : 0};
+                   zero_y, zero_y ? T * L->sh.d_model : 0, L->ctx->trace_span(K_ROUTER, L->id, L->seq)};
     Prof pr(L->ctx, s, K_ROUTER, (double)L->router_bytes + 2.0 * T * L->sh.d_model,
             2.0 * T * L->sh.n_experts * L->sh.d_model);
-    CUDA_TRY(launch_router(p, s));
+    CUDA_TRY(launch_router(p, s, true));
     L->stats.bytes_resident += L->router_bytes;
     return MOE_OK;
 }
 
-// The experts of one call: the shared expert on every token (family 0), then
-// the routed experts - hits first, then misses in miss order - and the
-// combine y = shared + sum_r g_r o_r.
-moe_status run_experts(moe_layer* L, const uint16_t* x, int T, float* y, const std::vector<int>& ready_of_miss,
+// The routed experts of a decode call, added into y (which already holds the
+// shared expert's output): one launch over the hits, whose weights are
+// resident, then one over the misses in miss order, whose producers wait for
+// each expert's ready flag.
+moe_status run_experts(moe_layer* L, const uint16_t* x, int T, float* y, const std::vector<MissFlags>& ready_of_miss,
                        cudaEvent_t copies_done, cudaStream_t s) {
     moe_ctx* C = L->ctx;
     const moe_shapes& sh = L->sh;
@@ -513,8 +653,6 @@ moe_status run_experts(moe_layer* L, const uint16_t* x, int T, float* y, const s
     L->perm.resize(npairs);
     group_pairs(L->h_ids.data(), npairs, sh.n_experts, L->offsets.data(), L->perm.data());
     std::vector<Item> items, miss;
-    for (int t0 = 0; t0 < T; t0 += kFfnMaxNT)
-        items.push_back(Item{L->d_shared, t0, std::min(T, t0 + kFfnMaxNT), nullptr, -1, 0});
     int nb = 0;
     size_t mi = 0;
     for (int e : L->step.distinct) {
@@ -528,30 +666,22 @@ moe_status run_experts(moe_layer* L, const uint16_t* x, int T, float* y, const s
             w = C->staging + (size_t)nb * L->ebytes;
             ++nb;
         }
-        const int ready = is_miss ? ready_of_miss[mi] : -1;
+        const MissFlags f = is_miss ? ready_of_miss[mi] : MissFlags{};
         for (int b = L->offsets[e]; b < L->offsets[e + 1]; b += kFfnMaxNT)
             (is_miss ? miss : items)
-                .push_back(Item{w, b, std::min(b + kFfnMaxNT, (int)L->offsets[e + 1]), L->perm.data(), ready, 1});
+                .push_back(Item{w, b, std::min(b + kFfnMaxNT, (int)L->offsets[e + 1]), L->perm.data(), f.gu, f.dn, 1});
     }
-    items.insert(items.end(), miss.begin(), miss.end());
-    FfnArgs a{};
-    a.x = x;
-    a.d = sh.d_model;
-    a.act = sh.act;
-    a.fam[0] = FfnFam{0, sh.d_ff_shared, 1};
-    a.fam[1] = FfnFam{0, sh.d_ff, sh.top_k};
-    a.gates = L->d_gates;
-    a.y = y;  // zeroed by the router launch of this call
-    a.ready = L->d_ready;
-    a.err = C->err_dev;
-    a.trace = nullptr;
+    const FfnArgs a = decode_args(L, x, y);
+    moe_status st = launch_items_any(L, items, a, K_FFN, s);
+    if (st != MOE_OK) return st;
+    // exposed copy time: from the end of the resident work to the last copy
     WaitRec w{};
     if (copies_done) {
         w.ffn_start = C->timing_event();
         w.copies_done = copies_done;
         CUDA_TRY(cudaEventRecord(w.ffn_start, s));
     }
-    moe_status st = launch_items_any(L, items, a, s);
+    st = launch_items_any(L, miss, a, K_FFN_MISS, s);
     if (copies_done) L->waits.push_back(w);
     return st;
 }
@@ -563,7 +693,7 @@ moe_status run_experts(moe_layer* L, const uint16_t* x, int T, float* y, const s
 // y += sum_r g_r o_r. Hits come before misses in the job order, so the
 // resident experts run while the copies land.
 moe_status run_experts_prefill(moe_layer* L, const uint16_t* x, int T, float* y,
-                               const std::vector<int>& ready_of_miss, cudaEvent_t copies_done, cudaStream_t s) {
+                               const std::vector<MissFlags>& ready_of_miss, cudaEvent_t copies_done, cudaStream_t s) {
     moe_ctx* C = L->ctx;
     const moe_shapes& sh = L->sh;
     const int k = sh.top_k, d = sh.d_model, P = T * k;
@@ -573,7 +703,7 @@ moe_status run_experts_prefill(moe_layer* L, const uint16_t* x, int T, float* y,
     group_pairs(L->h_ids.data(), P, sh.n_experts, L->offsets.data(), L->perm.data());
     PfItem* items = reinterpret_cast<PfItem*>(L->h_pf);
     int n = 0;
-    items[n++] = PfItem{L->d_shared, 0, T, -1, 0};
+    items[n++] = PfItem{L->d_shared, 0, T, -1, -1};
     std::vector<PfItem> miss;
     int nb = 0;
     size_t mi = 0;
@@ -583,7 +713,8 @@ moe_status run_experts_prefill(moe_layer* L, const uint16_t* x, int T, float* y,
         const bool is_miss = mi < L->step.miss_experts.size() && L->step.miss_experts[mi] == e;
         const int slot = is_miss ? L->step.miss_slots[mi] : L->cache.slot_of(e);
         const uint8_t* w = slot >= 0 ? L->d_slots + (size_t)slot * L->ebytes : C->staging + (size_t)(nb++) * L->ebytes;
-        const PfItem it{w, L->offsets[e], L->offsets[e + 1] - L->offsets[e], is_miss ? ready_of_miss[mi] : -1, 0};
+        const MissFlags f = is_miss ? ready_of_miss[mi] : MissFlags{};
+        const PfItem it{w, L->offsets[e], L->offsets[e + 1] - L->offsets[e], f.gu, f.dn};
         if (it.np > kPfMaxN) return set_error(MOE_EINVAL, "expert %d has %d rows in one chunk", e, it.np);
         if (is_miss)
             miss.push_back(it);
@@ -684,6 +815,7 @@ moe_status forward_chunk(moe_layer* L, const uint16_t* x, int T, const float* zb
     const moe_shapes& sh = L->sh;
     const int npairs = T * sh.top_k;
     auto t0 = std::chrono::steady_clock::now();
+    C->trace_mark("call", L->id, L->seq + 1);
     // the layer's previous call and any copies moe_cache_step issued come first;
     // a call on the stream that recorded ev_done is already ordered after it
     if (!L->have_last_stream || L->last_stream != s) CUDA_TRY(cudaStreamWaitEvent(s, L->ev_done, 0));
@@ -698,12 +830,18 @@ moe_status forward_chunk(moe_layer* L, const uint16_t* x, int T, const float* zb
     }
     ++L->seq;
     // a decode call's experts add into y, which the router launch zeroes
-    moe_status st = route_into(L, x, T, zbias, L->d_ids, L->d_gates, true, s, T <= kDecodeMaxT ? y : nullptr);
+    const bool decode = T <= kDecodeMaxT;
+    moe_status st = route_into(L, x, T, zbias, L->d_ids, L->d_gates, true, s, decode ? y : nullptr);
     if (st != MOE_OK) return st;
+    if (decode) {
+        st = run_shared(L, x, T, y, s);
+        if (st != MOE_OK) return st;
+    }
     L->stats.host_issue_us += us_since(t0);
     t0 = std::chrono::steady_clock::now();
     st = wait_published(L, npairs);
     L->stats.host_wait_us += us_since(t0);
+    C->trace_mark("ids", L->id, L->seq);
     if (st != MOE_OK) return st;
     t0 = std::chrono::steady_clock::now();
     st = check_err_word(C);
@@ -715,8 +853,9 @@ moe_status forward_chunk(moe_layer* L, const uint16_t* x, int T, const float* zb
     L->stats.misses += L->step.miss_experts.size();
     L->stats.bypass += L->step.bypass;
     const uint32_t epoch = ++L->epoch;
-    std::vector<int> ready_of_miss;
+    std::vector<MissFlags> ready_of_miss;
     st = issue_miss_copies(L, L->step, true, epoch, &ready_of_miss);
+    C->trace_mark("copies", L->id, L->seq);
     if (st != MOE_OK) return st;
     cudaEvent_t copies_done = nullptr;
     if (!L->step.miss_experts.empty() && C->profiling) {  // exposed copy time: profiling only
@@ -734,6 +873,7 @@ moe_status forward_chunk(moe_layer* L, const uint16_t* x, int T, const float* zb
     L->have_last_stream = true;
     if (L->step.bypass > 0) CUDA_TRY(cudaEventRecord(C->staging_free, s));
     L->stats.host_issue_us += us_since(t0);
+    C->trace_mark("end", L->id, L->seq);
     return MOE_OK;
 }
 
@@ -777,15 +917,65 @@ extern "C" moe_status moe_ctx_create(int device, moe_ctx** out) {
         return set_error(MOE_ECUDA, "stream/event creation failed");
     }
     *C->err_host = 0;
+    if (const char* tp = getenv("MOE_TRACE_FILE")) {
+        if (*tp && cudaMalloc(&C->trace_spans, sizeof(unsigned long long) * 2 * kTraceSpans) == cudaSuccess) {
+            std::vector<unsigned long long> init(2 * kTraceSpans, 0ull);
+            for (int i = 0; i < kTraceSpans; ++i) init[2 * i] = ~0ull;
+            cudaMemcpy(C->trace_spans, init.data(), init.size() * sizeof(unsigned long long), cudaMemcpyHostToDevice);
+            C->trace_path = tp;
+        }
+        cudaGetLastError();
+    }
     *out = C;
     return MOE_OK;
 }
+
+namespace {
+
+// Writes the timeline: a calibration line (host clock before and after a
+// one-thread kernel that reads %globaltimer, and the value it read), then one
+// line per launch and per host step.
+void write_trace(moe_ctx* C) {
+    cudaDeviceSynchronize();
+    std::vector<unsigned long long> spans(2 * C->trace_launches.size());
+    if (!spans.empty())
+        cudaMemcpy(spans.data(), C->trace_spans, spans.size() * sizeof(unsigned long long), cudaMemcpyDeviceToHost);
+    unsigned long long* d = C->trace_spans;  // reuse slot 0's words for the calibration read
+    const uint64_t h0 = realtime_ns();
+    read_globaltimer<<<1, 1>>>(d);
+    unsigned long long g = 0;
+    cudaMemcpy(&g, d, sizeof(g), cudaMemcpyDeviceToHost);
+    const uint64_t h1 = realtime_ns();
+    FILE* f = fopen(C->trace_path.c_str(), "w");
+    if (!f) return;
+    fprintf(f, "cal %llu %llu %llu\n", (unsigned long long)h0, (unsigned long long)h1, g);
+    for (const TraceLaunch& t : C->trace_launches)
+        fprintf(f, "launch %d %d %u %llu %llu %llu\n", t.kind, t.layer, t.seq, (unsigned long long)t.t_host,
+                spans[2 * t.slot], spans[2 * t.slot + 1]);
+    for (const TraceHost& t : C->trace_host)
+        fprintf(f, "host %s %d %u %llu\n", t.what, t.layer, t.seq, (unsigned long long)t.t);
+    // copies: host issue time, then start and end in ms after the first copy's start
+    for (const moe_ctx::TraceCopy& t : C->trace_copies) {
+        float a = 0, b = 0;
+        cudaEventElapsedTime(&a, C->trace_copies[0].a, t.a);
+        cudaEventElapsedTime(&b, C->trace_copies[0].a, t.b);
+        fprintf(f, "copy %zu %llu %.4f %.4f\n", t.bytes, (unsigned long long)t.t_host, a, b);
+    }
+    fclose(f);
+    cudaGetLastError();
+}
+
+}  // namespace
 
 extern "C" void moe_ctx_destroy(moe_ctx* C) {
     if (!C) return;
     cudaSetDevice(C->device);
     cudaStreamSynchronize(C->copy_stream);
     drain_prof(C);
+    if (C->trace_spans) {
+        write_trace(C);
+        cudaFree(C->trace_spans);
+    }
     for (cudaEvent_t e : C->timing_pool) cudaEventDestroy(e);
     cudaFree(C->staging);
     cudaFreeHost(C->err_host);
@@ -831,6 +1021,10 @@ extern "C" moe_status moe_layer_create(moe_ctx* C, const moe_shapes* s, const mo
     moe_layer* L = new (std::nothrow) moe_layer(s->n_experts, slots, policy);
     if (!L) return set_error(MOE_ENOMEM, "out of host memory");
     L->ctx = C;
+    {
+        static std::atomic<int> next_id{0};
+        L->id = next_id++;
+    }
     L->sh = *s;
     L->S = slots;
     L->policy = policy;

@@ -19,6 +19,7 @@
 #include <algorithm>
 
 #include "moe_internal.h"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -140,6 +141,15 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(const RouterP
     const int runs = p.d >> 4;
     const int vec = p.d >> 3;
     const bool has_row = e < p.E;
+    // the next kernel may start now; this one reads x and writes y only
+    // after the previous kernel has finished (griddepcontrol.wait below)
+    ptx::pdl_launch_dependents();
+    if (p.span && threadIdx.x == 0) atomicMin(p.span, (unsigned long long)ptx::globaltimer());
+    const uint8_t* row0 = p.codes + (size_t)(has_row ? e : 0) * p.d;
+    if (has_row)
+        for (int c = lane; c < runs && c < 32 * kRouterBatch; c += 32)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(row0 + (size_t)c * 16));
+    ptx::pdl_wait();
     if (p.zero) {
         const int nb = gridDim.x * gridDim.y * blockDim.x;
         for (int i = (blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x; i < p.zero_n; i += nb)
@@ -225,7 +235,10 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(const RouterP
         is_last = prev == gridDim.x - 1;
     }
     __syncthreads();
-    if (!is_last) return;
+    if (!is_last) {
+        if (p.span && threadIdx.x == 0) atomicMax(p.span + 1, (unsigned long long)ptx::globaltimer());
+        return;
+    }
     for (int j = warp; j < nt; j += kRouterWarps) {
         const int t = t0 + j;
         unsigned long long* hid = p.host_ids ? p.host_ids + (size_t)t * p.k : nullptr;
@@ -237,7 +250,10 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(const RouterP
                           p.gates + (size_t)t * p.k, hid, p.seq);
     }
     __syncthreads();
-    if (threadIdx.x == 0) p.counters[blockIdx.y] = 0;
+    if (threadIdx.x == 0) {
+        p.counters[blockIdx.y] = 0;
+        if (p.span) atomicMax(p.span + 1, (unsigned long long)ptx::globaltimer());
+    }
 }
 
 __global__ void combine_kernel(const float* __restrict__ o, const float* __restrict__ gates, int k, int d,
@@ -252,7 +268,7 @@ __global__ void combine_kernel(const float* __restrict__ o, const float* __restr
 
 }  // namespace
 
-cudaError_t launch_router(const RouterParams& p, cudaStream_t s) {
+cudaError_t launch_router(const RouterParams& p, cudaStream_t s, bool pdl) {
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(router_kernel<kRouterTB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -263,13 +279,16 @@ cudaError_t launch_router(const RouterParams& p, cudaStream_t s) {
         attr = true;
     }
     const size_t sm = (size_t)std::min(kRouterTB, p.T) * p.d * 2;
+    cudaLaunchAttribute la;
     if (p.T == 1) {
-        router_kernel<1><<<dim3((p.E + kRouterWarps - 1) / kRouterWarps, 1), kRouterWarps * 32, sm, s>>>(p);
-    } else {
-        dim3 grid((p.E + kRouterWarps - 1) / kRouterWarps, (p.T + kRouterTB - 1) / kRouterTB);
-        router_kernel<kRouterTB><<<grid, kRouterWarps * 32, sm, s>>>(p);
+        const cudaLaunchConfig_t c =
+            launch_config(dim3((p.E + kRouterWarps - 1) / kRouterWarps, 1), dim3(kRouterWarps * 32), sm, s, pdl, &la);
+        return cudaLaunchKernelEx(&c, router_kernel<1>, p);
     }
-    return cudaGetLastError();
+    const cudaLaunchConfig_t c = launch_config(
+        dim3((p.E + kRouterWarps - 1) / kRouterWarps, (p.T + kRouterTB - 1) / kRouterTB), dim3(kRouterWarps * 32), sm, s,
+        pdl, &la);
+    return cudaLaunchKernelEx(&c, router_kernel<kRouterTB>, p);
 }
 
 cudaError_t launch_combine(const float* o, const float* gates, int T, int k, int d, float* y, cudaStream_t s) {

@@ -46,15 +46,11 @@
 namespace moe {
 namespace {
 
-constexpr int kCons = 8;  // consumer warps
-constexpr int kThreads = (kCons + 1) * 32;
 constexpr int kStages = 4;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kRecord = 1152;                     // gate/up: 64 inputs x 32 rows of codes, then 32 scale/bias words
-constexpr int kStageBytes = 2 * kCons * kRecord;  // gate/up stage: kCons groups of gate and of up
 constexpr int kHalf = 512;                        // down: codes of 32 rows x 32 inputs
 constexpr int kSbBlock = 128;                     // down: scale/bias words of 32 rows
-constexpr int kDnTiles = kStageBytes / (kHalf + kSbBlock);  // down row tiles a stage can hold
 constexpr int kBarCons = 1;                       // named barrier of the consumer warps
 constexpr int kStageCap = 64 * 1024;              // bytes of staged inputs per CTA
 
@@ -221,9 +217,20 @@ __device__ __forceinline__ Unit unit_of(const FfnArgs& a, int u) {
     return r;
 }
 
-template <int NT, class L>
-__global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) ffn_kernel(const __grid_constant__ FfnArgs a,
-                                                                        const __grid_constant__ L list) {
+// C consumer warps (8 or 16) and one producer warp per CTA.
+template <int C>
+struct Shape {
+    static constexpr int kThreads = (C + 1) * 32;
+    static constexpr int kStageBytes = 2 * C * kRecord;  // gate/up stage: C groups of gate and of up
+    static constexpr int kDnTiles = kStageBytes / (kHalf + kSbBlock);  // down row tiles a stage can hold
+};
+
+template <int NT, int C, class L>
+__global__ void __launch_bounds__(Shape<C>::kThreads, (C == 8 && NT == 1) ? 2 : 1)
+    ffn_kernel(const __grid_constant__ FfnArgs a, const __grid_constant__ L list) {
+    constexpr int kCons = C;
+    constexpr int kStageBytes = Shape<C>::kStageBytes;
+    constexpr int kDnTiles = Shape<C>::kDnTiles;
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* ring = smem;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
@@ -245,6 +252,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) ffn_kernel(const __
     const int dn_per = (tiles_d + dn_stages - 1) / dn_stages;  // down row tiles per stage
 
     unsigned long long* tr = a.trace ? a.trace + (size_t)blockIdx.x * kFfnTracePoints : nullptr;
+    if (a.span && threadIdx.x == 0) atomicMin(a.span, (unsigned long long)ptx::globaltimer());
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             ptx::mbar_init(full + i, 1);
@@ -260,6 +268,9 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) ffn_kernel(const __
     if (threadIdx.x < kCons * 32 && lane == 0) staged_key[warp][0] = -1;
     __syncthreads();
     volatile int* abortp = &abort_flag;
+    // the next kernel may start now: it waits for this one before it writes
+    // anything this one reads
+    ptx::pdl_launch_dependents();
 
     if (warp == kCons) {
         // ---------------- producer ----------------
@@ -268,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) ffn_kernel(const __
             uint32_t phase = 1;  // a fresh "empty" barrier counts as released
             int issued = 0;
             bool ok = true;
-            int ready_item = -1;  // last item whose ready flag was confirmed
+            int ready_gu = -1, ready_dn = -1;  // last items whose gate/up (down) flag was confirmed
             auto next_stage = [&](uint32_t bytes) -> unsigned char* {
                 if (!ptx::mbar_wait_sleep(empty + slot, phase, abortp)) return nullptr;
                 ptx::mbar_arrive_expect_tx(full + slot, bytes);
@@ -284,13 +295,13 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) ffn_kernel(const __
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
                 const Unit un = unit_of(a, u);
                 const FfnItem& it = list.item[un.item];
-                if (it.ready >= 0 && ready_item != un.item) {
+                if (it.ready >= 0 && ready_gu != un.item) {
                     if (!wait_value(a.ready + it.ready, list.epoch, abortp)) {
                         ok = false;
                         break;
                     }
                     asm volatile("fence.proxy.async.global;" ::: "memory");
-                    ready_item = un.item;
+                    ready_gu = un.item;
                 }
                 const int inter = a.fam[un.fam].inter;
                 const size_t mat = qmat_bytes(inter, a.d);  // bytes of each of gate, up, down
@@ -308,6 +319,14 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) ffn_kernel(const __
                     advance();
                 }
                 // down: input chunk c of every row tile, and the scale blocks of group c / 2
+                if (ok && it.ready_dn >= 0 && ready_dn != un.item) {
+                    if (!wait_value(a.ready + it.ready_dn, list.epoch, abortp)) {
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    ready_dn = un.item;
+                }
                 const unsigned char* dn = it.w + 2 * mat;
                 const unsigned char* dc = dn + (size_t)un.c * tiles_d * kHalf;
                 const unsigned char* ds = dn + down_codes_bytes(a.d, inter) + (size_t)(un.c >> 1) * tiles_d * kSbBlock;
@@ -489,6 +508,10 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) ffn_kernel(const __
         ptx::named_sync(kBarCons, kCons * 32);
         if (tr && first_unit && warp == 0 && lane == 0) tr[2] = ptx::globaltimer();
         // ---- down: columns 32c .. 32c+31 of every row, added into y ----
+        // y was zeroed by an earlier kernel on the stream: before the first
+        // add, wait until the previous kernel (and so everything before it)
+        // has finished
+        if (first_unit) ptx::pdl_wait();
         constexpr bool kHReg = NT <= 2;  // h of the unit in registers for the whole down pass
         float hq[NT];
         float hr[kHReg ? NT : 1][32];
@@ -531,6 +554,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1) ffn_kernel(const __
         first_unit = false;
     }
     if (tr && warp == 0 && lane == 0) tr[4] = ptx::globaltimer();
+    if (a.span && warp == 0 && lane == 0) atomicMax(a.span + 1, (unsigned long long)ptx::globaltimer());
 }
 
 int sms() {
@@ -545,34 +569,35 @@ int sms() {
 
 // Shared memory: ring, barriers, per-warp staged inputs (NT rows of
 // `xs_stride` inputs), the cross-warp sums, h, and the group and h sums.
-template <int NT>
+template <int NT, int C>
 size_t ffn_smem(int xs_stride) {
-    return (size_t)kStages * kStageBytes + 2 * kStages * sizeof(uint64_t) +
-           sizeof(float) * ((size_t)kCons * NT * xs_stride + (size_t)kCons * NT * 64 + NT * 32 +
-                            (size_t)kCons * NT * (xs_stride / 64) + NT);
+    return (size_t)kStages * Shape<C>::kStageBytes + 2 * kStages * sizeof(uint64_t) +
+           sizeof(float) * ((size_t)C * NT * xs_stride + (size_t)C * NT * 64 + NT * 32 +
+                            (size_t)C * NT * (xs_stride / 64) + NT);
 }
 
 // Staged groups per warp and pass: all of a row's when they fit kStageCap.
-constexpr int groups_per_warp_cap(int nt) { return kStageCap / (4 * 64 * nt * kCons); }
+constexpr int groups_per_warp_cap(int nt, int c) { return kStageCap / (4 * 64 * nt * c); }
 
-template <int NT, class L>
-cudaError_t ffn_launch(FfnArgs a, const L& list, cudaStream_t s) {
+template <int NT, int C, class L>
+cudaError_t ffn_launch(FfnArgs a, const L& list, cudaStream_t s, bool pdl) {
     static int per_sm = 0;
     static size_t attr_smem = 0;
-    const int cap = groups_per_warp_cap(NT);
-    const int worst = ffn_smem<NT>(std::min(cap, (kMaxDModel / 64 + kCons - 1) / kCons) * 64);
+    constexpr int kThreads = Shape<C>::kThreads;
+    const int cap = groups_per_warp_cap(NT, C);
+    const int worst = ffn_smem<NT, C>(std::min(cap, (kMaxDModel / 64 + C - 1) / C) * 64);
     if ((size_t)worst > attr_smem) {
-        cudaError_t e = cudaFuncSetAttribute(ffn_kernel<NT, L>, cudaFuncAttributeMaxDynamicSharedMemorySize, worst);
+        cudaError_t e = cudaFuncSetAttribute(ffn_kernel<NT, C, L>, cudaFuncAttributeMaxDynamicSharedMemorySize, worst);
         if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ffn_kernel<NT, L>, kThreads, worst);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ffn_kernel<NT, C, L>, kThreads, worst);
         if (e != cudaSuccess) return e;
         if (per_sm < 1) return cudaErrorInvalidConfiguration;
         attr_smem = worst;
     }
     const int G1 = a.d / 64;
-    const int gpw = std::min((G1 + kCons - 1) / kCons, cap);
+    const int gpw = std::min((G1 + C - 1) / C, cap);
     a.xs_stride = gpw * 64;
-    a.kchunk = gpw * kCons;
+    a.kchunk = gpw * C;
     int units = 0;
     for (int f = 0; f < kFfnFams; ++f) {
         if (a.fam[f].n_items && (a.fam[f].inter % 32 || a.fam[f].x_div < 1)) return cudaErrorInvalidValue;
@@ -580,25 +605,29 @@ cudaError_t ffn_launch(FfnArgs a, const L& list, cudaStream_t s) {
     }
     if (a.fam[0].n_items + a.fam[1].n_items != list.n_items || a.d % 256 || units == 0) return cudaErrorInvalidValue;
     const int grid = std::min(units, per_sm * sms());
-    ffn_kernel<NT, L><<<grid, kThreads, ffn_smem<NT>(a.xs_stride), s>>>(a, list);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr;
+    const cudaLaunchConfig_t c =
+        launch_config(dim3(grid), dim3(kThreads), ffn_smem<NT, C>(a.xs_stride), s, pdl, &attr);
+    return cudaLaunchKernelEx(&c, ffn_kernel<NT, C, L>, a, list);
 }
 
 }  // namespace
 
 template <class L>
-cudaError_t launch_ffn(const FfnArgs& a, const L& list, cudaStream_t s) {
+cudaError_t launch_ffn(const FfnArgs& a, const L& list, cudaStream_t s, bool pdl) {
     if (list.n_items == 0) return cudaSuccess;
     int m = 0;
     for (int i = 0; i < list.n_items; ++i) m = std::max(m, (int)list.item[i].np);
-    if (m <= 1) return ffn_launch<1>(a, list, s);
-    if (m <= 2) return ffn_launch<2>(a, list, s);
-    if (m <= 4) return ffn_launch<4>(a, list, s);
-    if (m <= kFfnMaxNT) return ffn_launch<8>(a, list, s);
+    // one or two rows per item: 16 consumer warps (one CTA per SM); more rows
+    // need more registers per thread, and get 8
+    if (m <= 1) return ffn_launch<1, 16>(a, list, s, pdl);
+    if (m <= 2) return ffn_launch<2, 16>(a, list, s, pdl);
+    if (m <= 4) return ffn_launch<4, 8>(a, list, s, pdl);
+    if (m <= kFfnMaxNT) return ffn_launch<8, 8>(a, list, s, pdl);
     return cudaErrorInvalidValue;
 }
 
-template cudaError_t launch_ffn<FfnSmall>(const FfnArgs&, const FfnSmall&, cudaStream_t);
-template cudaError_t launch_ffn<FfnLarge>(const FfnArgs&, const FfnLarge&, cudaStream_t);
+template cudaError_t launch_ffn<FfnSmall>(const FfnArgs&, const FfnSmall&, cudaStream_t, bool);
+template cudaError_t launch_ffn<FfnLarge>(const FfnArgs&, const FfnLarge&, cudaStream_t, bool);
 
 }  // namespace moe

@@ -251,7 +251,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = blockIdx.x; j < P.n_jobs && ok; j += gridDim.x) {
             const Job b = decode_job(P, a, j);
             const PfItem it = a.items[b.item];
-            if (lane == 0 && it.ready >= 0 && !wait_flag(a.ready + it.ready, a.epoch, abortp)) {
+            // the part of the expert this phase reads: gate/up bytes, or down bytes
+            const int flag = phase == 1 ? it.ready : it.ready_dn;
+            if (lane == 0 && flag >= 0 && !wait_flag(a.ready + flag, a.epoch, abortp)) {
                 if (!*abortp) fail(32u);
                 ok = false;
             }

@@ -107,9 +107,15 @@ struct RouterParams {
     uint32_t seq;
     float* zero;  // optional: zero_n floats set to zero by the launch (the decode output, which
     int zero_n;   // the expert FFN then adds into)
+    // optional diagnostics: {earliest block start, latest block end} in
+    // %globaltimer nanoseconds, merged with atomicMin / atomicMax; null = off
+    unsigned long long* span;
 };
 
-cudaError_t launch_router(const RouterParams& p, cudaStream_t s);
+// pdl: launch as a programmatic dependent of the previous kernel on the
+// stream. The router then only prefetches its weights before it waits for
+// that kernel to finish; it lets the next kernel start early as well.
+cudaError_t launch_router(const RouterParams& p, cudaStream_t s, bool pdl = false);
 
 // y[t][n] += sum_{r<k} gates[t][r] * o[t*k + r][n], added in rank order.
 cudaError_t launch_combine(const float* o, const float* gates, int T, int k, int d, float* y, cudaStream_t s);
@@ -122,7 +128,8 @@ cudaError_t launch_combine(const float* o, const float* gates, int T, int k, int
 // gates[p]). Pair p of family f reads x row p / x_div and adds its
 // gate-weighted FFN output into y row p / x_div. An item whose bytes are still
 // being copied names a ready flag (index into `ready`) that must reach the
-// list's epoch before its weights are read; -1 means resident.
+// list's epoch before its weights are read (the gate/up bytes and the down
+// bytes have a flag each); -1 means resident.
 //
 // Device layout of an expert blob (see repack_qmatrix / repack_down):
 // gate | up (records by 32-row tile, then group of 64 inputs) | down
@@ -136,8 +143,8 @@ constexpr int kFfnFams = 2;
 struct FfnItem {
     const uint8_t* w;  // expert blob
     int16_t pb, np;    // pair range within pair[]
-    int16_t ready;     // ready-flag index, -1 if resident
-    int16_t pad;
+    int16_t ready;     // ready-flag index of the gate and up bytes, -1 if resident
+    int16_t ready_dn;  // ready-flag index of the down bytes, -1 if resident
 };
 
 template <int MAXI, int MAXP>
@@ -170,14 +177,35 @@ struct FfnArgs {
     // (start, first weights landed, first unit's h ready, first unit done,
     // end); null = off
     unsigned long long* trace;
+    // optional diagnostics: {earliest CTA start, latest CTA end}, as for the router
+    unsigned long long* span;
 };
 constexpr int kFfnTracePoints = 5;
 
 // One launch computing, for every item, unit by unit (32 intermediate rows at
 // a time), h = act(W_g x) * (W_u x) and the matching slice of W_d h, added
 // gate-weighted into y.
+// pdl: launch as a programmatic dependent of the previous kernel on the
+// stream: the weights stream and gate/up run as soon as SMs are free, and
+// each CTA waits for that kernel to finish before its first add into y.
 template <class L>
-cudaError_t launch_ffn(const FfnArgs& a, const L& list, cudaStream_t s);
+cudaError_t launch_ffn(const FfnArgs& a, const L& list, cudaStream_t s, bool pdl = false);
+
+// Launch configuration with the programmatic-dependent-launch attribute set
+// when pdl (attr must outlive the launch call).
+inline cudaLaunchConfig_t launch_config(dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                                        cudaLaunchAttribute* attr) {
+    cudaLaunchConfig_t c{};
+    c.gridDim = grid;
+    c.blockDim = block;
+    c.dynamicSmemBytes = smem;
+    c.stream = s;
+    attr->id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr->val.programmaticStreamSerializationAllowed = 1;
+    c.attrs = attr;
+    c.numAttrs = pdl ? 1 : 0;
+    return c;
+}
 
 // Bytes of the down matrix of one expert in the column-sliced layout (equal to
 // qmat_bytes(d, inter)).
@@ -199,8 +227,8 @@ constexpr int kPfMaxN = 128;
 struct PfItem {
     const uint8_t* w;  // expert blob: gate | up | down in the tiled layout
     int32_t pb, np;    // first row and row count (sorted positions, or tokens for family 0)
-    int32_t ready;     // ready-flag index, -1 if resident
-    int32_t pad;
+    int32_t ready;     // ready-flag index of the gate and up bytes, -1 if resident
+    int32_t ready_dn;  // ready-flag index of the down bytes, -1 if resident
 };
 
 struct PfArgs {

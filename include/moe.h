@@ -198,10 +198,12 @@ moe_status moe_cache_step(moe_layer* layer, const int32_t* ids, int32_t n_ids, i
  *   route -> (host) cache step + miss copies on the copy stream, while the
  *   shared expert runs on `stream` -> routed expert FFNs (hits first, misses
  *   after their ready events) -> y[t] = shared(x_t) + sum_{r<k} gate[t][r] *
- *   FFN_{ids[t][r]}(x_t), the routed terms added in rank order.
+ *   FFN_{ids[t][r]}(x_t).
  *   FFN_e(x) = W_down,e (act(W_gate,e x) * (W_up,e x)); fp32 accumulation.
- * T <= 64 runs the decode path (fused dequant GEMV kernels, fp32 arithmetic);
- * larger T runs as prefill in chunks of 128 tokens, each chunk routed, cached
+ * T <= 64 runs the decode path (fused dequant GEMV kernels, fp32 arithmetic),
+ * which adds each expert's share of y with fp32 atomic adds: the order of
+ * those additions is not fixed, so y may differ between calls in the last
+ * bits. Larger T runs as prefill in chunks of 128 tokens, each chunk routed, cached
  * and grouped by expert before the grouped expert GEMMs on the tensor cores
  * ([P1] §2.5, §8.4), whose operands are fp16 (weights fp16(s*q + b), x, and h
  * rounded to fp16) with fp32 accumulation. Bypassed experts are streamed into
@@ -262,10 +264,12 @@ const char* moe_last_error(void);
 
 /* Per-kernel device time, measured with CUDA events recorded around each
  * launch on the launching stream while profiling is on (off by default; it
- * adds event records to the stream). kind: 0 router + top-k, 1 expert FFN
- * (shared and routed experts and the combine), 2 combine, 3 prefill grouped
- * GEMM gate/up, 4 prefill grouped GEMM down, 5 prefill token-row conversion
- * to fp16. Returns launches, total
+ * adds event records to the stream). kind: 0 router + top-k, 1 decode expert
+ * FFN over resident weights (the shared expert, and the routed experts that
+ * hit), 2 combine, 3 prefill grouped GEMM gate/up, 4 prefill grouped GEMM
+ * down, 5 prefill token-row conversion to fp16, 6 decode expert FFN over the
+ * experts copied in by the call (its duration includes the wait for the
+ * copies). Returns launches, total
  * milliseconds and the algorithmic bytes and flops of those launches. Waits
  * for the events. */
 moe_status moe_ctx_set_profiling(moe_ctx* ctx, int32_t on);
