@@ -197,13 +197,6 @@ struct moe_ctx {
     unsigned long long* trace_spans = nullptr;  // device [kTraceSpans][2]
     std::vector<TraceLaunch> trace_launches;
     std::vector<TraceHost> trace_host;
-    struct TraceCopy {
-        cudaEvent_t a, b;
-        size_t bytes;
-        uint64_t t_host;
-    };
-    std::vector<TraceCopy> trace_copies;
-    cudaEvent_t trace_base = nullptr;
 
     unsigned long long* trace_span(int kind, int layer, uint32_t seq) {
         if (!trace_spans || (int)trace_launches.size() >= kTraceSpans) return nullptr;
@@ -237,6 +230,8 @@ struct moe_layer {
     uint32_t* d_router_sb = nullptr;
     uint8_t* d_shared = nullptr;
     uint8_t* d_slots = nullptr;
+    int32_t* d_slot_of = nullptr;  // device copy of the cache's expert -> slot map (-1 = not resident)
+    std::vector<int32_t> slot_before;  // slot table before the current step (host)
     uint8_t* h_pool = nullptr;    // pinned, E * ebytes
     uint32_t* d_ready = nullptr;  // ready flags: slots, then staging entries
     uint32_t epoch = 0;           // round number of the current call
@@ -505,21 +500,10 @@ moe_status issue_miss_copies(moe_layer* L, const StepResult& r, bool with_bypass
                 }
                 ++C->copies_issued;
             }
-            moe_ctx::TraceCopy tc{};
-            if (C->trace_spans && C->trace_copies.size() < (size_t)kTraceSpans) {
-                cudaEventCreate(&tc.a);
-                cudaEventCreate(&tc.b);
-                cudaEventRecord(tc.a, C->copy_stream);
-            }
             const cudaError_t ce = injected ? cudaErrorUnknown
                                             : cudaMemcpyAsync(copies[k].dst + off, copies[k].src + off, len,
                                                               cudaMemcpyHostToDevice, C->copy_stream);
-            if (tc.a) {
-                cudaEventRecord(tc.b, C->copy_stream);
-                tc.bytes = len;
-                tc.t_host = realtime_ns();
-                C->trace_copies.push_back(tc);
-            }
+
             if (ce != cudaSuccess) return fail_from(k, ce, injected);
             if (!flags) continue;
             const int g = (int)(k / kFlagGroup);
@@ -640,12 +624,66 @@ moe_status route_into(moe_layer* L, const uint16_t* x, int T, const float* zbias
     return MOE_OK;
 }
 
+// A one-token decode call's resident work in one launch queued right behind
+// the router, before the host has read the routing: the shared expert, and
+// each routed pair whose expert the device slot table shows resident (the
+// kernel looks the experts up itself once the router has finished). Misses
+// are skipped there and launched after the cache step. *prof_index is the
+// launch's timing record (profiling), whose bytes the caller corrects once
+// the misses are known.
+moe_status run_resident_on_device(moe_layer* L, const uint16_t* x, float* y, cudaStream_t s, long* prof_index) {
+    std::vector<Item> items;
+    items.push_back(Item{L->d_shared, 0, 1, nullptr, -1, -1, 0});
+    for (int p = 0; p < L->sh.top_k; ++p) items.push_back(Item{nullptr, p, p + 1, nullptr, -1, -1, 1});
+    FfnArgs a = decode_args(L, x, y);
+    a.ids = L->d_ids;
+    a.slot_of = L->d_slot_of;
+    a.slots = L->d_slots;
+    a.ebytes = L->ebytes;
+    *prof_index = L->ctx->profiling ? (long)L->ctx->prof.size() : -1;
+    return launch_items_any(L, items, a, K_FFN, s);
+}
+
 // The routed experts of a decode call, added into y (which already holds the
 // shared expert's output): one launch over the hits, whose weights are
 // resident, then one over the misses in miss order, whose producers wait for
 // each expert's ready flag.
+// The slot-table changes of the last cache step (removals first), from the
+// table before the step and the cache after it.
+void table_changes(const moe_layer* L, std::vector<std::pair<int, int>>& out) {
+    out.clear();
+    for (int sl = 0; sl < L->S; ++sl)
+        if (L->slot_before[sl] != L->cache.slot_expert[sl] && L->slot_before[sl] >= 0)
+            out.push_back({L->slot_before[sl], -1});
+    for (int sl = 0; sl < L->S; ++sl)
+        if (L->slot_before[sl] != L->cache.slot_expert[sl] && L->cache.slot_expert[sl] >= 0)
+            out.push_back({L->cache.slot_expert[sl], sl});
+}
+
+// The whole device slot table, from the cache, ordered on `s` (the source
+// is staged by the copy call, so it may change as soon as the call returns).
+moe_status table_upload(moe_layer* L, cudaStream_t s) {
+    std::vector<int32_t> t(L->sh.n_experts, -1);
+    for (int sl = 0; sl < L->S; ++sl)
+        if (L->cache.slot_expert[sl] >= 0) t[L->cache.slot_expert[sl]] = sl;
+    CUDA_TRY(cudaMemcpyAsync(L->d_slot_of, t.data(), t.size() * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+    return MOE_OK;
+}
+
+// The same outside any call: after the layer's earlier work, synchronously.
+moe_status table_upload_sync(moe_layer* L) {
+    if (L->ev_done) CUDA_TRY(cudaEventSynchronize(L->ev_done));
+    moe_status st = table_upload(L, L->ctx->copy_stream);
+    if (st != MOE_OK) return st;
+    CUDA_TRY(cudaStreamSynchronize(L->ctx->copy_stream));
+    return MOE_OK;
+}
+
+// device_hits: the hits were already launched before the cache step, resolved
+// on the device (see launch_routed_on_device); launch the misses only, which
+// also carry the step's slot-table changes.
 moe_status run_experts(moe_layer* L, const uint16_t* x, int T, float* y, const std::vector<MissFlags>& ready_of_miss,
-                       cudaEvent_t copies_done, cudaStream_t s) {
+                       cudaEvent_t copies_done, cudaStream_t s, bool device_hits = false) {
     moe_ctx* C = L->ctx;
     const moe_shapes& sh = L->sh;
     const int npairs = T * sh.top_k;
@@ -671,9 +709,24 @@ moe_status run_experts(moe_layer* L, const uint16_t* x, int T, float* y, const s
             (is_miss ? miss : items)
                 .push_back(Item{w, b, std::min(b + kFfnMaxNT, (int)L->offsets[e + 1]), L->perm.data(), f.gu, f.dn, 1});
     }
-    const FfnArgs a = decode_args(L, x, y);
-    moe_status st = launch_items_any(L, items, a, K_FFN, s);
+    FfnArgs a = decode_args(L, x, y);
+    moe_status st = device_hits ? MOE_OK : launch_items_any(L, items, a, K_FFN, s);
     if (st != MOE_OK) return st;
+    std::vector<std::pair<int, int>> upd;
+    table_changes(L, upd);
+    if (!upd.empty()) {
+        if (miss.empty() || (int)upd.size() > kFfnMaxUpd) {
+            st = table_upload(L, s);
+            if (st != MOE_OK) return st;
+        } else {
+            a.slot_of = L->d_slot_of;
+            a.n_upd = (int)upd.size();
+            for (size_t i = 0; i < upd.size(); ++i) {
+                a.upd_expert[i] = (int16_t)upd[i].first;
+                a.upd_slot[i] = (int16_t)upd[i].second;
+            }
+        }
+    }
     // exposed copy time: from the end of the resident work to the last copy
     WaitRec w{};
     if (copies_done) {
@@ -831,9 +884,16 @@ moe_status forward_chunk(moe_layer* L, const uint16_t* x, int T, const float* zb
     ++L->seq;
     // a decode call's experts add into y, which the router launch zeroes
     const bool decode = T <= kDecodeMaxT;
+    // one token: the hits are found on the device (the work list holds the
+    // shared item and the k pairs)
+    const bool device_routed = T == 1 && 1 + sh.top_k <= (int)(sizeof(FfnSmall::item) / sizeof(FfnItem));
     moe_status st = route_into(L, x, T, zbias, L->d_ids, L->d_gates, true, s, decode ? y : nullptr);
     if (st != MOE_OK) return st;
-    if (decode) {
+    long r_prof = -1;
+    if (device_routed) {
+        st = run_resident_on_device(L, x, y, s, &r_prof);
+        if (st != MOE_OK) return st;
+    } else if (decode) {
         st = run_shared(L, x, T, y, s);
         if (st != MOE_OK) return st;
     }
@@ -846,8 +906,19 @@ moe_status forward_chunk(moe_layer* L, const uint16_t* x, int T, const float* zb
     t0 = std::chrono::steady_clock::now();
     st = check_err_word(C);
     if (st != MOE_OK) return st;
+    L->slot_before = L->cache.slot_expert;
     if (!L->cache.step(L->h_ids.data(), npairs, L->step))
         return set_error(MOE_ESTATE, "router produced an invalid id");
+    if (device_routed) {
+        // the resident launch counted every routed pair as a hit
+        const size_t n_miss = L->step.miss_experts.size();
+        const double mb = (double)n_miss * L->ebytes;
+        L->stats.bytes_resident -= (uint64_t)mb;
+        if (r_prof >= 0 && r_prof < (long)C->prof.size()) {
+            C->prof[r_prof].bytes -= mb;
+            C->prof[r_prof].flops -= 6.0 * n_miss * sh.d_model * sh.d_ff;
+        }
+    }
     L->stats.steps += 1;
     L->stats.hits += L->step.hits;
     L->stats.misses += L->step.miss_experts.size();
@@ -856,14 +927,21 @@ moe_status forward_chunk(moe_layer* L, const uint16_t* x, int T, const float* zb
     std::vector<MissFlags> ready_of_miss;
     st = issue_miss_copies(L, L->step, true, epoch, &ready_of_miss);
     C->trace_mark("copies", L->id, L->seq);
-    if (st != MOE_OK) return st;
+    if (st != MOE_OK) {
+        table_upload(L, s);  // the failed slots were emptied: the device table follows
+        return st;
+    }
     cudaEvent_t copies_done = nullptr;
     if (!L->step.miss_experts.empty() && C->profiling) {  // exposed copy time: profiling only
         copies_done = C->timing_event();
         CUDA_TRY(cudaEventRecord(copies_done, C->copy_stream));
     }
-    st = T > kDecodeMaxT ? run_experts_prefill(L, x, T, y, ready_of_miss, copies_done, s)
-                         : run_experts(L, x, T, y, ready_of_miss, copies_done, s);
+    if (T > kDecodeMaxT) {
+        st = run_experts_prefill(L, x, T, y, ready_of_miss, copies_done, s);
+        if (st == MOE_OK && L->slot_before != L->cache.slot_expert) st = table_upload(L, s);
+    } else {
+        st = run_experts(L, x, T, y, ready_of_miss, copies_done, s, device_routed);
+    }
     if (st != MOE_OK) return st;
     if (ids_out) CUDA_TRY(cudaMemcpyAsync(ids_out, L->d_ids, sizeof(int32_t) * npairs, cudaMemcpyDeviceToDevice, s));
     if (gates_out)
@@ -954,13 +1032,7 @@ void write_trace(moe_ctx* C) {
                 spans[2 * t.slot], spans[2 * t.slot + 1]);
     for (const TraceHost& t : C->trace_host)
         fprintf(f, "host %s %d %u %llu\n", t.what, t.layer, t.seq, (unsigned long long)t.t);
-    // copies: host issue time, then start and end in ms after the first copy's start
-    for (const moe_ctx::TraceCopy& t : C->trace_copies) {
-        float a = 0, b = 0;
-        cudaEventElapsedTime(&a, C->trace_copies[0].a, t.a);
-        cudaEventElapsedTime(&b, C->trace_copies[0].a, t.b);
-        fprintf(f, "copy %zu %llu %.4f %.4f\n", t.bytes, (unsigned long long)t.t_host, a, b);
-    }
+
     fclose(f);
     cudaGetLastError();
 }
@@ -1000,6 +1072,7 @@ extern "C" void moe_layer_destroy(moe_layer* L) {
     cudaFree(L->d_router_sb);
     cudaFree(L->d_shared);
     cudaFree(L->d_slots);
+    cudaFree(L->d_slot_of);
     cudaFree(L->d_ready);
     cudaFreeHost(L->h_pool);
     cudaFreeHost(L->h_epochs);
@@ -1036,6 +1109,8 @@ extern "C" moe_status moe_layer_create(moe_ctx* C, const moe_shapes* s, const mo
               cudaMalloc(&L->d_router_sb, (size_t)s->n_experts * (s->d_model / 64) * 4) == cudaSuccess &&
               cudaMalloc(&L->d_shared, L->shared_bytes) == cudaSuccess &&
               cudaMalloc(&L->d_slots, (size_t)slots * L->ebytes) == cudaSuccess &&
+              cudaMalloc(&L->d_slot_of, (size_t)s->n_experts * sizeof(int32_t)) == cudaSuccess &&
+              cudaMemset(L->d_slot_of, 0xFF, (size_t)s->n_experts * sizeof(int32_t)) == cudaSuccess &&
               cudaMalloc(&L->d_ready, n_flags * sizeof(uint32_t)) == cudaSuccess &&
               cudaMemset(L->d_ready, 0, n_flags * sizeof(uint32_t)) == cudaSuccess &&
               cudaHostAlloc(&L->h_pool, (size_t)s->n_experts * L->ebytes, cudaHostAllocDefault) == cudaSuccess &&
@@ -1098,6 +1173,8 @@ extern "C" moe_status moe_layer_set_weights(moe_layer* L, const moe_host_weights
         });
     for (auto& th : pool) th.join();
     L->cache.reset();
+    moe_status st = table_upload_sync(L);
+    if (st != MOE_OK) return st;
     L->loaded = true;
     return MOE_OK;
 }
@@ -1128,6 +1205,7 @@ extern "C" moe_status moe_cache_step(moe_layer* L, const int32_t* ids, int32_t n
     if (!L || (!ids && n_ids > 0) || n_ids < 0) return set_error(MOE_EINVAL, "moe_cache_step: bad arguments");
     if (!L->loaded) return set_error(MOE_ESTATE, "moe_cache_step before moe_layer_set_weights");
     CUDA_TRY(cudaSetDevice(L->ctx->device));
+    L->slot_before = L->cache.slot_expert;
     if (!L->cache.step(ids, n_ids, L->step)) return set_error(MOE_EINVAL, "moe_cache_step: expert id out of range");
     L->stats.steps += 1;
     L->stats.hits += L->step.hits;
@@ -1136,6 +1214,11 @@ extern "C" moe_status moe_cache_step(moe_layer* L, const int32_t* ids, int32_t n
     // slots being overwritten may still be read by this layer's earlier kernels
     CUDA_TRY(cudaStreamWaitEvent(L->ctx->copy_stream, L->ev_done, 0));
     moe_status st = issue_miss_copies(L, L->step, false, ++L->epoch, nullptr);
+    // the device slot table follows the cache, behind the copies
+    if (L->slot_before != L->cache.slot_expert) {
+        moe_status tu = table_upload(L, L->ctx->copy_stream);
+        if (st == MOE_OK) st = tu;
+    }
     // the next forward treats these experts as resident: it waits for the copies first
     cudaError_t e = cudaEventRecord(L->ev_pending, L->ctx->copy_stream);
     L->pending = true;
@@ -1175,8 +1258,9 @@ extern "C" moe_status moe_forward(moe_layer* L, const void* x, int32_t T, const 
 extern "C" moe_status moe_cache_reset(moe_layer* L) {
     if (!L) return set_error(MOE_EINVAL, "layer is NULL");
     if (!L->loaded) return set_error(MOE_ESTATE, "moe_cache_reset before moe_layer_set_weights");
+    CUDA_TRY(cudaSetDevice(L->ctx->device));
     L->cache.reset();
-    return MOE_OK;
+    return table_upload_sync(L);
 }
 
 extern "C" moe_status moe_layer_stats(moe_layer* L, moe_stats* out) {

@@ -132,11 +132,14 @@ template <int NT, int M, int C>
 __device__ __forceinline__ void words_dot(const uint4 (&c)[M][C], const float* xs, int stride,
                                           float (&out)[M][NT]) {
     constexpr int W = 4 * C;
-    float2 acc[M][NT][2];
+    constexpr int A = 2;  // independent accumulators per (matrix, row); four measured no faster
+    float2 acc[M][NT][A];
 #pragma unroll
     for (int m = 0; m < M; ++m)
 #pragma unroll
-        for (int j = 0; j < NT; ++j) acc[m][j][0] = acc[m][j][1] = make_float2(0.0f, 0.0f);
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int u = 0; u < A; ++u) acc[m][j][u] = make_float2(0.0f, 0.0f);
     // with several rows of x, a full unroll would keep every word's activations
     // live at once; two words at a time keeps the register count in bounds
 #pragma unroll(NT <= 2 ? W : 2)
@@ -192,6 +195,16 @@ __device__ __forceinline__ void chunk_dot_reg(const uint4 c, const float (&h)[NT
         const float2 s = __fadd2_rn(acc[j][0], acc[j][1]);
         out[j] = s.x + s.y;
     }
+}
+
+// The weights of an item: its blob, or for a pair resolved on the device the
+// slot holding its expert, or null when that expert is not resident (the
+// unit is skipped). Reads what the router wrote: call after the wait for the
+// previous kernel.
+__device__ __forceinline__ const uint8_t* item_weights(const FfnArgs& a, const FfnItem& it, int pair) {
+    if (it.w) return it.w;
+    const int s = __ldg(a.slot_of + __ldg(a.ids + pair));
+    return s >= 0 ? a.slots + (size_t)s * a.ebytes : nullptr;
 }
 
 struct Unit {
@@ -273,6 +286,12 @@ __global__ void __launch_bounds__(Shape<C>::kThreads, (C == 8 && NT == 1) ? 2 : 
     ptx::pdl_launch_dependents();
 
     if (warp == kCons) {
+        // this call's slot-table changes (by an otherwise idle lane), once the
+        // launch that read the table has finished
+        if (lane == 1 && blockIdx.x == 0 && a.n_upd > 0) {
+            ptx::pdl_wait();
+            for (int i = 0; i < a.n_upd; ++i) const_cast<int32_t*>(a.slot_of)[a.upd_expert[i]] = a.upd_slot[i];
+        }
         // ---------------- producer ----------------
         if (lane == 0) {
             int slot = 0;
@@ -295,6 +314,9 @@ __global__ void __launch_bounds__(Shape<C>::kThreads, (C == 8 && NT == 1) ? 2 : 
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
                 const Unit un = unit_of(a, u);
                 const FfnItem& it = list.item[un.item];
+                if (!it.w) ptx::pdl_wait();  // the router's ids (a no-op once passed)
+                const uint8_t* wts = item_weights(a, it, list.pair[it.pb]);
+                if (!wts) continue;  // a miss: done by a later launch
                 if (it.ready >= 0 && ready_gu != un.item) {
                     if (!wait_value(a.ready + it.ready, list.epoch, abortp)) {
                         ok = false;
@@ -306,7 +328,7 @@ __global__ void __launch_bounds__(Shape<C>::kThreads, (C == 8 && NT == 1) ? 2 : 
                 const int inter = a.fam[un.fam].inter;
                 const size_t mat = qmat_bytes(inter, a.d);  // bytes of each of gate, up, down
                 // gate/up: row tile c of both matrices, kCons groups per stage
-                const unsigned char* gw = it.w + (size_t)un.c * G1 * kRecord;
+                const unsigned char* gw = wts + (size_t)un.c * G1 * kRecord;
                 for (int s0 = 0; s0 < G1; s0 += kCons) {
                     const int ng = min(kCons, G1 - s0);
                     unsigned char* st = next_stage((uint32_t)(2 * ng * kRecord));
@@ -327,7 +349,7 @@ __global__ void __launch_bounds__(Shape<C>::kThreads, (C == 8 && NT == 1) ? 2 : 
                     asm volatile("fence.proxy.async.global;" ::: "memory");
                     ready_dn = un.item;
                 }
-                const unsigned char* dn = it.w + 2 * mat;
+                const unsigned char* dn = wts + 2 * mat;
                 const unsigned char* dc = dn + (size_t)un.c * tiles_d * kHalf;
                 const unsigned char* ds = dn + down_codes_bytes(a.d, inter) + (size_t)(un.c >> 1) * tiles_d * kSbBlock;
                 for (int r0 = 0; r0 < tiles_d && ok; r0 += dn_per) {
@@ -394,16 +416,15 @@ __global__ void __launch_bounds__(Shape<C>::kThreads, (C == 8 && NT == 1) ? 2 : 
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
         const Unit un = unit_of(a, u);
         const FfnItem& it = list.item[un.item];
+        if (!it.w) {
+            ptx::pdl_wait();  // the router's ids (a no-op once passed)
+            if (!item_weights(a, it, list.pair[it.pb])) continue;  // the producer skips it too
+        }
         const int nt = it.np;
         const int x_div = a.fam[un.fam].x_div;
         int row[NT];
-        float gate[NT];
 #pragma unroll
-        for (int q = 0; q < NT; ++q) {
-            const int p = q < nt ? list.pair[it.pb + q] : 0;
-            row[q] = p / x_div;
-            gate[q] = q < nt ? (un.fam == 0 ? 1.0f : __ldg(a.gates + p)) : 0.0f;
-        }
+        for (int q = 0; q < NT; ++q) row[q] = (q < nt ? list.pair[it.pb + q] : 0) / x_div;
         // ---- gate/up of rows 32c .. 32c+31 ----
         float tot[2][NT];
 #pragma unroll
@@ -512,6 +533,11 @@ __global__ void __launch_bounds__(Shape<C>::kThreads, (C == 8 && NT == 1) ? 2 : 
         // add, wait until the previous kernel (and so everything before it)
         // has finished
         if (first_unit) ptx::pdl_wait();
+        // the gates were written by the router launch: read after the wait
+        float gate[NT];
+#pragma unroll
+        for (int q = 0; q < NT; ++q)
+            gate[q] = q < nt ? (un.fam == 0 ? 1.0f : __ldg(a.gates + list.pair[it.pb + q])) : 0.0f;
         constexpr bool kHReg = NT <= 2;  // h of the unit in registers for the whole down pass
         float hq[NT];
         float hr[kHReg ? NT : 1][32];
@@ -618,10 +644,11 @@ cudaError_t launch_ffn(const FfnArgs& a, const L& list, cudaStream_t s, bool pdl
     if (list.n_items == 0) return cudaSuccess;
     int m = 0;
     for (int i = 0; i < list.n_items; ++i) m = std::max(m, (int)list.item[i].np);
-    // one or two rows per item: 16 consumer warps (one CTA per SM); more rows
-    // need more registers per thread, and get 8
+    // one row per item: 16 consumer warps (one CTA per SM); more rows need more
+    // registers per thread than 17 warps leave (at most 96 when one SM
+    // sub-partition holds five of them), and get 8
     if (m <= 1) return ffn_launch<1, 16>(a, list, s, pdl);
-    if (m <= 2) return ffn_launch<2, 16>(a, list, s, pdl);
+    if (m <= 2) return ffn_launch<2, 8>(a, list, s, pdl);
     if (m <= 4) return ffn_launch<4, 8>(a, list, s, pdl);
     if (m <= kFfnMaxNT) return ffn_launch<8, 8>(a, list, s, pdl);
     return cudaErrorInvalidValue;

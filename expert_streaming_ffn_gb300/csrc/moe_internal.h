@@ -139,9 +139,10 @@ cudaError_t launch_combine(const float* o, const float* gates, int T, int k, int
 
 constexpr int kFfnMaxNT = 8;
 constexpr int kFfnFams = 2;
+constexpr int kFfnMaxUpd = 64;  // slot-table changes one launch can carry
 
 struct FfnItem {
-    const uint8_t* w;  // expert blob
+    const uint8_t* w;  // expert blob; null: a routed pair resolved on the device (see FfnArgs::ids)
     int16_t pb, np;    // pair range within pair[]
     int16_t ready;     // ready-flag index of the gate and up bytes, -1 if resident
     int16_t ready_dn;  // ready-flag index of the down bytes, -1 if resident
@@ -179,6 +180,21 @@ struct FfnArgs {
     unsigned long long* trace;
     // optional diagnostics: {earliest CTA start, latest CTA end}, as for the router
     unsigned long long* span;
+    // Items with w == null name one routed pair p (pair[pb]) whose expert is
+    // ids[p], written by the router launch before this one: if the expert's
+    // slot (slot_of[expert], -1 = not resident) holds it at the start of the
+    // call, the item's weights are slots + slot * ebytes; otherwise the item is
+    // skipped (its expert is a miss, done by a later launch).
+    const int32_t* ids;
+    const int32_t* slot_of;
+    const uint8_t* slots;
+    size_t ebytes;
+    // Slot-table changes of this call's cache step, written into slot_of once
+    // the previous kernel on the stream (the launch that read the table) has
+    // finished: slot_of[upd_expert[i]] = upd_slot[i].
+    int n_upd;
+    int16_t upd_expert[kFfnMaxUpd];
+    int16_t upd_slot[kFfnMaxUpd];
 };
 constexpr int kFfnTracePoints = 5;
 
