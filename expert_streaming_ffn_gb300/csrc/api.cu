@@ -440,15 +440,18 @@ struct MissFlags {
 constexpr int kFlagGroup = 8;
 
 // Issue the copies of one cache step's misses. A slot miss lands in its slot,
-// a bypass in the next staging entry. With flags wanted (ready_of_miss), each
-// expert is copied in two parts, every miss's gate and up matrices first and
-// then every miss's down matrix, and after each group of kFlagGroup misses'
-// part the copy stream writes `epoch` into that group's flag for the part
-// (group g: flags 2g for gate/up, 2g + 1 for down). On failure every slot
-// this step filled but whose copy is not known good is emptied, so the table
-// never claims bytes that are missing.
+// a bypass in the next staging entry. With flags wanted (ready_of_miss),
+// after each group of kFlagGroup misses the copy stream writes `epoch` into
+// that group's flags. With split, each expert is copied in two parts, every
+// miss's gate and up matrices first and then every miss's down matrix, each
+// part with its own flag (group g: 2g for gate/up, 2g + 1 for down), so that
+// gate/up work overlaps the down copies; a copy costs a few microseconds on
+// top of its bytes, so calls with many misses (prefill) copy each expert
+// whole and flag 2g covers both parts. On failure every slot this step
+// filled but whose copy is not known good is emptied, so the table never
+// claims bytes that are missing.
 moe_status issue_miss_copies(moe_layer* L, const StepResult& r, bool with_bypass, uint32_t epoch,
-                             std::vector<MissFlags>* ready_of_miss) {
+                             std::vector<MissFlags>* ready_of_miss, bool split = false) {
     moe_ctx* C = L->ctx;
     L->h_epochs[epoch % kEpochRing] = epoch;
     if (with_bypass && r.bypass > 0) {
@@ -487,10 +490,11 @@ moe_status issue_miss_copies(moe_layer* L, const StepResult& r, bool with_bypass
         return set_error(MOE_ECOPY, "copy of expert %d (slot %d) failed: %s", r.miss_experts[copies[k].i],
                          r.miss_slots[copies[k].i], injected ? "injected failure" : cudaGetErrorString(ce));
     };
-    const int parts = flags ? 2 : 1;
+    split = split && flags;
+    const int parts = split ? 2 : 1;
     for (int part = 0; part < parts; ++part) {
         const size_t off = part == 0 ? 0 : gu_bytes;
-        const size_t len = !flags ? L->ebytes : part == 0 ? gu_bytes : L->ebytes - gu_bytes;
+        const size_t len = !split ? L->ebytes : part == 0 ? gu_bytes : L->ebytes - gu_bytes;
         for (size_t k = 0; k < copies.size(); ++k) {
             bool injected = false;
             if (part == 0) {
@@ -507,7 +511,7 @@ moe_status issue_miss_copies(moe_layer* L, const StepResult& r, bool with_bypass
             if (ce != cudaSuccess) return fail_from(k, ce, injected);
             if (!flags) continue;
             const int g = (int)(k / kFlagGroup);
-            (*ready_of_miss)[copies[k].i] = MissFlags{2 * g, 2 * g + 1};
+            (*ready_of_miss)[copies[k].i] = MissFlags{2 * g, split ? 2 * g + 1 : 2 * g};
             if (k + 1 == copies.size() || (k + 1) % kFlagGroup == 0) {
                 const cudaError_t fe = set_flag(2 * g + part);
                 if (fe != cudaSuccess) return fail_from(k, fe, false);
@@ -925,7 +929,7 @@ moe_status forward_chunk(moe_layer* L, const uint16_t* x, int T, const float* zb
     L->stats.bypass += L->step.bypass;
     const uint32_t epoch = ++L->epoch;
     std::vector<MissFlags> ready_of_miss;
-    st = issue_miss_copies(L, L->step, true, epoch, &ready_of_miss);
+    st = issue_miss_copies(L, L->step, true, epoch, &ready_of_miss, L->step.miss_experts.size() <= kFlagGroup);
     C->trace_mark("copies", L->id, L->seq);
     if (st != MOE_OK) {
         table_upload(L, s);  // the failed slots were emptied: the device table follows
