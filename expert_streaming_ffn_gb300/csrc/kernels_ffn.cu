@@ -46,7 +46,6 @@
 namespace moe {
 namespace {
 
-constexpr int kStages = 4;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kRecord = 1152;                     // gate/up: 64 inputs x 32 rows of codes, then 32 scale/bias words
 constexpr int kHalf = 512;                        // down: codes of 32 rows x 32 inputs
@@ -75,7 +74,9 @@ __device__ __forceinline__ float magic_nibble(uint32_t v) {
 }
 
 __device__ __forceinline__ void codes8(uint32_t v, float2 (&o)[4]) {
-    const uint32_t w = v >> 12;
+    // v >> 12 as the high word of v * 2^20: an integer multiply-add, which
+    // runs beside the logic unit that the eight extractions keep busy
+    const uint32_t w = __umulhi(v, 1u << 20);
     const float2 off = make_float2(-8388608.0f, -8388608.0f);
     o[0] = __fadd2_rn(make_float2(magic_nibble<0xFu>(v), magic_nibble<0xF0u>(v)), off);
     o[1] = __fadd2_rn(make_float2(magic_nibble<0xF00u>(v), magic_nibble<0xF000u>(v)), off);
@@ -149,8 +150,8 @@ __device__ __forceinline__ void words_dot(const uint4 (&c)[M][C], const float* x
         for (int m = 0; m < M; ++m) codes8(word_at<C>(c[m], w), q[m]);
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
-            const float4* xp = reinterpret_cast<const float4*>(xs + j * stride + w * 8);
-            const float4 a = xp[0], b = xp[1];
+            const uint32_t xp = ptx::smem_addr(xs + j * stride + w * 8);
+            const float4 a = ptx::lds_f4(xp), b = ptx::lds_f4(xp + 16);
 #pragma unroll
             for (int m = 0; m < M; ++m) {
                 acc[m][j][0] = __ffma2_rn(q[m][0], make_float2(a.x, a.y), acc[m][j][0]);
@@ -234,14 +235,17 @@ __device__ __forceinline__ Unit unit_of(const FfnArgs& a, int u) {
 template <int C>
 struct Shape {
     static constexpr int kThreads = (C + 1) * 32;
+    // ring depth: one CTA of 16 consumer warps per SM has room for five stages
+    static constexpr int kStages = C >= 16 ? 5 : 4;
     static constexpr int kStageBytes = 2 * C * kRecord;  // gate/up stage: C groups of gate and of up
     static constexpr int kDnTiles = kStageBytes / (kHalf + kSbBlock);  // down row tiles a stage can hold
 };
 
 template <int NT, int C, class L>
-__global__ void __launch_bounds__(Shape<C>::kThreads, (C == 8 && NT == 1) ? 2 : 1)
+__global__ void __launch_bounds__(Shape<C>::kThreads, (C <= 11 && NT == 1) ? 2 : 1)
     ffn_kernel(const __grid_constant__ FfnArgs a, const __grid_constant__ L list) {
     constexpr int kCons = C;
+    constexpr int kStages = Shape<C>::kStages;
     constexpr int kStageBytes = Shape<C>::kStageBytes;
     constexpr int kDnTiles = Shape<C>::kDnTiles;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -431,9 +435,16 @@ __global__ void __launch_bounds__(Shape<C>::kThreads, (C == 8 && NT == 1) ? 2 : 
         for (int m = 0; m < 2; ++m)
 #pragma unroll
             for (int q = 0; q < NT; ++q) tot[m][q] = 0.0f;
-        for (int s0 = 0; s0 < G1; s0 += kCons) {
-            const int g0 = s0 - s0 % kchunk;  // first group of this staging pass
-            if (s0 == g0) {
+        // this warp's offsets within a stage, and its staged group of the pass
+        const uint32_t cb0 = ptx::smem_addr(ring) + warp * kRecord + lane * 16;
+        const uint32_t sb0 = ptx::smem_addr(ring) + warp * kRecord + 1024 + lane * 4;
+        int g0 = 0, i = 0;  // first group of the current staging pass, and the stage's index in it
+        for (int s0 = 0; s0 < G1; s0 += kCons, ++i) {
+            if (s0 == g0 + kchunk) {
+                g0 = s0;
+                i = 0;
+            }
+            if (i == 0) {
                 // this warp's groups of the pass, g0 + warp + kCons i, staged as
                 // position-scaled fp32 unless the same rows and pass are staged already
                 bool same = key[0] == g0 && key[1] == nt;
@@ -482,20 +493,17 @@ __global__ void __launch_bounds__(Shape<C>::kThreads, (C == 8 && NT == 1) ? 2 : 
             }
             const unsigned char* st = take_stage();
             if (st && s0 + warp < G1) {
-                const int i = (s0 - g0) / kCons;  // this warp's staged group of the pass
-                const unsigned char* cb = st + warp * kRecord + lane * 16;
-                const unsigned char* sbp = st + warp * kRecord + 1024 + lane * 4;
-                const uint4 words[2][2] = {
-                    {*reinterpret_cast<const uint4*>(cb), *reinterpret_cast<const uint4*>(cb + 512)},
-                    {*reinterpret_cast<const uint4*>(cb + kCons * kRecord),
-                     *reinterpret_cast<const uint4*>(cb + kCons * kRecord + 512)}};
-                const float2 fg = unpack_sb(*reinterpret_cast<const uint32_t*>(sbp));
-                const float2 fu = unpack_sb(*reinterpret_cast<const uint32_t*>(sbp + kCons * kRecord));
+                const uint32_t so = (uint32_t)(st - ring);  // the stage's offset in the ring
+                const uint32_t cb = cb0 + so, sbp = sb0 + so;
+                const uint4 words[2][2] = {{ptx::lds_u4(cb), ptx::lds_u4(cb + 512)},
+                                           {ptx::lds_u4(cb + kCons * kRecord), ptx::lds_u4(cb + kCons * kRecord + 512)}};
+                const float2 fg = unpack_sb(ptx::lds_u32(sbp));
+                const float2 fu = unpack_sb(ptx::lds_u32(sbp + kCons * kRecord));
                 float pr[2][NT];
                 words_dot<NT, 2, 2>(words, xme + i * 64, xs_stride, pr);
 #pragma unroll
                 for (int q = 0; q < NT; ++q) {
-                    const float xq = xsme[q * cpw + i];
+                    const float xq = ptx::lds_f32(ptx::smem_addr(xsme + q * cpw + i));
                     tot[0][q] += fmaf(fg.x, pr[0][q], fg.y * xq);
                     tot[1][q] += fmaf(fu.x, pr[1][q], fu.y * xq);
                 }
@@ -555,23 +563,30 @@ __global__ void __launch_bounds__(Shape<C>::kThreads, (C == 8 && NT == 1) ? 2 : 
                     hr[q][j + 3] = v.w;
                 }
         }
+        // this lane's output element of row tile 0 in each token's y row
+        float* yq[NT];
+#pragma unroll
+        for (int q = 0; q < NT; ++q) yq[q] = a.y + (size_t)row[q] * a.d + lane;
+        const uint32_t dc0 = ptx::smem_addr(ring) + lane * 16;
+        const uint32_t ds0 = ptx::smem_addr(ring) + kDnTiles * kHalf + lane * 4;
         for (int r0 = 0; r0 < tiles_d; r0 += dn_per) {
             const int n = min(dn_per, tiles_d - r0);
             const unsigned char* st = take_stage();
             if (st) {
+                const uint32_t so = (uint32_t)(st - ring);
                 for (int i = warp; i < n; i += kCons) {
-                    const uint4 words[1][1] = {{*reinterpret_cast<const uint4*>(st + i * kHalf + lane * 16)}};
-                    const float2 f = unpack_sb(*reinterpret_cast<const uint32_t*>(st + kDnTiles * kHalf + i * kSbBlock + lane * 4));
+                    const uint4 words[1][1] = {{ptx::lds_u4(dc0 + so + i * kHalf)}};
+                    const float2 f = unpack_sb(ptx::lds_u32(ds0 + so + i * kSbBlock));
                     float pr[1][NT];
                     if constexpr (kHReg) {
                         chunk_dot_reg<NT>(words[0][0], hr, pr[0]);
                     } else {
                         words_dot<NT, 1, 1>(words, hs, 32, pr);
                     }
-                    const int col = 32 * (r0 + i) + lane;
+                    const int col = 32 * (r0 + i);
 #pragma unroll
                     for (int q = 0; q < NT; ++q)
-                        if (q < nt) atomicAdd(a.y + (size_t)row[q] * a.d + col, gate[q] * fmaf(f.x, pr[0][q], f.y * hq[q]));
+                        if (q < nt) atomicAdd(yq[q] + col, gate[q] * fmaf(f.x, pr[0][q], f.y * hq[q]));
                 }
             }
             release_stage();
@@ -597,7 +612,7 @@ int sms() {
 // `xs_stride` inputs), the cross-warp sums, h, and the group and h sums.
 template <int NT, int C>
 size_t ffn_smem(int xs_stride) {
-    return (size_t)kStages * Shape<C>::kStageBytes + 2 * kStages * sizeof(uint64_t) +
+    return (size_t)Shape<C>::kStages * Shape<C>::kStageBytes + 2 * Shape<C>::kStages * sizeof(uint64_t) +
            sizeof(float) * ((size_t)C * NT * xs_stride + (size_t)C * NT * 64 + NT * 32 +
                             (size_t)C * NT * (xs_stride / 64) + NT);
 }
@@ -607,18 +622,14 @@ constexpr int groups_per_warp_cap(int nt, int c) { return kStageCap / (4 * 64 * 
 
 template <int NT, int C, class L>
 cudaError_t ffn_launch(FfnArgs a, const L& list, cudaStream_t s, bool pdl) {
-    static int per_sm = 0;
-    static size_t attr_smem = 0;
     constexpr int kThreads = Shape<C>::kThreads;
     const int cap = groups_per_warp_cap(NT, C);
-    const int worst = ffn_smem<NT, C>(std::min(cap, (kMaxDModel / 64 + C - 1) / C) * 64);
-    if ((size_t)worst > attr_smem) {
+    static bool attr = false;
+    if (!attr) {
+        const int worst = ffn_smem<NT, C>(std::min(cap, (kMaxDModel / 64 + C - 1) / C) * 64);
         cudaError_t e = cudaFuncSetAttribute(ffn_kernel<NT, C, L>, cudaFuncAttributeMaxDynamicSharedMemorySize, worst);
         if (e != cudaSuccess) return e;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ffn_kernel<NT, C, L>, kThreads, worst);
-        if (e != cudaSuccess) return e;
-        if (per_sm < 1) return cudaErrorInvalidConfiguration;
-        attr_smem = worst;
+        attr = true;
     }
     const int G1 = a.d / 64;
     const int gpw = std::min((G1 + C - 1) / C, cap);
@@ -630,10 +641,27 @@ cudaError_t ffn_launch(FfnArgs a, const L& list, cudaStream_t s, bool pdl) {
         units += a.fam[f].n_items * (a.fam[f].inter / 32);
     }
     if (a.fam[0].n_items + a.fam[1].n_items != list.n_items || a.d % 256 || units == 0) return cudaErrorInvalidValue;
+    // resident CTAs per SM at this launch's shared memory (cached per size)
+    const size_t smem = ffn_smem<NT, C>(a.xs_stride);
+    static size_t occ_smem[4] = {0, 0, 0, 0};
+    static int occ_val[4] = {0, 0, 0, 0};
+    int per_sm = 0;
+    for (int i = 0; i < 4 && !per_sm; ++i)
+        if (occ_smem[i] == smem) per_sm = occ_val[i];
+    if (!per_sm) {
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ffn_kernel<NT, C, L>, kThreads, smem);
+        if (e != cudaSuccess) return e;
+        if (per_sm < 1) return cudaErrorInvalidConfiguration;
+        for (int i = 3; i > 0; --i) {
+            occ_smem[i] = occ_smem[i - 1];
+            occ_val[i] = occ_val[i - 1];
+        }
+        occ_smem[0] = smem;
+        occ_val[0] = per_sm;
+    }
     const int grid = std::min(units, per_sm * sms());
-    cudaLaunchAttribute attr;
-    const cudaLaunchConfig_t c =
-        launch_config(dim3(grid), dim3(kThreads), ffn_smem<NT, C>(a.xs_stride), s, pdl, &attr);
+    cudaLaunchAttribute la;
+    const cudaLaunchConfig_t c = launch_config(dim3(grid), dim3(kThreads), smem, s, pdl, &la);
     return cudaLaunchKernelEx(&c, ffn_kernel<NT, C, L>, a, list);
 }
 
