@@ -55,6 +55,11 @@ def parse():
     ap.add_argument("--prefill-only", action="store_true",
                     help="run only the prefill leg and print its JSON (for profiling; not the bench line)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--prefill-resident-only", action="store_true",
+                    help="prefill leg: skip the streaming pass (profiling the grouped GEMMs on resident weights)")
+    ap.add_argument("--resident", action="store_true",
+                    help="every expert resident (one slot per expert, all loaded before the warm-up): "
+                         "the decode FFN launches then read HBM only (profiling)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
@@ -164,9 +169,11 @@ def gpu_bus_id(dev: int) -> str | None:
         return None
 
 
-def ncu_traffic(kernel: str):
+def ncu_traffic(kernel: str, algorithmic_bytes_per_launch=None):
     """DRAM bytes per launch of `kernel` from the committed ncu record, or None
-    when the kernel's source has changed since the counters were taken."""
+    when the kernel's source has changed since the counters were taken. A
+    record taken on a different launch size gives DRAM bytes per algorithmic
+    byte, scaled here to this run's launches."""
     import hashlib
 
     try:
@@ -177,6 +184,10 @@ def ncu_traffic(kernel: str):
         with open(os.path.join(ROOT, rec["source"]), "rb") as f:
             if hashlib.sha256(f.read()).hexdigest() != rec["source_sha256"]:
                 return None
+        if "dram_bytes_per_algorithmic_byte" in rec:
+            if algorithmic_bytes_per_launch is None:
+                return None
+            return rec["dram_bytes_per_algorithmic_byte"] * algorithmic_bytes_per_launch
         return rec["dram_bytes_per_launch"]
     except (OSError, ValueError, KeyError):
         return None
@@ -269,10 +280,13 @@ def run_ours(args, world, rank, local):
     ctx = moe.moe_ctx_create(local)
     layers, zbs = [], []
     w = None
+    slots = s.n_experts if args.resident else wl.cache_slots
     for l in range(n_layers):
         w = synth.layer_weights(s, l, seed, reuse=w)
-        h = moe.moe_layer_create(ctx, s, wl.cache_slots, wl.policy)
+        h = moe.moe_layer_create(ctx, s, slots, wl.policy)
         moe.moe_layer_set_weights(h, w)
+        if args.resident:
+            moe.moe_cache_step(h, np.arange(s.n_experts))  # copies every expert into its slot
         layers.append(h)
         zbs.append(torch.from_numpy(synth.zipf_bias(s, l, wl.zipf_s, wl.zipf_beta, seed)).to(dev))
     # inputs resident in HBM: x[step][layer][d] bf16, drawn per (step, layer)
@@ -409,9 +423,10 @@ def run_ours(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded int4/int8 weights and N(0,1) RMS-normalised bf16 activations)",
-        "config": {"workload": "decode_2816", "layers": n_layers, "tokens_per_step": 1, "d_model": s.d_model,
+        "config": {"workload": "decode_2816" + (" (every expert resident)" if args.resident else ""),
+                   "layers": n_layers, "tokens_per_step": 1, "d_model": s.d_model,
                    "experts": s.n_experts, "top_k": s.top_k, "d_ff": s.d_ff, "d_ff_shared": s.d_ff_shared,
-                   "cache_slots": wl.cache_slots, "policy": "LFU", "zipf_s": wl.zipf_s,
+                   "cache_slots": slots, "policy": "LFU", "zipf_s": wl.zipf_s,
                    "l2": f"inputs larger than L2: {resident / args.steps / 1e9:.2f} GB of weights read per step "
                          f"vs {L2_BYTES / 2**20:.0f} MiB L2",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -423,7 +438,8 @@ def run_ours(args, world, rank, local):
         "resident_GB_per_token": resident / args.steps / 1e9,
         "hbm_GBs_all_kernels": all_bytes / (all_ms * 1e-3) / 1e9 if all_ms else None,
         "roofline": {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(name),
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": ncu_traffic(name, by / n_l if n_l else None),
                      "algorithmic_bytes_per_launch": by / n_l if n_l else None,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                      else "fallback 6.8 TB/s"},
@@ -508,14 +524,17 @@ def run_prefill(args, ctx, dev, stream, seed):
 
     # (1) streaming
     layers, w = [], None
+    if args.prefill_resident_only:
+        P = 0
     for l in range(P):
         h, w = make(s, wl.cache_slots, l, w)
         layers.append(h)
-    moe.moe_forward(layers[0], xs[0][:128], y=y[:128])  # load the kernels
-    torch.cuda.synchronize(dev)
-    moe.moe_layer_destroy(layers[0])  # a fresh cache for the timed pass
-    layers[0], w = make(s, wl.cache_slots, 0, w)
-    ms, kt, stats = _prefill_pass(ctx, dev, stream, layers, xs, y)
+    if P:
+        moe.moe_forward(layers[0], xs[0][:128], y=y[:128])  # load the kernels
+        torch.cuda.synchronize(dev)
+        moe.moe_layer_destroy(layers[0])  # a fresh cache for the timed pass
+        layers[0], w = make(s, wl.cache_slots, 0, w)
+    ms, kt, stats = _prefill_pass(ctx, dev, stream, layers, xs, y) if P else (0.0, moe.moe_ctx_kernel_times(ctx), [])
     for h in layers:
         moe.moe_layer_destroy(h)
     kinds = ("gemm_gateup", "gemm_down", "pf_gather", "combine", "router")
@@ -525,8 +544,8 @@ def run_prefill(args, ctx, dev, stream, seed):
     misses = sum(x["misses"] for x in stats)
     out = {
         "workload": "prefill_2816", "layers_measured": P, "prompt_tokens": prompt, "chunk": wl.tokens,
-        "tok_s_per_layer": prompt * P / (ms * 1e-3),
-        "tok_s_30_layers": prompt / (ms * 1e-3 / P * 30),
+        "tok_s_per_layer": prompt * P / (ms * 1e-3) if P else None,
+        "tok_s_30_layers": prompt / (ms * 1e-3 / P * 30) if P else None,
         "expert_TFLOPs": fl / (kms * 1e-3) / 1e12 if kms else None,
         "expert_kernel_ms": kms, "wall_ms": ms,
         "hit_rate": hits / (hits + misses) if hits + misses else None,
