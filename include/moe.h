@@ -221,10 +221,10 @@ moe_status moe_forward(moe_layer* layer, const void* x_bf16, int32_t T, const fl
 /* Empties the layer's expert cache: every slot becomes free and every count
  * zero, as the per-layer slot cache of [P1] §6.2.2 is when created (and
  * after moe_layer_set_weights). Slot contents are not touched; the next calls
- * refill them. Orders
- * itself after the layer's earlier calls on the host side only, so call it
- * between calls, not while another thread uses the layer.
- * Errors: MOE_EINVAL (layer NULL), MOE_ESTATE (no weights). */
+ * refill them. Waits for the layer's earlier calls to finish on the device
+ * (the device copy of the slot table is rewritten), so call it between calls,
+ * not while another thread uses the layer.
+ * Errors: MOE_EINVAL (layer NULL), MOE_ESTATE (no weights), MOE_ECUDA. */
 moe_status moe_cache_reset(moe_layer* layer);
 
 /* Counters (see moe_stats). Waits for the layer's outstanding timing events. */
