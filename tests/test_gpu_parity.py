@@ -239,3 +239,103 @@ def test_cache_reset_empties_the_table(ctx):
             r.forward(synth.tokens(s, 0, 40 + step, 4, False))
     finally:
         r.close()
+
+
+# ---- one-token calls: the hits are looked up on the device in a copy of the
+# slot table, which every other path that changes the cache must keep current
+
+
+@pytest.mark.parametrize("slots,k", [(1, 2), (16, 2), (4, 1), (4, 16), (4, 24)])
+def test_one_token_degenerate_caches_and_top_k(ctx, slots, k):
+    # one slot (the rest bypasses), all resident, k = 1, k = 16, and k = 24 (more
+    # pairs than the device-routed list holds: the host-built path)
+    s = synth.Shapes(512, 32, k, 256, 512, synth.GELU_TANH)
+    r = Rig(ctx, s, 0, slots)
+    try:
+        for step in range(6):
+            r.forward(synth.tokens(s, 0, step, 1, False))
+    finally:
+        r.close()
+
+
+def test_one_token_after_cache_step_call(ctx):
+    s = synth.SHAPES_TINY
+    r = Rig(ctx, s, 0, 4)
+    try:
+        ids = np.array([[3, 5], [5, 9]], np.int32)
+        moe.moe_cache_step(r.h, ids)
+        r.cache.step(ids)
+        for step in range(4):
+            r.forward(synth.tokens(s, 0, 30 + step, 1, False))
+    finally:
+        r.close()
+
+
+def test_one_token_after_injected_copy_failure(ctx):
+    s = synth.SHAPES_TINY
+    r = Rig(ctx, s, 0, 4)
+    try:
+        for step in range(2):
+            r.forward(synth.tokens(s, 0, 40 + step, 1, False))
+        moe.moe_ctx_inject_copy_failure(ctx, 0)
+        x = torch.from_numpy(synth.tokens(s, 0, 42, 1, False).view(np.int16)).view(torch.bfloat16).cuda()
+        try:
+            moe.moe_forward(r.h, x)
+            failed = False
+        except moe.MoeError as e:
+            assert e.status == moe.MOE_ECOPY
+            failed = True
+        torch.cuda.synchronize()
+        if failed:
+            # the oracle never saw the failed call: restart both from an empty cache
+            moe.moe_layer_set_weights(r.h, r.w)
+            r.cache = oracle.Cache(s.n_experts, 4, moe.LFU)
+        else:
+            moe.moe_ctx_inject_copy_failure(ctx, -1)  # the call had no miss to fail
+            r.cache.step(oracle.topk_gates(oracle.router_logits(synth.tokens(s, 0, 42, 1, False), r.w.router,
+                                                                s.n_experts, None), s.top_k)[0])
+        for step in range(4):
+            r.forward(synth.tokens(s, 0, 43 + step, 1, False))
+    finally:
+        r.close()
+
+
+def test_one_token_mixed_with_batches_and_prefill(ctx):
+    # the host-built paths (a 4-token call, a 130-token prefill) change the cache
+    # too; one-token calls after them must see the same table as the host
+    s = synth.SHAPES_TINY
+    r = Rig(ctx, s, 3, 4)
+    try:
+        for step, T in enumerate([1, 4, 1, 130, 1, 1, 4, 1]):
+            r.forward(synth.tokens(s, 3, 50 + step, T, False), y_tokens=[0, T - 1])
+        moe.moe_cache_reset(r.h)
+        r.cache = oracle.Cache(s.n_experts, 4, moe.LFU)
+        for step in range(3):
+            r.forward(synth.tokens(s, 3, 60 + step, 1, False))
+    finally:
+        r.close()
+
+
+def test_timeline_trace_file(tmp_path, monkeypatch):
+    path = tmp_path / "trace.txt"
+    monkeypatch.setenv("MOE_TRACE_FILE", str(path))
+    c = moe.moe_ctx_create(0)
+    s = synth.SHAPES_TINY
+    try:
+        r = Rig(c, s, 0, 4)
+        try:
+            for step in range(3):
+                r.forward(synth.tokens(s, 0, 70 + step, 1, False))
+        finally:
+            r.close()
+    finally:
+        moe.moe_ctx_destroy(c)
+    lines = path.read_text().splitlines()
+    assert lines[0].startswith("cal ")
+    launches = [l.split() for l in lines if l.startswith("launch ")]
+    assert len(launches) >= 6  # a router and a resident launch per call
+    for l in launches:
+        start, end = int(l[5]), int(l[6])
+        assert 0 < start <= end  # every launch ran and recorded its span
+    marks = {l.split()[1] for l in lines if l.startswith("host ")}
+    assert {"call", "ids", "copies", "end"} <= marks
