@@ -63,14 +63,16 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 // Top-k of one token's logits by one warp. Lane l holds the candidates of
 // experts l + 32 j as 64-bit words (key << 32 | ~e), so that a larger word is
 // a larger logit or, for equal logits, a lower expert index; it sorts them
-// once, descending. Each of the k rounds then takes the warp-wide maximum of
-// the lanes' heads (one max-reduction of the keys, one of the index part
-// among the lanes that hold that key), and the lane that owned it moves to
-// its next candidate; lane r ends up with rank r. Then gates = softmax over
-// the k chosen logits.
+// once, descending. With at most 8 candidates per lane and k <= 8 the lanes'
+// lists are merged by a butterfly (below); otherwise each of the k rounds
+// takes the warp-wide maximum of the lanes' heads (one max-reduction of the
+// keys, one of the index part among the lanes that hold that key), and the
+// lane that owned it moves to its next candidate. Lane r ends up with rank r.
+// Then gates = softmax over the k chosen logits.
 template <int MAXV>
 __device__ void topk_warp(const float* logits, int E, int k, int lane, int32_t* ids, float* gates,
                           unsigned long long* host_ids, uint32_t seq) {
+    const int k_all = k;
     unsigned long long c[MAXV];
 #pragma unroll
     for (int j = 0; j < MAXV; ++j) {
@@ -90,6 +92,42 @@ __device__ void topk_warp(const float* logits, int E, int k, int lane, int32_t* 
             }
     float mine_v = -INFINITY;
     int mine_i = 0;
+    if (MAXV == 8 && k <= 8) {
+        // Butterfly merge of the lanes' sorted lists: at each step a lane keeps
+        // the 8 largest of its list and its partner's (the larger of c[j] and
+        // the partner's c[7-j] for each j is the 8 largest, in bitonic order;
+        // three half-cleaner stages sort them again). After five steps every
+        // lane holds the 8 largest overall, descending.
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            unsigned long long m[MAXV];
+#pragma unroll
+            for (int j = 0; j < MAXV; ++j) {
+                const unsigned long long o = __shfl_xor_sync(kFull, c[MAXV - 1 - j], off);
+                m[j] = c[j] > o ? c[j] : o;
+            }
+#pragma unroll
+            for (int dist = MAXV / 2; dist >= 1; dist >>= 1)
+#pragma unroll
+                for (int j = 0; j < MAXV; ++j)
+                    if ((j & dist) == 0 && m[j] < m[j + dist]) {
+                        const unsigned long long t = m[j];
+                        m[j] = m[j + dist];
+                        m[j + dist] = t;
+                    }
+#pragma unroll
+            for (int j = 0; j < MAXV; ++j) c[j] = m[j];
+        }
+        unsigned long long w = c[0];
+#pragma unroll
+        for (int j = 1; j < MAXV; ++j)
+            if (lane == j) w = c[j];
+        if (lane < k) {
+            mine_v = key_value((uint32_t)(w >> 32));
+            mine_i = (int)~(uint32_t)w;
+        }
+        k = 0;  // ranks done: skip the rounds below
+    }
     for (int r = 0; r < k; ++r) {
         const uint32_t hk = (uint32_t)(c[0] >> 32), hi = (uint32_t)c[0];
         const uint32_t top = __reduce_max_sync(kFull, hk);
@@ -106,11 +144,11 @@ __device__ void topk_warp(const float* logits, int E, int k, int lane, int32_t* 
         }
     }
     const float top = __shfl_sync(kFull, mine_v, 0);
-    const float ex = lane < k ? expf(mine_v - top) : 0.0f;
+    const float ex = lane < k_all ? expf(mine_v - top) : 0.0f;
     float sum = ex;
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
-    if (lane < k) {
+    if (lane < k_all) {
         ids[lane] = mine_i;
         gates[lane] = ex / sum;
         if (host_ids)
