@@ -110,7 +110,17 @@ typedef struct {
 
 /* Create a context on CUDA device `device` (made current on the calling
  * thread). Owns a copy stream and the transient staging arena shared by its
- * layers. Errors: MOE_EINVAL (no such device), MOE_ECUDA. */
+ * layers. If the environment variable MOE_TRACE_FILE names a file when the
+ * context is created, the context records a timeline (diagnostics): for each
+ * launch of its layers, the host's issue time (CLOCK_REALTIME ns) and the
+ * device span from the earliest block start to the latest block end
+ * (%globaltimer ns); for each call, the host's steps (call, routing seen,
+ * copies issued, end). moe_ctx_destroy writes it as text lines
+ * "cal <host ns before> <host ns after> <device ns>" (a one-thread kernel
+ * read between the two host reads), "launch <kind> <layer> <call> <host ns>
+ * <device start> <device end>" (kind as for moe_ctx_kernel_times) and
+ * "host <step> <layer> <call> <host ns>".
+ * Errors: MOE_EINVAL (no such device), MOE_ECUDA. */
 moe_status moe_ctx_create(int device, moe_ctx** out);
 void moe_ctx_destroy(moe_ctx* ctx); /* after all its layers are destroyed */
 
