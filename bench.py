@@ -300,6 +300,14 @@ def run_ours(args, world, rank, local):
     sptr = stream.cuda_stream
     row = s.d_model * 2
 
+    def reset_caches():
+        # empty caches (the cache trajectory starts again), or with --resident
+        # every expert copied back in
+        for h in layers:
+            moe.moe_cache_reset(h)
+            if args.resident:
+                moe.moe_cache_step(h, np.arange(s.n_experts))
+
     def step(st):
         base = x_dev.data_ptr() + st * n_layers * row
         for l in range(n_layers):
@@ -337,8 +345,7 @@ def run_ours(args, world, rank, local):
     # same steps again, from the same cache state (empty caches, the same
     # warm-up), with per-kernel CUDA events on the launching stream; the
     # exposed copy time is measured in this pass too (it needs events)
-    for h in layers:
-        moe.moe_cache_reset(h)
+    reset_caches()
     for st in range(args.warmup):
         step(st)
     torch.cuda.synchronize(dev)
@@ -386,8 +393,7 @@ def run_ours(args, world, rank, local):
 
         # the same cache trajectory as the timed loop: empty caches, the same
         # warm-up steps, then the same timed steps
-        for h in layers:
-            moe.moe_cache_reset(h)
+        reset_caches()
         for st in range(args.warmup):
             e2e_step(st)
         barrier(world)

@@ -157,6 +157,13 @@ __device__ void topk_warp(const float* logits, int E, int k, int lane, int32_t* 
     }
 }
 
+// The top-k for more than 256 experts, out of line: its 32 candidates per
+// lane would otherwise set the register budget of every router launch.
+__device__ __noinline__ void topk_warp_large(const float* logits, int E, int k, int lane, int32_t* ids, float* gates,
+                                             unsigned long long* host_ids, uint32_t seq) {
+    topk_warp<32>(logits, E, k, lane, ids, gates, host_ids, seq);
+}
+
 // Code byte m of a word as the float q (exact): 2^23 + q from a byte permute
 // into the magic word 0x4B000000, minus 2^23.
 __device__ __forceinline__ float byte_code(uint32_t w, int m) {
@@ -170,7 +177,7 @@ __device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
 }
 
 template <int TB>
-__global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(const RouterParams p) {
+__global__ void __launch_bounds__(kRouterWarps * 32, TB == 1 ? 5 : 1) router_kernel(const RouterParams p) {
     extern __shared__ uint4 xsm[];  // the block's token rows, [nt][d / 8] of 8 bf16 each
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x * kRouterWarps + warp;
@@ -198,11 +205,14 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(const RouterP
     // Lane l owns runs c = l + 32 i (16 inputs each), walked in increasing c.
     // A batch's loads are all in flight together; the first batch is issued
     // before the token rows are staged, so the two latencies overlap.
-    uint4 q[kRouterBatch];
-    uint32_t sbw[kRouterBatch];
+    // one token: six runs per lane in flight (d = 2816 has 5.5 per lane), few
+    // enough registers to share an SM with an FFN CTA; more tokens: eight
+    constexpr int kB = TB == 1 ? 6 : kRouterBatch;
+    uint4 q[kB];
+    uint32_t sbw[kB];
     auto load_batch = [&](int b0) {
 #pragma unroll
-        for (int i = 0; i < kRouterBatch; ++i) {
+        for (int i = 0; i < kB; ++i) {
             const int c = lane + 32 * (b0 + i);
             if (has_row && c < runs) {
                 q[i] = ld_stream(row + (size_t)c * 16);
@@ -230,10 +240,10 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(const RouterP
         float acc[TB];
 #pragma unroll
         for (int j = 0; j < TB; ++j) acc[j] = 0.0f;
-        for (int b0 = 0; 32 * b0 < runs; b0 += kRouterBatch) {
+        for (int b0 = 0; 32 * b0 < runs; b0 += kB) {
             if (b0 > 0) load_batch(b0);
 #pragma unroll
-            for (int i = 0; i < kRouterBatch; ++i) {
+            for (int i = 0; i < kB; ++i) {
                 const int c = lane + 32 * (b0 + i);
                 if (c >= runs) continue;
                 const float2 f = unpack_sb(sbw[i]);
@@ -284,8 +294,8 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(const RouterP
             topk_warp<8>(p.logits + (size_t)t * p.E, p.E, p.k, lane, p.ids + (size_t)t * p.k,
                          p.gates + (size_t)t * p.k, hid, p.seq);
         else
-            topk_warp<32>(p.logits + (size_t)t * p.E, p.E, p.k, lane, p.ids + (size_t)t * p.k,
-                          p.gates + (size_t)t * p.k, hid, p.seq);
+            topk_warp_large(p.logits + (size_t)t * p.E, p.E, p.k, lane, p.ids + (size_t)t * p.k,
+                            p.gates + (size_t)t * p.k, hid, p.seq);
     }
     __syncthreads();
     if (threadIdx.x == 0) {

@@ -61,33 +61,36 @@ __device__ __forceinline__ float2 unpack_sb(uint32_t w) {
     return __half22float2(h);
 }
 
-// 4-bit codes to floats: code q at nibble position p of a word becomes the
-// float 2^23 + q * 16^p via (word & (15 << 4p)) | 0x4B000000 (exact), and
-// subtracting 2^23 leaves q * 16^p. Nibbles 5..7 are taken from the word
-// shifted right by 12, so the positions used are p = 0,1,2,3,4,2,3,4.
-// (v & mask) | 0x4B000000 as one three-input logic operation.
+// 4-bit codes to floats without a conversion: the word masked to the nibble
+// at position p, read as an fp32 bit pattern, is the subnormal q * 16^p *
+// 2^-149 (exact; nibbles 0..5 lie in the mantissa field). The inputs it
+// multiplies are staged as x * 2^(kStageExp - 4p), so the fused multiply-add
+// forms q * x * 2^(kStageExp - 149) exactly before its one rounding, a normal
+// number for any |q x| above 2^-77; the sums are scaled back by the exact
+// power of two kDotUnscale. Nibbles 5..7 are taken from the word shifted
+// right by 12, so the positions used are p = 0,1,2,3,4,2,3,4.
+constexpr int kStageExp = 100;  // staged |x| may reach 2^27 before overflow
+constexpr float kDotUnscale = 562949953421312.0f;  // 2^(149 - kStageExp) = 2^49
+
 template <uint32_t kMask>
-__device__ __forceinline__ float magic_nibble(uint32_t v) {
-    uint32_t r;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(v), "n"(kMask), "r"(0x4B000000u));
-    return __uint_as_float(r);
+__device__ __forceinline__ float nibble_code(uint32_t v) {
+    return __uint_as_float(v & kMask);
 }
 
 __device__ __forceinline__ void codes8(uint32_t v, float2 (&o)[4]) {
     // v >> 12 as the high word of v * 2^20: an integer multiply-add, which
     // runs beside the logic unit that the eight extractions keep busy
     const uint32_t w = __umulhi(v, 1u << 20);
-    const float2 off = make_float2(-8388608.0f, -8388608.0f);
-    o[0] = __fadd2_rn(make_float2(magic_nibble<0xFu>(v), magic_nibble<0xF0u>(v)), off);
-    o[1] = __fadd2_rn(make_float2(magic_nibble<0xF00u>(v), magic_nibble<0xF000u>(v)), off);
-    o[2] = __fadd2_rn(make_float2(magic_nibble<0xF0000u>(v), magic_nibble<0xF00u>(w)), off);
-    o[3] = __fadd2_rn(make_float2(magic_nibble<0xF000u>(w), magic_nibble<0xF0000u>(w)), off);
+    o[0] = make_float2(nibble_code<0xFu>(v), nibble_code<0xF0u>(v));
+    o[1] = make_float2(nibble_code<0xF00u>(v), nibble_code<0xF000u>(v));
+    o[2] = make_float2(nibble_code<0xF0000u>(v), nibble_code<0xF00u>(w));
+    o[3] = make_float2(nibble_code<0xF000u>(w), nibble_code<0xF0000u>(w));
 }
 
-// 16^-p for staged slot s of a run of 8 (p = 0,1,2,3,4,2,3,4), as the power of two 2^(-4p).
+// The staging factor 2^(kStageExp - 4p) for slot s of a run of 8 (p = 0,1,2,3,4,2,3,4).
 __device__ __forceinline__ float pos_scale(int s) {
     const int p = s < 5 ? s : s - 3;
-    return __int_as_float((127 - 4 * p) << 23);
+    return __int_as_float((127 + kStageExp - 4 * p) << 23);
 }
 
 __device__ __forceinline__ float act_fn(float z, int act) {
@@ -166,7 +169,7 @@ __device__ __forceinline__ void words_dot(const uint4 (&c)[M][C], const float* x
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
             const float2 s = __fadd2_rn(acc[m][j][0], acc[m][j][1]);
-            out[m][j] = s.x + s.y;
+            out[m][j] = (s.x + s.y) * kDotUnscale;
         }
 }
 
@@ -194,7 +197,7 @@ __device__ __forceinline__ void chunk_dot_reg(const uint4 c, const float (&h)[NT
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
         const float2 s = __fadd2_rn(acc[j][0], acc[j][1]);
-        out[j] = s.x + s.y;
+        out[j] = (s.x + s.y) * kDotUnscale;
     }
 }
 
