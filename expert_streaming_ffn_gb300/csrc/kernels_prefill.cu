@@ -61,13 +61,12 @@ constexpr int kRawBytes = 4 * kUnit * kRecord;  // 4 row tiles x kUnit records
 // nI issuers in turn (nI = 4 for up to 64 token rows, else 2), each issuer
 // accumulating into its own 256/nI columns of the buffer; the epilogue sums them.
 constexpr int kTmemCols = 512;
-// With fewer A stages than issuers, runs of jobs whose K-block count is not a
-// multiple of the issuer count stalled until the bounded waits expired (seen
-// with 4 issuers over 3 stages and 11 K-blocks per job); keep them at least equal.
-static_assert(kStages >= kIssuers, "the A ring needs at least one stage per MMA issuer");
+// Within a job every round of an A stage has the same issuer (kStages is a
+// multiple of nI); between jobs the issuers hand off (see the MMA issue loop).
+static_assert(kStages % kIssuers == 0 && kStages % 2 == 0, "an A stage keeps its issuer within a job");
 static_assert(kStages % kDqGroups == 0, "each dequantising group owns whole A stages");
 // shared memory: A ring, B ring, raw ring, barriers, TMEM address; +1 KB to align
-constexpr int kSmemBytes = 1024 + kStages * kABytes + kSlotsB * kBBytes + kRawStages * kRawBytes + 256;
+constexpr int kSmemBytes = 1024 + kStages * kABytes + kSlotsB * kBBytes + kRawStages * kRawBytes + 320;
 
 // Shared-memory matrix descriptor of a K-major operand tile whose rows are 128
 // bytes apart with the 128-byte swizzle (8-row atoms of 1024 bytes).
@@ -188,7 +187,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* acc_full = a_empty + kStages;       // [2] accumulator complete
     uint64_t* acc_empty = acc_full + 2;           // [2] accumulator read out
     uint64_t* drain = acc_empty + 2;              // [1] every MMA of the CTA done
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* handoff = drain + 1;                // [1] every issuer done with a job's A stages
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(handoff + 1);
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -212,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(acc_empty + i, 4);
         }
         ptx::mbar_init(drain, kIssuers);
+        ptx::mbar_init(handoff, kIssuers);
         abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -230,7 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // diagnostics: the first kPfFailRecords expired waits of the launch, as
     // (block << 48 | warp << 40 | what << 32 | job << 16 | K-block), what =
-    // 1 raw_empty, 2 b_empty, 3 acc_empty, 4 b_full, 5 a_full, 6 acc_full, 7 raw_full, 8 a_empty
+    // 1 raw_empty, 2 b_empty, 3 acc_empty, 4 b_full, 5 a_full, 6 acc_full, 7 raw_full, 8 a_empty,
+    // 9 handoff
     auto record = [&](int what, int job, int kb) {
         if (!a.trace) return;
         unsigned long long* rec = a.trace + kPfTraceKb * kPfTracePoints;
@@ -448,6 +450,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mma_commit(acc_full + buf);
                 } else if (!*abortp) {
                     fail(128u);
+                }
+                // Hand-off: every issuer has taken its last A stage of this job
+                // before any waits on a stage of the next. K-block kb goes to
+                // issuer kb % nI, so when a job's K-block count is not a multiple
+                // of nI a stage changes owner between jobs; a new owner that ran
+                // ahead would test the stage's phase parity two phases early and
+                // pass it (an mbarrier parity tells only adjacent phases apart).
+                ptx::mbar_arrive(handoff);
+                if (!ptx::mbar_wait_sleep(handoff, njob & 1, abortp)) {
+                    record(9, j, nkb);
+                    if (!*abortp) fail(128u);
                 }
             }
             // every MMA issued by this thread has completed once this arrives

@@ -170,6 +170,28 @@ def test_prefill_chunk_2816(ctx):
         r.close()
 
 
+def test_prefill_prompt_repeated_all_resident(ctx):
+    """A 1024-token prompt (8 chunks of 128) through a layer with a slot per
+    expert, six times: the first pass copies every expert in, the rest run on
+    resident weights. The down GEMM's jobs have 11 K-blocks, so the MMA issuers'
+    A stages change owner between jobs; every pass must finish without an
+    expired wait and give the same bits (the arithmetic order is fixed)."""
+    s = synth.SHAPES_2816
+    r = Rig(ctx, s, 6, s.n_experts)
+    try:
+        xb = synth.tokens(s, 6, 0, 1024, True)
+        first, y0 = r.forward(xb, None, y_tokens=[0, 517, 1023])
+        x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+        for rep in range(5):
+            y = moe.moe_forward(r.h, x)
+            torch.cuda.synchronize()
+            assert torch.equal(y, y0), f"pass {rep + 1} differs from the first"
+        st = moe.moe_layer_stats(r.h)
+        assert st["misses"] == len(np.unique(first))
+    finally:
+        r.close()
+
+
 def test_route_call_matches_oracle(ctx):
     s = synth.SHAPES_2816
     r = Rig(ctx, s, 9, 16)
