@@ -263,6 +263,9 @@ struct moe_layer {
     // table (pinned host copy and its device twin)
     __half* d_x16 = nullptr;
     __half* d_h16 = nullptr;
+    // prefill: K-split partial sums (the shared expert's tiles)
+    float* d_part = nullptr;
+    size_t part_floats = 0;
     uint8_t* d_pf = nullptr;
     uint8_t* h_pf = nullptr;
     size_t pf_bytes = 0;
@@ -301,6 +304,9 @@ void free_scratch(moe_layer* L) {
     cudaFree(L->d_o);
     cudaFree(L->d_x16);
     cudaFree(L->d_h16);
+    cudaFree(L->d_part);
+    L->d_part = nullptr;
+    L->part_floats = 0;
     cudaFree(L->d_pf);
     cudaFreeHost(L->h_pf);
     L->d_x16 = L->d_h16 = nullptr;
@@ -339,6 +345,8 @@ moe_status ensure_scratch(moe_layer* L, int T) {
              cudaMalloc(&L->d_h16, sizeof(__half) * ((size_t)T * s.d_ff_shared + pairs * s.d_ff)) == cudaSuccess &&
              cudaMalloc(&L->d_pf, L->pf_bytes) == cudaSuccess &&
              cudaHostAlloc(&L->h_pf, L->pf_bytes, cudaHostAllocDefault) == cudaSuccess;
+        L->part_floats = pf_part_floats(s.d_model, s.d_ff_shared);
+        if (ok && L->part_floats) ok = cudaMalloc(&L->d_part, sizeof(float) * L->part_floats) == cudaSuccess;
     }
     if (!ok) {
         cudaGetLastError();
@@ -805,6 +813,8 @@ moe_status run_experts_prefill(moe_layer* L, const uint16_t* x, int T, float* y,
     a.ready = L->d_ready;
     a.epoch = L->epoch;
     a.err = C->err_dev;
+    a.part = L->d_part;
+    a.part_cap = L->d_part ? L->part_floats : 0;
     const int rows[2] = {T, P};
     WaitRec wr{};
     if (copies_done) {
@@ -823,11 +833,15 @@ moe_status run_experts_prefill(moe_layer* L, const uint16_t* x, int T, float* y,
     const double by_dn = bytes - by_gu;
     {
         Prof p(C, s, K_GEMM_GU, by_gu, fl_gu);
-        CUDA_TRY(launch_pf_gemm(a, 1, xs, xg, rows, s));
+        int n_launch = 1;
+        CUDA_TRY(launch_pf_gemm(a, 1, xs, xg, rows, s, &n_launch));
+        C->launches += n_launch - 1;  // the K-split epilogue launch
     }
     {
         Prof p(C, s, K_GEMM_DN, by_dn, fl_dn);
-        CUDA_TRY(launch_pf_gemm(a, 2, a.h[0], a.h[1], rows, s));
+        int n_launch = 1;
+        CUDA_TRY(launch_pf_gemm(a, 2, a.h[0], a.h[1], rows, s, &n_launch));
+        C->launches += n_launch - 1;  // the K-split epilogue launch
     }
     {
         Prof p(C, s, K_COMBINE, 4.0 * ((double)P * d + 2.0 * T * d), 2.0 * P * d);

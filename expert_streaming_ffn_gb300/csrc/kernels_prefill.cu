@@ -114,14 +114,17 @@ __device__ __forceinline__ float act_fn(float z, int act) {
     return 0.5f * z * (1.0f + tanhf(0.7978845608028654f * (z + 0.044715f * z * z * z)));
 }
 
+// A job: one M tile of one item over K-blocks kb0 .. kb0 + nkb - 1, part
+// `part` of the tile's ks[fam] parts.
 struct Job {
-    int item, fam, tile;
+    int item, fam, tile, part, kb0, nkb;
 };
 
 struct Plan {
     int phase;
     int tiles[2];    // M tiles per item
     int kblocks[2];  // K blocks of 64
+    int ks[2];       // K parts of a tile
     int n_jobs, jobs0;
 };
 
@@ -132,23 +135,35 @@ __device__ __forceinline__ Plan make_plan(const PfArgs& a, int phase) {
         p.tiles[f] = phase == 1 ? a.inter[f] / 64 : a.d / kTileM;
         p.kblocks[f] = phase == 1 ? a.d / 64 : a.inter[f] / 64;
     }
-    p.jobs0 = a.n_fam0 * p.tiles[0];
-    p.n_jobs = p.jobs0 + (a.n_items - a.n_fam0) * p.tiles[1];
+    for (int f = 0; f < 2; ++f) p.ks[f] = a.ks[f] > 1 ? a.ks[f] : 1;
+    p.jobs0 = a.n_fam0 * p.tiles[0] * p.ks[0];
+    p.n_jobs = p.jobs0 + (a.n_items - a.n_fam0) * p.tiles[1] * p.ks[1];
     return p;
 }
 
+// A tile's parts are consecutive jobs, so they run at once on neighbouring
+// CTAs.
 __device__ __forceinline__ Job decode_job(const Plan& p, const PfArgs& a, int j) {
     Job b;
-    if (j < p.jobs0) {
-        b.fam = 0;
-        b.item = j / p.tiles[0];
-        b.tile = j - b.item * p.tiles[0];
+    // (selects, not indexing: an indexed Plan array would live in local memory)
+    b.fam = j < p.jobs0 ? 0 : 1;
+    if (b.fam) j -= p.jobs0;
+    const int ks = b.fam ? p.ks[1] : p.ks[0];
+    const int per_item = (b.fam ? p.tiles[1] : p.tiles[0]) * ks;
+    const int i = j / per_item;
+    const int r = j - i * per_item;
+    b.item = b.fam ? a.n_fam0 + i : i;
+    const int K = b.fam ? p.kblocks[1] : p.kblocks[0];
+    if (ks == 1) {
+        b.tile = r;
+        b.part = 0;
+        b.kb0 = 0;
+        b.nkb = K;
     } else {
-        j -= p.jobs0;
-        b.fam = 1;
-        const int i = j / p.tiles[1];
-        b.tile = j - i * p.tiles[1];
-        b.item = a.n_fam0 + i;
+        b.tile = r / ks;
+        b.part = r - b.tile * ks;
+        b.kb0 = b.part * K / ks;
+        b.nkb = (b.part + 1) * K / ks - b.kb0;
     }
     return b;
 }
@@ -264,8 +279,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             asm volatile("fence.proxy.async.global;" ::: "memory");
             const int I = a.inter[b.fam];
             const size_t mat = qmat_bytes(I, a.d);
-            const int nkb = P.kblocks[b.fam];
+            const int nkb = b.nkb;
             for (int kb0 = 0; kb0 < nkb; kb0 += kUnit) {
+                const int kbA = b.kb0 + kb0;  // the unit's first K-block within the matrix
                 const int nu = min(kUnit, nkb - kb0);
                 bool w = true;
                 if (lane == 0) {
@@ -293,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int G = a.d / 64;
                         const unsigned char* m = it.w + (size_t)(lane >> 1) * mat;
                         const int rt = 2 * b.tile + (lane & 1);
-                        ptx::bulk_g2s(raw + lane * kUnit * kRecord, m + ((size_t)rt * G + kb0) * kRecord,
+                        ptx::bulk_g2s(raw + lane * kUnit * kRecord, m + ((size_t)rt * G + kbA) * kRecord,
                                       nu * kRecord, raw_full + r);
                     }
                 } else {
@@ -304,11 +320,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int RT = a.d / 32;
                     const unsigned char* dn = it.w + 2 * mat;
                     if (lane < 2 * nu)
-                        ptx::bulk_g2s(raw + lane * 2048, dn + ((size_t)(2 * kb0 + lane) * RT + 4 * b.tile) * 512, 2048,
+                        ptx::bulk_g2s(raw + lane * 2048, dn + ((size_t)(2 * kbA + lane) * RT + 4 * b.tile) * 512, 2048,
                                       raw_full + r);
                     else if (lane >= 16 && lane - 16 < nu)
                         ptx::bulk_g2s(raw + kUnit * 4096 + (lane - 16) * 512,
-                                      dn + down_codes_bytes(a.d, I) + ((size_t)(kb0 + lane - 16) * RT + 4 * b.tile) * 128,
+                                      dn + down_codes_bytes(a.d, I) + ((size_t)(kbA + lane - 16) * RT + 4 * b.tile) * 128,
                                       512, raw_full + r);
                 }
                 __syncwarp();
@@ -345,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const PfItem it = a.items[b.item];
                 const int nb = pad16(it.np);
                 const int kpb = kPfMaxN / nb;  // K-blocks per slot
-                const int nkb = P.kblocks[b.fam];
+                const int nkb = b.nkb;
                 for (int kb0 = 0; kb0 < nkb; kb0 += kpb) {
                     const int nk = min(kpb, nkb - kb0);
                     if (!ptx::mbar_wait_sleep(b_empty + s, ph ^ 1, abortp)) {
@@ -358,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mbar_arrive_expect_tx(b_full + s, (uint32_t)(nk * nb * 128));
                     for (int kk = 0; kk < nk; ++kk) {
                         unsigned char* dst = bt + kk * nb * 128;
-                        const int x = (kb0 + kk) * 64;
+                        const int x = (b.kb0 + kb0 + kk) * 64;
                         if (b.fam == 0) {
                             ptx::tma_load_2d(dst, &map0, x, 0, b_full + s);  // one box of all the rows
                         } else {
@@ -396,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Job b = decode_job(P, a, j);
                 const int nb = pad16(a.items[b.item].np);
                 const int kpb = kPfMaxN / nb;
-                const int nkb = P.kblocks[b.fam];
+                const int nkb = b.nkb;
                 const int nI = nb <= 64 ? 4 : 2;
                 const int buf = njob & 1;
                 const uint32_t idesc = f16_idesc(kTileM, nb);
@@ -470,6 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= kWarpEpi && warp < kWarpEpi + 4) {
         // ---------------- epilogue ----------------
         const int q = warp - kWarpEpi;  // TMEM lanes 32q .. 32q + 31
+        const int row = 32 * q + lane;  // this thread's row of the 128-row tile
         int njob = 0;
         for (int j = blockIdx.x; j < P.n_jobs; j += gridDim.x, ++njob) {
             const Job b = decode_job(P, a, j);
@@ -484,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after();
             const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + buf * 256;
             const int nI = nb <= 64 ? 4 : 2;
-            const int used = min(nI, P.kblocks[b.fam]);  // issuers that accumulated anything
+            const int used = min(nI, b.nkb);  // issuers that accumulated anything
             // v = the sum of the issuers' accumulators for 16 columns from c, in issuer order
             auto load_sum = [&](int c, uint32_t (&v)[16]) {
                 ptx::tmem_ld16(taddr + c, v);
@@ -497,7 +514,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ptx::tmem_ld_wait();
             };
-            if (phase == 1) {
+            // K split: this part's sums go to the part buffer
+            // ([split tile][part][column][row], so a warp's stores are whole
+            // lines) and pf_reduce_kernel adds the parts and writes the tile
+            const int ks = b.fam ? P.ks[1] : P.ks[0];
+            if (ks > 1) {
+                const size_t fam_tile =
+                    (size_t)(b.item - (b.fam ? a.n_fam0 : 0)) * (b.fam ? P.tiles[1] : P.tiles[0]) + b.tile;
+                const size_t n0 = P.ks[0] > 1 ? (size_t)a.n_fam0 * P.tiles[0] : 0;  // family 0's split tiles
+                const size_t part = (b.fam ? n0 * P.ks[0] : 0) + fam_tile * ks + b.part;
+                float* mine = a.part + part * kPfMaxN * kTileM + row;
+                for (int c = 0; c < nb; c += 16) {
+                    uint32_t v[16];
+                    load_sum(c, v);
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) mine[(size_t)(c + m) * kTileM] = __uint_as_float(v[m]);
+                }
+            } else if (phase == 1) {
                 const int I = a.inter[b.fam];
                 const int irow = 64 * b.tile + 16 * q + (lane >> 1);
                 __half* hb = a.h[b.fam];
@@ -517,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             } else {
-                const int n = kTileM * b.tile + 32 * q + lane;
+                const int n = kTileM * b.tile + row;
                 for (int c = 0; c < nb; c += 16) {
                     uint32_t v[16];
                     load_sum(c, v);
@@ -525,8 +558,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int m = 0; m < 16; ++m) {
                         const int col = c + m;
                         if (col >= it.np) break;
-                        const size_t row = b.fam == 0 ? (size_t)col : (size_t)a.pair[it.pb + col];
-                        a.out[b.fam][row * a.d + n] = __uint_as_float(v[m]);
+                        const size_t orow = b.fam == 0 ? (size_t)col : (size_t)a.pair[it.pb + col];
+                        a.out[b.fam][orow * a.d + n] = __uint_as_float(v[m]);
                     }
                 }
             }
@@ -567,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool wtracer = a.trace && blockIdx.x == 0 && lane == 0;
         for (int j = blockIdx.x, njob = 0; j < P.n_jobs; j += gridDim.x, ++njob) {
             const Job b = decode_job(P, a, j);
-            const int nkb = P.kblocks[b.fam];
+            const int nkb = b.nkb;
             for (int kb0 = 0; kb0 < nkb; kb0 += kUnit) {
                 const int nu = min(kUnit, nkb - kb0);
                 const bool have = ptx::mbar_wait_sleep(raw_full + r, rph, abortp);
@@ -638,6 +671,72 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// The K-split tiles' epilogue: block (t, y) takes split tile t (family 0's
+// first) and columns 16y .. 16y + 15, thread r row r of the tile; it adds the
+// tile's parts in part order and writes h (gate/up) or the outputs (down)
+// exactly as the GEMM's epilogue does for a whole tile.
+__global__ void __launch_bounds__(kTileM) pf_reduce_kernel(const __grid_constant__ PfArgs a, const int phase) {
+    const Plan P = make_plan(a, phase);
+    const int row = threadIdx.x, lane = row & 31, q = row >> 5;
+    const int n0 = P.ks[0] > 1 ? a.n_fam0 * P.tiles[0] : 0;
+    int t = blockIdx.x, fam, item, tile, ks;
+    size_t part0;
+    if (t < n0) {
+        fam = 0;
+        item = t / P.tiles[0];
+        tile = t - item * P.tiles[0];
+        ks = P.ks[0];
+        part0 = (size_t)t * ks;
+    } else {
+        t -= n0;
+        fam = 1;
+        const int i = t / P.tiles[1];
+        tile = t - i * P.tiles[1];
+        item = a.n_fam0 + i;
+        ks = P.ks[1];
+        part0 = (size_t)n0 * P.ks[0] + (size_t)t * ks;
+    }
+    const PfItem it = a.items[item];
+    const int c = blockIdx.y * 16;
+    if (c >= it.np) return;  // the whole block
+    const size_t stride = (size_t)kPfMaxN * kTileM;
+    const float* src = a.part + part0 * stride + (size_t)c * kTileM + row;
+    float v[16];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) v[m] = src[(size_t)m * kTileM];
+    for (int pp = 1; pp < ks; ++pp) {
+        const float* sp = src + pp * stride;
+        float w[16];
+#pragma unroll
+        for (int m = 0; m < 16; ++m) w[m] = sp[(size_t)m * kTileM];
+#pragma unroll
+        for (int m = 0; m < 16; ++m) v[m] += w[m];
+    }
+    if (phase == 1) {
+        const int I = a.inter[fam];
+        const int irow = 64 * tile + 16 * q + (lane >> 1);
+        __half* hb = a.h[fam];
+        const bool odd = lane & 1;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const float mine = odd ? v[m + 8] : v[m];
+            const float other = __shfl_xor_sync(kFull, odd ? v[m] : v[m + 8], 1);
+            const float g = odd ? other : mine, u = odd ? mine : other;
+            const int col = c + m + (odd ? 8 : 0);
+            if (col < it.np) hb[(size_t)(it.pb + col) * I + irow] = __float2half_rn(act_fn(g, a.act) * u);
+        }
+    } else {
+        const int n = kTileM * tile + row;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const int col = c + m;
+            if (col >= it.np) break;
+            const size_t orow = fam == 0 ? (size_t)col : (size_t)a.pair[it.pb + col];
+            a.out[fam][orow * a.d + n] = v[m];
+        }
+    }
+}
+
 __global__ void pf_gather_kernel(const uint16_t* __restrict__ x, int T, int d, const int32_t* __restrict__ pair,
                                  int P, int k, __half* __restrict__ xs, __half* __restrict__ xg) {
     const int per_row = d / 8;
@@ -704,7 +803,26 @@ int num_sms() {
     return n;
 }
 
+// K parts of a tile of `kblocks` K-blocks when a launch has `tiles` tiles in
+// all: enough to give every SM a job, at most 8 and at least 4 K-blocks each.
+// A launch with at least half as many tiles as SMs is not split (its tiles
+// already fill the GPU, and the split costs a second launch).
+int pf_split(int tiles, int kblocks) {
+    if (2 * tiles >= num_sms()) return 1;
+    int s = num_sms() / std::max(tiles, 1);
+    s = std::min(s, 8);
+    s = std::min(s, kblocks / 4);
+    return std::max(s, 1);
+}
+
 }  // namespace
+
+// pf_split keeps a launch's tiles x parts within the SM count.
+size_t pf_part_floats(int d, int inter0) {
+    (void)d;
+    (void)inter0;
+    return (size_t)num_sms() * kTileM * kPfMaxN;
+}
 
 cudaError_t launch_pf_gather(const uint16_t* x, int T, int d, const int32_t* pair, int P, int k, __half* xs,
                              __half* xg, cudaStream_t s) {
@@ -715,7 +833,7 @@ cudaError_t launch_pf_gather(const uint16_t* x, int T, int d, const int32_t* pai
 }
 
 cudaError_t launch_pf_gemm(const PfArgs& a, int phase, const void* b0, const void* b1, const int rows[2],
-                           cudaStream_t s) {
+                           cudaStream_t s, int* launched) {
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(pf_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -735,9 +853,32 @@ cudaError_t launch_pf_gemm(const PfArgs& a, int phase, const void* b0, const voi
     if (e != cudaSuccess) return e;
     const int tiles0 = phase == 1 ? a.inter[0] / 64 : a.d / kTileM;
     const int tiles1 = phase == 1 ? a.inter[1] / 64 : a.d / kTileM;
-    const int jobs = a.n_fam0 * tiles0 + (a.n_items - a.n_fam0) * tiles1;
+    // K splits when the launch's tiles are too few to fill the GPU (the shared
+    // expert alone has 44 or 22); a family whose parts would not fit the
+    // buffer is not split
+    PfArgs b = a;
+    const int n_t[2] = {a.n_fam0 * tiles0, (a.n_items - a.n_fam0) * tiles1};
+    const int kb[2] = {phase == 1 ? a.d / 64 : a.inter[0] / 64, phase == 1 ? a.d / 64 : a.inter[1] / 64};
+    size_t parts = 0;
+    int split_tiles = 0;
+    for (int f = 0; f < 2; ++f) {
+        b.ks[f] = a.part ? pf_split(n_t[0] + n_t[1], kb[f]) : 1;
+        if (b.ks[f] > 1 && (parts + (size_t)n_t[f] * b.ks[f]) * kTileM * kPfMaxN > a.part_cap) b.ks[f] = 1;
+        if (b.ks[f] > 1) {
+            parts += (size_t)n_t[f] * b.ks[f];
+            split_tiles += n_t[f];
+        }
+    }
+    const int jobs = n_t[0] * b.ks[0] + n_t[1] * b.ks[1];
     const int grid = std::min(jobs, num_sms());
-    pf_gemm_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, phase, m0, m1);
+    pf_gemm_kernel<<<grid, kThreads, kSmemBytes, s>>>(b, phase, m0, m1);
+    if (launched) *launched = 1;
+    if (split_tiles > 0) {
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        pf_reduce_kernel<<<dim3(split_tiles, kPfMaxN / 16), kTileM, 0, s>>>(b, phase);
+        if (launched) *launched = 2;
+    }
     return cudaGetLastError();
 }
 

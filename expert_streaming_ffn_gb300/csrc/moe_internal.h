@@ -258,6 +258,16 @@ struct PfArgs {
     const uint32_t* ready;
     uint32_t epoch;
     unsigned* err;
+    // K split of the tiles of a launch that has too few to fill the GPU (the
+    // shared expert's 128-row tiles alone leave most SMs idle): each of a
+    // tile's ks[fam] parts covers a slice of K and writes its fp32 sums to
+    // `part` ([split tile][part][kPfMaxN columns][128 rows], family 0's split
+    // tiles first); a second kernel adds them in part order and runs the
+    // epilogue. part_cap is the buffer's size in floats; with a null buffer no
+    // tile is split. ks is set by launch_pf_gemm.
+    float* part;
+    size_t part_cap;
+    int ks[2];
     // optional diagnostics: block 0 records %globaltimer for the first
     // kPfTraceKb K-blocks of its first job at kPfTracePoints moments (raw
     // records landed, A stage free, A stage written, MMA inputs ready, MMAs
@@ -277,7 +287,13 @@ cudaError_t launch_pf_gather(const uint16_t* x, int T, int d, const int32_t* pai
 // phase 1: gate/up (B rows from xs / xg, K = d); phase 2: down (B rows from
 // h[0] / h[1], K = inter). `rows[f]` is the number of rows of family f's B
 // matrix (T for family 0, P for family 1).
+// Floats of K-split partial sums a layer with these shapes needs for its
+// prefill GEMMs on the current device.
+size_t pf_part_floats(int d, int inter0);
+
+// One phase of the grouped GEMM: the GEMM launch, and the K-split epilogue
+// launch when tiles are split; *launched (if given) gets the launch count.
 cudaError_t launch_pf_gemm(const PfArgs& a, int phase, const void* b0, const void* b1, const int rows[2],
-                           cudaStream_t s);
+                           cudaStream_t s, int* launched = nullptr);
 
 }  // namespace moe
