@@ -7,8 +7,9 @@
 //        fetch of an expert's weights serves every row of the chunk routed to it.
 //
 // One launch per phase. A job is one 128-row tile of one item's weight matrix
-// over all of K, against all of the item's token rows (N <= 128, padded to a
-// multiple of 16):
+// over all of K (or, when a launch has too few tiles to fill the GPU, over a
+// slice of K, the slices' sums added by pf_reduce_kernel), against all of the
+// item's token rows (N <= 128, padded to a multiple of 16):
 //   phase 1 (gate/up): the tile interleaves 64 gate rows and the same 64 up
 //     rows (in each 32-row quarter, even rows gate and odd rows up), so the
 //     epilogue forms h = act(gate) * up from neighbouring lanes;
