@@ -192,6 +192,26 @@ def test_prefill_prompt_repeated_all_resident(ctx):
         r.close()
 
 
+def test_prefill_split_k_small_launch(ctx):
+    """A layer of d = 2816 with one 64-wide routed expert and the 2816-wide
+    shared expert: its prefill launches have too few 128-row tiles to fill the
+    GPU, so each tile's K range is split over several CTAs and the parts are
+    added by a second kernel. Outputs match the oracle, and a repeat gives the
+    same bits."""
+    s0 = synth.SHAPES_2816
+    s = synth.Shapes(s0.d_model, 1, 1, 64, s0.d_ff_shared, s0.act)
+    r = Rig(ctx, s, 2, 1)
+    try:
+        xb = synth.tokens(s, 2, 0, 128, True)
+        _, y0 = r.forward(xb, None, y_tokens=[0, 1, 77, 127])
+        x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+        y = moe.moe_forward(r.h, x)
+        torch.cuda.synchronize()
+        assert torch.equal(y, y0)
+    finally:
+        r.close()
+
+
 def test_route_call_matches_oracle(ctx):
     s = synth.SHAPES_2816
     r = Rig(ctx, s, 9, 16)
