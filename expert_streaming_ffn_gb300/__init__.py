@@ -73,6 +73,7 @@ SIGNATURES = [
     ("moe_route_noalloc", _i32, [_vp, _vp, _i32, _vp, _vp, _vp, _vp]),
     ("moe_cache_step", _i32, [_vp, _vp, _i32, _vp, _vp, _vp, _vp]),
     ("moe_forward", _i32, [_vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp]),
+    ("moe_forward_prompt", _i32, [_vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp]),
     ("moe_cache_reset", _i32, [_vp]),
     ("moe_layer_stats", _i32, [_vp, _P(moe_stats)]),
     ("moe_layer_reset_stats", _i32, [_vp]),
@@ -242,6 +243,19 @@ def moe_forward(layer: int, x, zbias=None, y=None, ids_out=None, gates_out=None,
         y = torch.empty((T, d), dtype=torch.float32, device=x.device)
     _check(load().moe_forward(layer, _dptr(x), T, _dptr(zbias), _dptr(y), _dptr(ids_out), _dptr(gates_out),
                               _stream(stream)), "moe_forward")
+    return y
+
+
+def moe_forward_prompt(layer: int, x, zbias=None, y=None, ids_out=None, gates_out=None, stream=None):
+    """The whole prompt x (CUDA bf16 [T][d]) in one layer-major call: one
+    routing, one cache step, grouped GEMMs over all of it. Returns y."""
+    import torch
+
+    T, d = x.shape
+    if y is None:
+        y = torch.empty((T, d), dtype=torch.float32, device=x.device)
+    _check(load().moe_forward_prompt(layer, _dptr(x), T, _dptr(zbias), _dptr(y), _dptr(ids_out), _dptr(gates_out),
+                                     _stream(stream)), "moe_forward_prompt")
     return y
 
 

@@ -296,6 +296,13 @@ moe_status check_shapes(const moe_shapes* s) {
     return MOE_OK;
 }
 
+// Items of one prefill call of T tokens: the shared expert per block of
+// kPfMaxN tokens, and each routed expert's pairs in pieces of at most kPfMaxN.
+size_t pf_max_items(const moe_shapes& s, int T) {
+    const size_t pairs = (size_t)T * s.top_k;
+    return (T + kPfMaxN - 1) / kPfMaxN + std::min<size_t>(s.n_experts, pairs) + pairs / kPfMaxN;
+}
+
 void free_scratch(moe_layer* L) {
     cudaFree(L->d_logits);
     cudaFree(L->d_rcount);
@@ -339,7 +346,7 @@ moe_status ensure_scratch(moe_layer* L, int T) {
               cudaHostAlloc(&L->h_pub, sizeof(unsigned long long) * pairs, cudaHostAllocMapped) == cudaSuccess &&
               cudaHostGetDevicePointer(&L->h_pub_dev, L->h_pub, 0) == cudaSuccess;
     if (ok && T > kDecodeMaxT) {
-        const size_t items = 1 + std::min<size_t>(s.n_experts, pairs);
+        const size_t items = pf_max_items(s, T);
         L->pf_bytes = items * sizeof(PfItem) + pairs * sizeof(int32_t);
         ok = cudaMalloc(&L->d_x16, sizeof(__half) * ((size_t)T + pairs) * s.d_model) == cudaSuccess &&
              cudaMalloc(&L->d_h16, sizeof(__half) * ((size_t)T * s.d_ff_shared + pairs * s.d_ff)) == cudaSuccess &&
@@ -751,44 +758,49 @@ moe_status run_experts(moe_layer* L, const uint16_t* x, int T, float* y, const s
     return st;
 }
 
-// The experts of a prefill chunk (T > kDecodeMaxT) as grouped GEMMs on the
-// tensor cores: every token row of an expert in one item (the shared expert
-// over all T tokens; each routed expert over its pairs, sorted by expert),
-// then gate/up, down into y (shared) and o (routed), and the combine
-// y += sum_r g_r o_r. Hits come before misses in the job order, so the
-// resident experts run while the copies land.
+// The experts of a prefill call (T > kDecodeMaxT: a 128-token chunk, or a
+// whole prompt run layer-major) as grouped GEMMs on the tensor cores. An item
+// is up to kPfMaxN token rows of one expert: the shared expert over each block
+// of kPfMaxN tokens, each routed expert over its pairs (sorted by expert) in
+// pieces of at most kPfMaxN. Then gate/up, down into y (shared) and o
+// (routed), and the combine y += sum_r g_r o_r. Hits come before misses in
+// the job order, so the resident experts run while the copies land.
 moe_status run_experts_prefill(moe_layer* L, const uint16_t* x, int T, float* y,
                                const std::vector<MissFlags>& ready_of_miss, cudaEvent_t copies_done, cudaStream_t s) {
     moe_ctx* C = L->ctx;
     const moe_shapes& sh = L->sh;
     const int k = sh.top_k, d = sh.d_model, P = T * k;
-    if (T > kPfMaxN || !L->d_pf) return set_error(MOE_EINVAL, "prefill chunk of %d tokens (at most %d)", T, kPfMaxN);
+    if (T > L->cap_T || !L->d_pf) return set_error(MOE_EINVAL, "prefill call of %d tokens (scratch for %d)", T, L->cap_T);
     L->offsets.resize(sh.n_experts + 1);
     L->perm.resize(P);
     group_pairs(L->h_ids.data(), P, sh.n_experts, L->offsets.data(), L->perm.data());
     PfItem* items = reinterpret_cast<PfItem*>(L->h_pf);
+    const size_t max_items = pf_max_items(sh, T);
     int n = 0;
-    items[n++] = PfItem{L->d_shared, 0, T, -1, -1};
+    const int n_shared = (T + kPfMaxN - 1) / kPfMaxN;
+    for (int t0 = 0; t0 < T; t0 += kPfMaxN) items[n++] = PfItem{L->d_shared, t0, std::min(kPfMaxN, T - t0), -1, -1};
     std::vector<PfItem> miss;
     int nb = 0;
     size_t mi = 0;
-    double bytes = (double)L->shared_bytes;
+    double bytes = (double)L->shared_bytes * n_shared;  // the shared weights, read once per token block
     for (int e : L->step.distinct) {
         while (mi < L->step.miss_experts.size() && L->step.miss_experts[mi] < e) ++mi;
         const bool is_miss = mi < L->step.miss_experts.size() && L->step.miss_experts[mi] == e;
         const int slot = is_miss ? L->step.miss_slots[mi] : L->cache.slot_of(e);
         const uint8_t* w = slot >= 0 ? L->d_slots + (size_t)slot * L->ebytes : C->staging + (size_t)(nb++) * L->ebytes;
         const MissFlags f = is_miss ? ready_of_miss[mi] : MissFlags{};
-        const PfItem it{w, L->offsets[e], L->offsets[e + 1] - L->offsets[e], f.gu, f.dn};
-        if (it.np > kPfMaxN) return set_error(MOE_EINVAL, "expert %d has %d rows in one chunk", e, it.np);
-        if (is_miss)
-            miss.push_back(it);
-        else
-            items[n++] = it;
-        bytes += (double)L->ebytes;
+        for (int p0 = L->offsets[e]; p0 < L->offsets[e + 1]; p0 += kPfMaxN) {
+            const PfItem it{w, p0, std::min(kPfMaxN, L->offsets[e + 1] - p0), f.gu, f.dn};
+            if ((size_t)n + miss.size() >= max_items) return set_error(MOE_ESTATE, "prefill item list overflow");
+            if (is_miss)
+                miss.push_back(it);
+            else
+                items[n++] = it;
+            bytes += (double)L->ebytes;  // each piece reads the expert's weights
+        }
     }
     for (const PfItem& it : miss) items[n++] = it;
-    const size_t item_bytes = sizeof(PfItem) * (1 + std::min<size_t>(sh.n_experts, P));
+    const size_t item_bytes = sizeof(PfItem) * max_items;
     int32_t* pair_h = reinterpret_cast<int32_t*>(L->h_pf + item_bytes);
     std::copy(L->perm.begin(), L->perm.end(), pair_h);
     CUDA_TRY(cudaMemcpyAsync(L->d_pf, L->h_pf, L->pf_bytes, cudaMemcpyHostToDevice, s));
@@ -796,7 +808,7 @@ moe_status run_experts_prefill(moe_layer* L, const uint16_t* x, int T, float* y,
     PfArgs a{};
     a.items = reinterpret_cast<const PfItem*>(L->d_pf);
     a.n_items = n;
-    a.n_fam0 = 1;
+    a.n_fam0 = n_shared;
     a.d = d;
     a.act = sh.act;
     a.T = T;
@@ -879,7 +891,8 @@ double us_since(std::chrono::steady_clock::time_point t) {
     return std::chrono::duration<double, std::micro>(std::chrono::steady_clock::now() - t).count();
 }
 
-// One call of at most kPrefillChunk tokens.
+// One call: at most kPrefillChunk tokens from moe_forward, or a whole
+// layer-major prompt from moe_forward_prompt.
 moe_status forward_chunk(moe_layer* L, const uint16_t* x, int T, const float* zbias, float* y, int32_t* ids_out,
                          float* gates_out, cudaStream_t s) {
     moe_ctx* C = L->ctx;
@@ -1271,6 +1284,16 @@ extern "C" moe_status moe_forward(moe_layer* L, const void* x, int32_t T, const 
         if (st != MOE_OK) return st;
     }
     return MOE_OK;
+}
+
+extern "C" moe_status moe_forward_prompt(moe_layer* L, const void* x, int32_t T, const float* zbias, float* y,
+                                         int32_t* ids_out, float* gates_out, void* stream) {
+    if (!L || !x || !y || T < 1 || T > kPromptMaxT) return set_error(MOE_EINVAL, "moe_forward_prompt: bad arguments");
+    if (!L->loaded) return set_error(MOE_ESTATE, "moe_forward_prompt before moe_layer_set_weights");
+    CUDA_TRY(cudaSetDevice(L->ctx->device));
+    moe_status st = ensure_scratch(L, std::max(T, L->cap_T));
+    if (st != MOE_OK) return st;
+    return forward_chunk(L, static_cast<const uint16_t*>(x), T, zbias, y, ids_out, gates_out, (cudaStream_t)stream);
 }
 
 extern "C" moe_status moe_cache_reset(moe_layer* L) {

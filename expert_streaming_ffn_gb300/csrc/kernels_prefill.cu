@@ -376,11 +376,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int kk = 0; kk < nk; ++kk) {
                         unsigned char* dst = bt + kk * nb * 128;
                         const int x = (b.kb0 + kb0 + kk) * 64;
-                        if (b.fam == 0) {
+                        if (b.fam == 0 && a.n_fam0 == 1) {
                             ptx::tma_load_2d(dst, &map0, x, 0, b_full + s);  // one box of all the rows
                         } else {
+                            // 16-row boxes (family 0 too when it has several
+                            // token blocks: its map then has 16-row boxes)
+                            const CUtensorMap* m = b.fam == 0 ? &map0 : &map1;
                             for (int r0 = 0; r0 < nb; r0 += 16)
-                                ptx::tma_load_2d(dst + r0 * 128, &map1, x, it.pb + r0, b_full + s);
+                                ptx::tma_load_2d(dst + r0 * 128, m, x, it.pb + r0, b_full + s);
                         }
                     }
                     ++issued;
@@ -559,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int m = 0; m < 16; ++m) {
                         const int col = c + m;
                         if (col >= it.np) break;
-                        const size_t orow = b.fam == 0 ? (size_t)col : (size_t)a.pair[it.pb + col];
+                        const size_t orow = b.fam == 0 ? (size_t)(it.pb + col) : (size_t)a.pair[it.pb + col];
                         a.out[b.fam][orow * a.d + n] = __uint_as_float(v[m]);
                     }
                 }
@@ -732,7 +735,7 @@ __global__ void __launch_bounds__(kTileM) pf_reduce_kernel(const __grid_constant
         for (int m = 0; m < 16; ++m) {
             const int col = c + m;
             if (col >= it.np) break;
-            const size_t orow = fam == 0 ? (size_t)col : (size_t)a.pair[it.pb + col];
+            const size_t orow = fam == 0 ? (size_t)(it.pb + col) : (size_t)a.pair[it.pb + col];
             a.out[fam][orow * a.d + n] = v[m];
         }
     }
@@ -846,9 +849,10 @@ cudaError_t launch_pf_gemm(const PfArgs& a, int phase, const void* b0, const voi
         return cudaErrorInvalidValue;
     CUtensorMap m0, m1;
     const int k0 = phase == 1 ? a.d : a.inter[0], k1 = phase == 1 ? a.d : a.inter[1];
-    // family 0 is the shared expert over every token row: one box of all of them
-    if (rows[0] != a.T || a.T < 1 || a.T > kPfMaxN) return cudaErrorInvalidValue;
-    const int box0 = a.T <= 16 ? 16 : (a.T + 15) & ~15;
+    // family 0 is the shared expert over every token row: one item per block
+    // of kPfMaxN tokens (a single one loads all its rows as one box)
+    if (rows[0] != a.T || a.T < 1 || a.n_fam0 != (a.T + kPfMaxN - 1) / kPfMaxN) return cudaErrorInvalidValue;
+    const int box0 = a.n_fam0 > 1 ? 16 : a.T <= 16 ? 16 : (a.T + 15) & ~15;
     cudaError_t e = encode_rows(&m0, b0, rows[0], k0, box0);
     if (e == cudaSuccess) e = encode_rows(&m1, b1, std::max(rows[1], 1), k1, 16);
     if (e != cudaSuccess) return e;

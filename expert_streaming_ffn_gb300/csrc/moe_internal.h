@@ -28,6 +28,7 @@ constexpr int kMaxTopK = 32;
 constexpr int kMaxDModel = 8192;
 constexpr int kDecodeMaxT = 64;     // T above this runs the prefill path
 constexpr int kPrefillChunk = 128;  // tokens per prefill chunk ([P1] §2.5, §8.4)
+constexpr int kPromptMaxT = 4096;   // tokens of one layer-major prompt call
 
 // Records a message for moe_last_error() (thread-local) and returns s.
 moe_status set_error(moe_status s, const char* fmt, ...);

@@ -228,6 +228,24 @@ moe_status moe_cache_step(moe_layer* layer, const int32_t* ids, int32_t n_ids, i
 moe_status moe_forward(moe_layer* layer, const void* x_bf16, int32_t T, const float* zbias, float* y,
                        int32_t* ids_out, float* gates_out, void* stream);
 
+/* The whole layer on a prompt of T tokens run layer-major (a widening of the
+ * prefill path: [P1] §8.4 runs a prompt as chunks so that one fetch of an
+ * expert serves every row of the chunk; here the chunk is the whole prompt):
+ * one routing of all T tokens, one cache step over all T*k pairs (so each
+ * distinct expert is fetched at most once per call, and the cache trajectory
+ * is that of one step, not of one step per 128 tokens), the grouped expert
+ * GEMMs over every token routed to each expert (items of up to 128 token
+ * rows; the shared expert per block of 128 tokens), and the combine. Same
+ * arithmetic as moe_forward's prefill path. T <= 64 runs the decode path, as
+ * moe_forward does.
+ * x: device bf16 [T][d_model], 1 <= T <= 4096; zbias: device f32 [E] or NULL;
+ * y: device f32 [T][d_model]; ids_out / gates_out as for moe_forward.
+ * Blocks the calling thread once until the routing is known on the host.
+ * Errors: MOE_EINVAL (bad arguments, T > 4096), MOE_ENOMEM (scratch for T
+ * tokens), MOE_ESTATE, MOE_ECOPY, MOE_ECUDA. */
+moe_status moe_forward_prompt(moe_layer* layer, const void* x_bf16, int32_t T, const float* zbias, float* y,
+                              int32_t* ids_out, float* gates_out, void* stream);
+
 /* Empties the layer's expert cache: every slot becomes free and every count
  * zero, as the per-layer slot cache of [P1] §6.2.2 is when created (and
  * after moe_layer_set_weights). Slot contents are not touched; the next calls

@@ -212,6 +212,63 @@ def test_prefill_split_k_small_launch(ctx):
         r.close()
 
 
+def _prompt_check(r, xb, y_tokens):
+    """One moe_forward_prompt call checked against the oracle: ids bit-exact,
+    gates within 1e-6, the cache table after ONE step over all the call's ids,
+    and y on the sampled tokens."""
+    T, k = xb.shape[0], r.s.top_k
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    gates = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    y = moe.moe_forward_prompt(r.h, x, None, ids_out=ids, gates_out=gates)
+    torch.cuda.synchronize()
+    lg = oracle.router_logits(xb, r.w.router, r.s.n_experts, None)
+    oids, ogates = oracle.topk_gates(lg, k)
+    assert (ids.cpu().numpy() == oids).all()
+    assert np.abs(gates.cpu().numpy() - ogates).max() <= GATE_TOL
+    r.cache.step(oids)
+    se, cnt = moe.moe_cache_dump(r.h, r.slots)
+    ose, ocnt = r.cache.dump()
+    assert (se == ose).all() and (cnt == ocnt).all(), "cache table differs from one oracle step"
+    yg = y.cpu().numpy()
+    for t in y_tokens:
+        ref = r.ref.combine(xb[t:t + 1], oids[t:t + 1], ogates[t:t + 1])[0]
+        err = np.abs(yg[t] - ref).max()
+        assert err <= Y_TOL * np.abs(ref).max(), (t, err, np.abs(ref).max())
+    return y
+
+
+@pytest.mark.parametrize("T", [65, 300])
+def test_prompt_layer_major_tiny(ctx, T):
+    """A prompt longer than a chunk in one layer-major call: several shared
+    token blocks (the last ragged), one cache step, twice in a row (the second
+    call on a warm cache gives the same bits)."""
+    s = synth.SHAPES_TINY
+    r = Rig(ctx, s, 0, 4)
+    try:
+        xb = synth.tokens(s, 0, 0, T, False)
+        y0 = _prompt_check(r, xb, [0, T // 2, T - 1])
+        y1 = _prompt_check(r, xb, [0, T - 1])
+        assert torch.equal(y0, y1)
+    finally:
+        r.close()
+
+
+def test_prompt_layer_major_2816(ctx):
+    """A 1024-token prompt of d = 2816 in one call: ~32 token rows per routed
+    expert, the shared expert in 8 token blocks, most experts bypassing the
+    16-slot cache through the staging arena."""
+    s = synth.SHAPES_2816
+    r = Rig(ctx, s, 4, 16)
+    try:
+        xb = synth.tokens(s, 4, 0, 1024, True)
+        _prompt_check(r, xb, [0, 129, 1023])
+        st = moe.moe_layer_stats(r.h)
+        assert st["bypass"] > 0 and st["steps"] == 1
+    finally:
+        r.close()
+
+
 def test_route_call_matches_oracle(ctx):
     s = synth.SHAPES_2816
     r = Rig(ctx, s, 9, 16)
