@@ -463,8 +463,9 @@ def run_ours(args, world, rank, local):
     print(json.dumps(out), flush=True)
 
 
-def _prefill_pass(ctx, dev, stream, layers, xs, y):
-    """One pass of every layer's prompt (8 chunks of 128) with per-kernel events."""
+def _prefill_pass(ctx, dev, stream, layers, xs, y, prompt=False):
+    """One pass of every layer's prompt (8 chunks of 128, or one layer-major
+    call with prompt=True) with per-kernel events."""
     import torch
 
     import expert_streaming_ffn_gb300 as moe
@@ -477,7 +478,10 @@ def _prefill_pass(ctx, dev, stream, layers, xs, y):
     torch.cuda.synchronize(dev)
     ev0.record(stream)
     for h, x in zip(layers, xs):
-        moe.moe_forward(h, x, y=y)
+        if prompt:
+            moe.moe_forward_prompt(h, x, y=y)
+        else:
+            moe.moe_forward(h, x, y=y)
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     kt = moe.moe_ctx_kernel_times(ctx)
@@ -502,12 +506,14 @@ def _gemm_summary(kt, peaks):
 def run_prefill(args, ctx, dev, stream, seed):
     """prefill_2816: a 1024-token prompt as 8 chunks of 128 tokens per layer.
 
-    Three runs: (1) streaming, as configured (16-slot LFU, misses copied from
+    Four runs: (1) streaming, as configured (16-slot LFU, misses copied from
     pinned host memory); (2) all-resident (256 slots, prompt run once to fill
     the slots, then timed), which times the grouped GEMMs on weights already in
     HBM; (3) the shared-expert GEMM alone (a layer of the same d and shared
     expert with a single 64-wide routed expert), the dense contraction the
-    tensor-core roofline applies to."""
+    tensor-core roofline applies to; (4) `layer_major`: the whole prompt in one
+    moe_forward_prompt call per layer (one routing, one cache step, ~32 token
+    rows per routed expert), streaming and all-resident."""
     import torch
 
     import expert_streaming_ffn_gb300 as moe
@@ -568,6 +574,30 @@ def run_prefill(args, ctx, dev, stream, seed):
     out["all_resident"] = {"tok_s_per_layer": prompt / (ms2 * 1e-3), "wall_ms": ms2,
                            "hit_rate": st2[0]["hits"] / max(1, st2[0]["hits"] + st2[0]["misses"]),
                            "kernels": _gemm_summary(kt2, peaks)}
+
+    # (4) layer-major: the same prompt through moe_forward_prompt (one routing,
+    # one cache step and one grouped GEMM pair per layer), streaming from a
+    # fresh 16-slot cache and with every expert resident
+    lm = {}
+    for name, slots in (("streaming", wl.cache_slots), ("all_resident", s.n_experts)):
+        h, w = make(s, slots, 0, w)
+        if slots == s.n_experts:
+            moe.moe_cache_step(h, np.arange(s.n_experts))
+        moe.moe_forward_prompt(h, xs[0], y=y)  # loads the kernels, fills the resident slots
+        torch.cuda.synchronize(dev)
+        if slots != s.n_experts:
+            moe.moe_layer_destroy(h)
+            h, w = make(s, slots, 0, w)
+        ms4, kt4, st4 = _prefill_pass(ctx, dev, stream, [h], xs[:1], y, prompt=True)
+        moe.moe_layer_destroy(h)
+        kms4 = sum(kt4[k][1] for k in ("gemm_gateup", "gemm_down"))
+        fl4 = sum(kt4[k][3] for k in ("gemm_gateup", "gemm_down"))
+        lm[name] = {"tok_s_per_layer": prompt / (ms4 * 1e-3), "wall_ms": ms4,
+                    "expert_TFLOPs": fl4 / (kms4 * 1e-3) / 1e12 if kms4 else None,
+                    "h2d_GB": st4[0]["bytes_h2d"] / 1e9,
+                    "exposed_copy_ms": st4[0]["exposed_copy_us"] / 1e3,
+                    "kernels": _gemm_summary(kt4, peaks)}
+    out["layer_major"] = lm
 
     # (3) the shared-expert GEMM: 128 x 2816 x 2816 (gate, up) and 128 x 2816 x 2816 (down) per chunk
     s3 = synth.Shapes(s.d_model, 1, 1, 64, s.d_ff_shared, s.act)
