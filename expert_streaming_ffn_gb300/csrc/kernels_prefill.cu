@@ -610,7 +610,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool have = ptx::mbar_wait_sleep(raw_full + r, rph, abortp);
                 if (!have && lane == 0) record(7, j, kb0);
                 if (!have && lane == 0 && !*abortp) fail(64u);
-                const unsigned char* raw = ringR + r * kRawBytes;
+                // shared-space addresses: ringR and ringA come from an aligned
+                // integer, so plain pointer accesses would be generic ones
+                const uint32_t raw_s = ptx::smem_addr(ringR + r * kRawBytes);
                 // this group's K-blocks of the unit: stage s + u is ours when (s + u) % 2 == grp
                 const int u0 = ((s & 1) == grp) ? 0 : 1;
                 uint4 cw[2];
@@ -619,8 +621,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int m = 0; m < 2; ++m) {
                     const int u = u0 + 2 * m;
                     if (have && u < nu) {
-                        cw[m] = *reinterpret_cast<const uint4*>(raw + codes_off + u * codes_step);
-                        sbw[m] = *reinterpret_cast<const uint32_t*>(raw + sb_off + u * sb_step);
+                        cw[m] = ptx::lds_u4(raw_s + codes_off + u * codes_step);
+                        sbw[m] = ptx::lds_u32(raw_s + sb_off + u * sb_step);
                     }
                 }
                 for (int u = 0; u < nu; ++u) {
@@ -636,11 +638,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint32_t w = m ? sbw[1] : sbw[0];
                             const __half2 s2 = __half2half2(__ushort_as_half((unsigned short)(w & 0xFFFFu)));
                             const __half2 b2 = __half2half2(__ushort_as_half((unsigned short)(w >> 16)));
-                            unsigned char* arow = ringA + s * kABytes + rho * 128;
+                            const uint32_t arow = ptx::smem_addr(ringA + s * kABytes + rho * 128);
                             const uint32_t words[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
                             for (int q = 0; q < 4; ++q)  // 16-byte chunk 4 hh + q (8 elements) of the 128-byte row
-                                *reinterpret_cast<uint4*>(arow + (((4 * hh + q) ^ swz) << 4)) = dequant8(words[q], s2, b2);
+                                ptx::sts_u4(arow + (((4 * hh + q) ^ swz) << 4), dequant8(words[q], s2, b2));
                             ptx::fence_proxy_async_smem();  // generic-proxy writes, read next by the tensor core
                         } else if (have && lane == 0) {
                             record(8, j, kb0 + u);

@@ -187,6 +187,11 @@ __device__ __forceinline__ float4 lds_f4(uint32_t a) {
                  : "memory");
     return v;
 }
+// A 16-byte store to shared memory by 32-bit shared address.
+__device__ __forceinline__ void sts_u4(uint32_t a, const uint4& v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
 __device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
     uint32_t v;
     asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
