@@ -238,11 +238,13 @@ def _prompt_check(r, xb, y_tokens):
     return y
 
 
-@pytest.mark.parametrize("T", [65, 300])
+@pytest.mark.parametrize("T", [65, 300, 4096])
 def test_prompt_layer_major_tiny(ctx, T):
     """A prompt longer than a chunk in one layer-major call: several shared
     token blocks (the last ragged), one cache step, twice in a row (the second
-    call on a warm cache gives the same bits)."""
+    call on a warm cache gives the same bits). At the largest prompt (4096
+    tokens, ~512 rows per expert) every routed expert is split into pieces of
+    128 rows."""
     s = synth.SHAPES_TINY
     r = Rig(ctx, s, 0, 4)
     try:
