@@ -507,30 +507,43 @@ moe_status issue_miss_copies(moe_layer* L, const StepResult& r, bool with_bypass
     };
     split = split && flags;
     const int parts = split ? 2 : 1;
+    // Whole-expert copies of consecutive experts into consecutive places (the
+    // staging arena's bypass entries, or a fresh cache's slots) go as one copy,
+    // within a flag group: fewer, larger copies keep the copy engine fed at the
+    // link's rate rather than at the host's issue rate. Not with an injected
+    // failure armed, which names one expert's copy.
+    const bool merge = !split && C->fail_copy_at < 0;
     for (int part = 0; part < parts; ++part) {
         const size_t off = part == 0 ? 0 : gu_bytes;
         const size_t len = !split ? L->ebytes : part == 0 ? gu_bytes : L->ebytes - gu_bytes;
-        for (size_t k = 0; k < copies.size(); ++k) {
+        for (size_t k = 0; k < copies.size();) {
+            size_t e = k + 1;  // the run [k, e)
+            while (merge && e < copies.size() && e % kFlagGroup != 0 &&
+                   copies[e].dst == copies[e - 1].dst + L->ebytes && copies[e].src == copies[e - 1].src + L->ebytes)
+                ++e;
             bool injected = false;
             if (part == 0) {
                 if (C->fail_copy_at >= 0 && C->copies_issued == C->fail_copy_at) {
                     injected = true;
                     C->fail_copy_at = -1;
                 }
-                ++C->copies_issued;
+                C->copies_issued += (long)(e - k);
             }
+            const size_t bytes = (e - k - 1) * L->ebytes + len;
             const cudaError_t ce = injected ? cudaErrorUnknown
-                                            : cudaMemcpyAsync(copies[k].dst + off, copies[k].src + off, len,
+                                            : cudaMemcpyAsync(copies[k].dst + off, copies[k].src + off, bytes,
                                                               cudaMemcpyHostToDevice, C->copy_stream);
 
             if (ce != cudaSuccess) return fail_from(k, ce, injected);
-            if (!flags) continue;
-            const int g = (int)(k / kFlagGroup);
-            (*ready_of_miss)[copies[k].i] = MissFlags{2 * g, split ? 2 * g + 1 : 2 * g};
-            if (k + 1 == copies.size() || (k + 1) % kFlagGroup == 0) {
-                const cudaError_t fe = set_flag(2 * g + part);
-                if (fe != cudaSuccess) return fail_from(k, fe, false);
+            if (flags) {
+                const int g = (int)(k / kFlagGroup);
+                for (size_t j = k; j < e; ++j) (*ready_of_miss)[copies[j].i] = MissFlags{2 * g, split ? 2 * g + 1 : 2 * g};
+                if (e == copies.size() || e % kFlagGroup == 0) {
+                    const cudaError_t fe = set_flag(2 * g + part);
+                    if (fe != cudaSuccess) return fail_from(k, fe, false);
+                }
             }
+            k = e;
         }
     }
     L->stats.bytes_h2d += (uint64_t)copies.size() * L->ebytes;
