@@ -60,6 +60,16 @@ def parse():
     ap.add_argument("--resident", action="store_true",
                     help="every expert resident (one slot per expert, all loaded before the warm-up): "
                          "the decode FFN launches then read HBM only (profiling)")
+    ap.add_argument("--no-storage", action="store_true", help="skip the storage-tier leg")
+    ap.add_argument("--storage-only", action="store_true",
+                    help="run only the storage-tier leg and print its JSON (not the bench line)")
+    ap.add_argument("--storage-layers", type=int, default=4)
+    ap.add_argument("--storage-steps", type=int, default=64)
+    ap.add_argument("--storage-warmup", type=int, default=48)
+    ap.add_argument("--storage-host-slots", type=int, default=32)
+    ap.add_argument("--storage-readers", type=int, default=8)
+    ap.add_argument("--storage-readahead", type=int, default=4)
+    ap.add_argument("--storage-dir", default=None, help="where the expert files go (default: the temp dir)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
@@ -408,6 +418,14 @@ def run_ours(args, world, rank, local):
     if not args.no_prefill and args.prefill_layers > 0:
         prefill = run_prefill(args, ctx, dev, stream, seed)
 
+    storage = None
+    if not args.no_storage and args.storage_layers > 0:
+        try:
+            storage = run_storage(args, ctx, dev, stream, seed)
+            storage["pinned_pool_ms_per_layer_token"] = ms_max / args.steps / n_layers
+        except Exception as ex:  # noqa: BLE001 - the leg reports its failure; the bench line stands
+            storage = {"error": f"{type(ex).__name__}: {ex}"}
+
     for h in layers:
         moe.moe_layer_destroy(h)
     moe.moe_ctx_destroy(ctx)
@@ -454,6 +472,7 @@ def run_ours(args, world, rank, local):
                            "launches": kt["expert_ffn_miss"][0], "ms": round(kt["expert_ffn_miss"][1], 4)}
                           if kt.get("expert_ffn_miss", (0, 0))[1] > 0 else None),
         "prefill": prefill,
+        "storage": storage,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,
@@ -610,6 +629,132 @@ def run_prefill(args, ctx, dev, stream, seed):
     return out
 
 
+def _fs_type(path: str) -> str | None:
+    """File system type of the mount holding path (from /proc/mounts)."""
+    try:
+        path = os.path.realpath(path)
+        best, typ = "", None
+        with open("/proc/mounts") as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) >= 3 and (path == parts[1] or path.startswith(parts[1].rstrip("/") + "/")) \
+                        and len(parts[1]) >= len(best):
+                    best, typ = parts[1], parts[2]
+        return typ
+    except OSError:
+        return None
+
+
+def run_storage(args, ctx, dev, stream, seed):
+    """decode_2816 with the routed experts streamed from expert files.
+
+    The storage tier in place of the pinned pool: one expert file per layer
+    (moe_store_write), each layer's misses read by reader threads (O_DIRECT
+    where the file system allows it) into a host tier of
+    --storage-host-slots experts, then copied to the layer's 16 HBM slots.
+    --storage-layers layers, one token per step, Zipf(1.1) routing as in the
+    decode bench. Two runs from fresh stores and caches: `demand` (reads only
+    when a miss needs them) and `readahead` (before each layer, the next
+    layer's --storage-readahead most-routed experts that are in neither its
+    slots nor its tier are read ahead)."""
+    import shutil
+    import tempfile
+    import types
+
+    import torch
+
+    import expert_streaming_ffn_gb300 as moe
+    import synth
+
+    wl = synth.WORKLOADS["decode_2816"]
+    s = wl.shapes
+    L = args.storage_layers
+    H = args.storage_host_slots
+    steps = args.storage_warmup + args.storage_steps
+    root = tempfile.mkdtemp(prefix="moe_store_", dir=args.storage_dir)
+    out = {"workload": "decode_2816 streamed from expert files", "layers": L, "cache_slots": wl.cache_slots,
+           "host_slots": H, "readers": args.storage_readers, "steps": args.storage_steps,
+           "warmup": args.storage_warmup, "file_system": _fs_type(root)}
+    try:
+        t0 = time.perf_counter()
+        paths, w = [], None
+        for l in range(L):
+            w = synth.layer_weights(s, l, seed, reuse=w)
+            paths.append(os.path.join(root, f"layer{l}.experts"))
+            moe.moe_store_write(paths[-1], s, w)
+        del w
+        out["write_s"] = time.perf_counter() - t0
+        out["file_GB"] = sum(os.path.getsize(p) for p in paths) / 1e9
+        zbs = [torch.from_numpy(synth.zipf_bias(s, l, wl.zipf_s, wl.zipf_beta, seed)).to(dev) for l in range(L)]
+        xs_np = np.empty((steps, L, s.d_model), np.uint16)
+        for st in range(steps):
+            for l in range(L):
+                xs_np[st, l] = synth.tokens(s, l, st, 1, wl.rms_normalise, seed)[0]
+        x_dev = torch.from_numpy(xs_np.view(np.int16)).view(torch.bfloat16).to(dev)
+        y_dev = torch.empty((L, s.d_model), dtype=torch.float32, device=dev)
+        row = s.d_model * 2
+        sptr = stream.cuda_stream
+        for mode, pf in (("demand", 0), ("readahead", args.storage_readahead)):
+            stores, layers = [], []
+            for l in range(L):
+                stores.append(moe.moe_store_open(paths[l], s, H, args.storage_readers, moe.MOE_STORE_DIRECT))
+                layers.append(moe.moe_layer_create_streamed(ctx, s, wl.cache_slots, stores[-1], wl.policy))
+                resident = types.SimpleNamespace(router=synth.router_weights(s, l, seed),
+                                                 shared=synth.ffn_weights(s, l, 0, seed, shared=True))
+                moe.moe_layer_set_weights(layers[-1], resident, routed=False)
+
+            def step(st):
+                base = x_dev.data_ptr() + st * L * row
+                for l in range(L):
+                    if pf:
+                        moe.moe_layer_prefetch(layers[(l + 1) % L], pf)
+                    moe.moe_forward_ptr(layers[l], base + l * row, 1, zbs[l].data_ptr(), y_dev[l].data_ptr(),
+                                        sptr)
+
+            for st in range(args.storage_warmup):
+                step(st)
+            torch.cuda.synchronize(dev)
+            for h, sto in zip(layers, stores):
+                moe.moe_layer_reset_stats(h)
+                moe.moe_store_reset_stats(sto)
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t_wall = time.perf_counter()
+            ev0.record(stream)
+            for st in range(args.storage_warmup, steps):
+                step(st)
+            ev1.record(stream)
+            torch.cuda.synchronize(dev)
+            t_wall = time.perf_counter() - t_wall
+            ms = ev0.elapsed_time(ev1)
+            ls = [moe.moe_layer_stats(h) for h in layers]
+            ss = [moe.moe_store_get_stats(x) for x in stores]
+            for h in layers:
+                moe.moe_layer_destroy(h)
+            for x in stores:
+                moe.moe_store_close(x)
+            K = args.storage_steps
+            hits = sum(x["hits"] for x in ls)
+            misses = sum(x["misses"] for x in ls)
+            tot = {k: sum(x[k] for x in ss) for k in ("fetches", "tier_hits", "reads", "prefetch_reads",
+                                                       "prefetch_used", "bytes_read", "read_errors")}
+            read_us = sum(x["read_us"] for x in ss)
+            wait_us = sum(x["wait_us"] for x in ss)
+            out[mode] = {
+                "tok_s": K / (ms * 1e-3), "ms_per_layer_token": ms / K / L,
+                "hbm_hit_rate": hits / (hits + misses) if hits + misses else None,
+                "tier_hit_rate": tot["tier_hits"] / tot["fetches"] if tot["fetches"] else None,
+                "reads_per_token": tot["reads"] / K, "read_MB_per_token": tot["bytes_read"] / K / 1e6,
+                "read_GBs": tot["bytes_read"] / t_wall / 1e9,
+                "mean_read_ms": read_us / tot["reads"] / 1e3 if tot["reads"] else None,
+                "fetch_wait_ms_per_token": wait_us / K / 1e3,
+                "prefetch_reads": tot["prefetch_reads"], "prefetch_used": tot["prefetch_used"],
+                "read_errors": tot["read_errors"], "direct_io": bool(ss[0]["direct"]),
+            }
+    finally:
+        shutil.rmtree(root, ignore_errors=True)
+    return out
+
+
 def main():
     args = parse()
     world, rank, local = dist_init()
@@ -627,6 +772,18 @@ def main():
         moe.moe_ctx_destroy(ctx)
         if rank == 0:
             print(json.dumps({"prefill": out}), flush=True)
+    elif args.storage_only:
+        import torch
+
+        import expert_streaming_ffn_gb300 as moe
+
+        torch.cuda.set_device(local)
+        moe.load()
+        ctx = moe.moe_ctx_create(local)
+        out = run_storage(args, ctx, torch.device("cuda", local), torch.cuda.current_stream(), 1000 * rank)
+        moe.moe_ctx_destroy(ctx)
+        if rank == 0:
+            print(json.dumps({"storage": out}), flush=True)
     else:
         run_ours(args, world, rank, local)
     if world > 1:

@@ -20,7 +20,8 @@ from . import build as _build
 LIB_PATH = _build.LIB
 _lib = None
 
-MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA, MOE_ECOPY, MOE_ETIMEOUT, MOE_ESTATE = range(7)
+MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA, MOE_ECOPY, MOE_ETIMEOUT, MOE_ESTATE, MOE_EBUSY, MOE_EIO = range(9)
+MOE_STORE_DIRECT = 1
 LFU, LRU = 0, 1
 GELU_TANH, SILU = 0, 1
 KERNEL_KINDS = ("router", "expert_ffn", "combine", "gemm_gateup", "gemm_down", "pf_gather", "expert_ffn_miss")
@@ -33,7 +34,7 @@ class MoeError(RuntimeError):
 
 
 _STATUS = {0: "MOE_OK", 1: "MOE_EINVAL", 2: "MOE_ENOMEM", 3: "MOE_ECUDA", 4: "MOE_ECOPY", 5: "MOE_ETIMEOUT",
-           6: "MOE_ESTATE"}
+           6: "MOE_ESTATE", 7: "MOE_EBUSY", 8: "MOE_EIO"}
 
 
 class moe_shapes(ctypes.Structure):
@@ -58,6 +59,13 @@ class moe_stats(ctypes.Structure):
                 ("bypass", ctypes.c_uint64), ("bytes_h2d", ctypes.c_uint64), ("bytes_resident", ctypes.c_uint64),
                 ("exposed_copy_us", ctypes.c_double), ("host_wait_us", ctypes.c_double),
                 ("host_issue_us", ctypes.c_double)]
+
+
+class moe_store_stats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_uint64) for n in ("fetches", "tier_hits", "reads", "prefetch_reads", "prefetch_used",
+                                                "bytes_read", "read_errors")] + \
+               [("read_us", ctypes.c_double), ("wait_us", ctypes.c_double), ("direct", ctypes.c_int32),
+                ("host_slots", ctypes.c_int32), ("readers", ctypes.c_int32)]
 
 
 # (name, restype, argtypes) of every exported symbol in include/moe.h
@@ -92,6 +100,19 @@ SIGNATURES = [
     ("moe_ctx_reset_kernel_times", _i32, [_vp]),
     ("moe_ctx_launches", _i32, [_vp, _P(ctypes.c_uint64)]),
     ("moe_ctx_inject_copy_failure", _i32, [_vp, _i64]),
+    ("moe_store_expert_stride", _sz, [_P(moe_shapes)]),
+    ("moe_store_write", _i32, [ctypes.c_char_p, _P(moe_shapes), _P(moe_host_weights)]),
+    ("moe_store_open", _i32, [ctypes.c_char_p, _P(moe_shapes), _i32, _i32, _i32, _P(_vp)]),
+    ("moe_store_close", _i32, [_vp]),
+    ("moe_store_fetch", _i32, [_vp, _i32, _P(_vp)]),
+    ("moe_store_release", _i32, [_vp, _i32]),
+    ("moe_store_prefetch", _i32, [_vp, _vp, _i32, _P(_i32)]),
+    ("moe_store_wait_idle", _i32, [_vp]),
+    ("moe_store_get_stats", _i32, [_vp, _P(moe_store_stats)]),
+    ("moe_store_reset_stats", _i32, [_vp]),
+    ("moe_store_tier", _i32, [_vp, _vp, _vp]),
+    ("moe_layer_create_streamed", _i32, [_vp, _P(moe_shapes), _P(moe_quant_layout), _i32, _i32, _vp, _P(_vp)]),
+    ("moe_layer_prefetch", _i32, [_vp, _i32, _P(_i32)]),
 ]
 
 
@@ -184,14 +205,23 @@ def _qm(codes, scale, bias, keep) -> moe_qmatrix:
     return moe_qmatrix(_hptr(c), _hptr(s), _hptr(b))
 
 
-def moe_layer_set_weights(layer: int, w) -> None:
-    """w: canonical-layout arrays with the attributes of synth.LayerWeights."""
-    keep: list = []
+def _host_weights(w, keep: list, routed: bool = True, resident: bool = True) -> moe_host_weights:
+    """moe_host_weights over canonical-layout arrays (the attributes of
+    synth.LayerWeights); the routed or the resident matrices may be left NULL."""
+    null = moe_qmatrix(None, None, None)
     g, u, d = w.shared
-    hw = moe_host_weights(_qm(*w.router, keep), _qm(*g, keep), _qm(*u, keep), _qm(*d, keep),
-                          _qm(w.gate_codes, w.gate_scale, w.gate_bias, keep),
-                          _qm(w.up_codes, w.up_scale, w.up_bias, keep),
-                          _qm(w.down_codes, w.down_scale, w.down_bias, keep))
+    res = [_qm(*w.router, keep), _qm(*g, keep), _qm(*u, keep), _qm(*d, keep)] if resident else [null] * 4
+    rt = [_qm(w.gate_codes, w.gate_scale, w.gate_bias, keep), _qm(w.up_codes, w.up_scale, w.up_bias, keep),
+          _qm(w.down_codes, w.down_scale, w.down_bias, keep)] if routed else [null] * 3
+    return moe_host_weights(*res, *rt)
+
+
+def moe_layer_set_weights(layer: int, w, routed: bool = True) -> None:
+    """w: canonical-layout arrays with the attributes of synth.LayerWeights.
+    routed=False passes NULL routed matrices (a streamed layer reads them from
+    its store)."""
+    keep: list = []
+    hw = _host_weights(w, keep, routed=routed)
     _check(load().moe_layer_set_weights(layer, ctypes.byref(hw)), "moe_layer_set_weights")
 
 
@@ -322,6 +352,91 @@ def moe_group_pairs(ids, n_experts: int):
     perm = np.empty(max(n, 1), np.int32)
     _check(load().moe_group_pairs(_hptr(ids), n, n_experts, _hptr(offsets), _hptr(perm)), "moe_group_pairs")
     return offsets, perm[:n].copy()
+
+
+# ---------------------------------------------------------------------------
+# storage tier (expert files; no GPU needed except for streamed layers)
+
+
+def moe_store_expert_stride(shapes) -> int:
+    sh = make_shapes(shapes)
+    return load().moe_store_expert_stride(ctypes.byref(sh))
+
+
+def moe_store_write(path: str, shapes, w) -> None:
+    """Write the routed experts of w (canonical layout) as an expert file."""
+    sh = make_shapes(shapes)
+    keep: list = []
+    hw = _host_weights(w, keep, resident=False)
+    _check(load().moe_store_write(os.fsencode(path), ctypes.byref(sh), ctypes.byref(hw)), "moe_store_write")
+
+
+def moe_store_open(path: str, shapes, host_slots: int, readers: int = 4, flags: int = 0) -> int:
+    sh = make_shapes(shapes)
+    h = ctypes.c_void_p()
+    _check(load().moe_store_open(os.fsencode(path), ctypes.byref(sh), host_slots, readers, flags, ctypes.byref(h)),
+           "moe_store_open")
+    return h.value
+
+
+def moe_store_close(store: int) -> None:
+    _check(load().moe_store_close(store), "moe_store_close")
+
+
+def moe_store_fetch(store: int, expert: int, nbytes: int) -> np.ndarray:
+    """Fetch (and pin) an expert; returns a copy of its first nbytes bytes."""
+    p = ctypes.c_void_p()
+    _check(load().moe_store_fetch(store, expert, ctypes.byref(p)), "moe_store_fetch")
+    return np.ctypeslib.as_array(ctypes.cast(p, ctypes.POINTER(ctypes.c_uint8)), shape=(nbytes,)).copy()
+
+
+def moe_store_release(store: int, expert: int) -> None:
+    _check(load().moe_store_release(store, expert), "moe_store_release")
+
+
+def moe_store_prefetch(store: int, experts) -> int:
+    e = np.ascontiguousarray(np.asarray(experts).reshape(-1), np.int32)
+    q = ctypes.c_int32()
+    _check(load().moe_store_prefetch(store, _hptr(e) if e.size else None, e.size, ctypes.byref(q)),
+           "moe_store_prefetch")
+    return q.value
+
+
+def moe_store_wait_idle(store: int) -> None:
+    _check(load().moe_store_wait_idle(store), "moe_store_wait_idle")
+
+
+def moe_store_get_stats(store: int) -> dict:
+    st = moe_store_stats()
+    _check(load().moe_store_get_stats(store, ctypes.byref(st)), "moe_store_get_stats")
+    return {n: getattr(st, n) for n, _ in moe_store_stats._fields_}
+
+
+def moe_store_reset_stats(store: int) -> None:
+    _check(load().moe_store_reset_stats(store), "moe_store_reset_stats")
+
+
+def moe_store_tier(store: int, host_slots: int):
+    """(expert per entry, state per entry): 0 empty, 1 being read, 2 ready, 3 failed."""
+    ex = np.empty(host_slots, np.int32)
+    stt = np.empty(host_slots, np.int32)
+    _check(load().moe_store_tier(store, _hptr(ex), _hptr(stt)), "moe_store_tier")
+    return ex, stt
+
+
+def moe_layer_create_streamed(ctx: int, shapes, cache_slots: int, store: int, policy: int = LFU) -> int:
+    sh = make_shapes(shapes)
+    q = moe_quant_layout(4, 64, 8, 64)
+    h = ctypes.c_void_p()
+    _check(load().moe_layer_create_streamed(ctx, ctypes.byref(sh), ctypes.byref(q), cache_slots, policy, store,
+                                            ctypes.byref(h)), "moe_layer_create_streamed")
+    return h.value
+
+
+def moe_layer_prefetch(layer: int, n: int) -> int:
+    q = ctypes.c_int32()
+    _check(load().moe_layer_prefetch(layer, n, ctypes.byref(q)), "moe_layer_prefetch")
+    return q.value
 
 
 # ---------------------------------------------------------------------------

@@ -29,6 +29,7 @@
 #include <algorithm>
 #include <atomic>
 #include <chrono>
+#include <deque>
 #include <mutex>
 #include <new>
 #include <string>
@@ -273,13 +274,24 @@ struct moe_layer {
     std::vector<int32_t> offsets, perm;
     moe_stats stats{};
     std::vector<WaitRec> waits;
+    // storage tier (moe_layer_create_streamed): misses are fetched from the
+    // store's host tier instead of h_pool; an entry stays pinned until the
+    // copy that reads it has finished (the event recorded behind it on the
+    // copy stream). route_hist counts, per expert, the steps that routed to it.
+    moe_expert_store* store = nullptr;
+    uint8_t* store_pinned = nullptr;  // the tier buffer registered with CUDA
+    struct StorePin {
+        std::vector<int> experts;
+        cudaEvent_t ev;
+    };
+    std::deque<StorePin> store_pins;  // in copy-stream order
+    std::vector<cudaEvent_t> store_events;  // free events for store_pins
+    std::vector<uint32_t> route_hist;
 
     moe_layer(int E, int S_, int pol) : cache(E, S_, pol) {}
 };
 
-namespace {
-
-moe_status check_shapes(const moe_shapes* s) {
+moe_status moe::check_shapes(const moe_shapes* s) {
     if (!s) return set_error(MOE_EINVAL, "shapes is NULL");
     if (s->d_model < 256 || s->d_model > kMaxDModel || s->d_model % 256 != 0)
         return set_error(MOE_EINVAL, "d_model %d must be a multiple of 256 in [256, %d]", s->d_model, kMaxDModel);
@@ -295,6 +307,8 @@ moe_status check_shapes(const moe_shapes* s) {
     if (s->act != 0 && s->act != 1) return set_error(MOE_EINVAL, "act %d must be 0 (GELU tanh) or 1 (SiLU)", s->act);
     return MOE_OK;
 }
+
+namespace {
 
 // Items of one prefill call of T tokens: the shared expert per block of
 // kPfMaxN tokens, and each routed expert's pairs in pieces of at most kPfMaxN.
@@ -465,8 +479,160 @@ constexpr int kFlagGroup = 8;
 // whole and flag 2g covers both parts. On failure every slot this step
 // filled but whose copy is not known good is emptied, so the table never
 // claims bytes that are missing.
+// Release the tier entries whose copies have finished (all of them, waiting
+// for each copy, with wait_all).
+moe_status release_store_pins(moe_layer* L, bool wait_all) {
+    while (!L->store_pins.empty()) {
+        moe_layer::StorePin& p = L->store_pins.front();
+        if (wait_all) {
+            CUDA_TRY(cudaEventSynchronize(p.ev));
+        } else {
+            const cudaError_t q = cudaEventQuery(p.ev);
+            if (q == cudaErrorNotReady) break;
+            if (q != cudaSuccess) CUDA_TRY(q);
+        }
+        for (int e : p.experts) store_release(L->store, e);
+        L->store_events.push_back(p.ev);
+        L->store_pins.pop_front();
+    }
+    return MOE_OK;
+}
+
+// Record an event on the copy stream behind the copies issued so far; the
+// listed experts' tier entries are released once it completes.
+moe_status pin_until_copied(moe_layer* L, std::vector<int> experts) {
+    if (experts.empty()) return MOE_OK;
+    cudaEvent_t ev = nullptr;
+    if (!L->store_events.empty()) {
+        ev = L->store_events.back();
+        L->store_events.pop_back();
+    } else {
+        CUDA_TRY(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+    }
+    const cudaError_t e = cudaEventRecord(ev, L->ctx->copy_stream);
+    if (e != cudaSuccess) {
+        L->store_events.push_back(ev);
+        CUDA_TRY(e);
+    }
+    L->store_pins.push_back(moe_layer::StorePin{std::move(experts), ev});
+    return MOE_OK;
+}
+
+// issue_miss_copies for a layer that streams from an expert store: the same
+// destinations, flags, parts and failure handling, but each expert's source
+// is its entry in the store's host tier. The reads of every miss are queued
+// first (as many as the tier has free entries), then each copy is issued as
+// soon as its read lands, so reads, copies and the kernels waiting on the
+// flags overlap. An entry stays pinned until its last copy has finished.
+// Nothing is merged: tier entries are not consecutive experts.
+moe_status issue_store_copies(moe_layer* L, const StepResult& r, bool with_bypass, uint32_t epoch,
+                              std::vector<MissFlags>* ready_of_miss, bool split) {
+    moe_ctx* C = L->ctx;
+    L->h_epochs[epoch % kEpochRing] = epoch;
+    moe_status st = release_store_pins(L, false);
+    if (st != MOE_OK) return st;
+    if (with_bypass && r.bypass > 0) {
+        st = ensure_staging(C, (size_t)r.bypass * L->ebytes);
+        if (st != MOE_OK) return st;
+        CUDA_TRY(cudaStreamWaitEvent(C->copy_stream, C->staging_free, 0));
+    }
+    if (ready_of_miss) ready_of_miss->assign(r.miss_experts.size(), MissFlags{});
+    struct Copy {
+        size_t i;
+        uint8_t* dst;
+        const uint8_t* src;
+    };
+    std::vector<Copy> copies;
+    std::vector<int32_t> wanted;
+    int nb = 0;
+    for (size_t i = 0; i < r.miss_experts.size(); ++i) {
+        const int slot = r.miss_slots[i];
+        if (slot < 0 && !with_bypass) continue;
+        uint8_t* dst = slot >= 0 ? L->d_slots + (size_t)slot * L->ebytes : C->staging + (size_t)(nb++) * L->ebytes;
+        copies.push_back(Copy{i, dst, nullptr});
+        wanted.push_back(r.miss_experts[i]);
+    }
+    store_readahead(L->store, wanted.data(), (int)wanted.size(), false);
+    const bool flags = ready_of_miss != nullptr;
+    // a split copy reads its entry twice, so every entry of the call stays
+    // pinned across both parts: only when the tier can hold them all
+    split = split && flags && copies.size() <= (size_t)store_host_slots(L->store);
+    const int parts = split ? 2 : 1;
+    const size_t gu_bytes = 2 * qmat_bytes(L->sh.d_ff, L->sh.d_model);
+    auto set_flag = [&](int flag) {
+        return cudaMemcpyAsync(L->d_ready + flag, L->h_epochs + epoch % kEpochRing, sizeof(uint32_t),
+                               cudaMemcpyHostToDevice, C->copy_stream);
+    };
+    std::vector<int> held;  // entries fetched but not yet behind a recorded event
+    auto fail_from = [&](size_t k, moe_status code, const char* why) {
+        for (size_t j = copies[k].i; j < r.miss_experts.size(); ++j)
+            if (r.miss_slots[j] >= 0) L->cache.evict(r.miss_slots[j]);
+        pin_until_copied(L, held);  // the copies already issued may still read them
+        return set_error(code, "copy of expert %d (slot %d) failed: %s", r.miss_experts[copies[k].i],
+                         r.miss_slots[copies[k].i], why);
+    };
+    for (int part = 0; part < parts; ++part) {
+        const size_t off = part == 0 ? 0 : gu_bytes;
+        const size_t len = !split ? L->ebytes : part == 0 ? gu_bytes : L->ebytes - gu_bytes;
+        for (size_t k = 0; k < copies.size(); ++k) {
+            const int e = r.miss_experts[copies[k].i];
+            bool injected = false;
+            if (part == 0) {
+                for (;;) {  // the expert's bytes in the tier
+                    st = store_acquire(L->store, e, &copies[k].src);
+                    if (st != MOE_EBUSY || L->store_pins.empty()) break;
+                    // every entry is pinned by copies still in flight: wait for the oldest
+                    st = release_store_pins(L, false);
+                    if (st == MOE_OK && !L->store_pins.empty()) {
+                        const cudaError_t we = cudaEventSynchronize(L->store_pins.front().ev);
+                        st = we == cudaSuccess ? release_store_pins(L, false)
+                                               : set_error(MOE_ECUDA, "%s", cudaGetErrorString(we));
+                    }
+                    if (st != MOE_OK) break;
+                }
+                if (st != MOE_OK) {
+                    const std::string why = moe_last_error();
+                    return fail_from(k, MOE_ECOPY, why.c_str());
+                }
+                held.push_back(e);
+                if (C->fail_copy_at >= 0 && C->copies_issued == C->fail_copy_at) {
+                    injected = true;
+                    C->fail_copy_at = -1;
+                }
+                C->copies_issued += 1;
+            }
+            const cudaError_t ce = injected ? cudaErrorUnknown
+                                            : cudaMemcpyAsync(copies[k].dst + off, copies[k].src + off, len,
+                                                              cudaMemcpyHostToDevice, C->copy_stream);
+            if (ce != cudaSuccess) {
+                if (!injected) cudaGetLastError();
+                return fail_from(k, MOE_ECOPY, injected ? "injected failure" : cudaGetErrorString(ce));
+            }
+            if (part == parts - 1) {
+                st = pin_until_copied(L, {e});
+                if (st != MOE_OK) return st;
+                held.erase(std::find(held.begin(), held.end(), e));
+            }
+            if (flags) {
+                const int g = (int)(k / kFlagGroup);
+                (*ready_of_miss)[copies[k].i] = MissFlags{2 * g, split ? 2 * g + 1 : 2 * g};
+                if (k + 1 == copies.size() || (k + 1) % kFlagGroup == 0) {
+                    const cudaError_t fe = set_flag(2 * g + part);
+                    if (fe != cudaSuccess) {
+                        cudaGetLastError();
+                        return fail_from(k, MOE_ECOPY, cudaGetErrorString(fe));
+                    }
+                }
+            }
+        }
+    }
+    L->stats.bytes_h2d += (uint64_t)copies.size() * L->ebytes;
+    return MOE_OK;
+}
+
 moe_status issue_miss_copies(moe_layer* L, const StepResult& r, bool with_bypass, uint32_t epoch,
                              std::vector<MissFlags>* ready_of_miss, bool split = false) {
+    if (L->store) return issue_store_copies(L, r, with_bypass, epoch, ready_of_miss, split);
     moe_ctx* C = L->ctx;
     L->h_epochs[epoch % kEpochRing] = epoch;
     if (with_bypass && r.bypass > 0) {
@@ -953,6 +1119,8 @@ moe_status forward_chunk(moe_layer* L, const uint16_t* x, int T, const float* zb
     L->slot_before = L->cache.slot_expert;
     if (!L->cache.step(L->h_ids.data(), npairs, L->step))
         return set_error(MOE_ESTATE, "router produced an invalid id");
+    if (L->store)
+        for (int e : L->step.distinct) ++L->route_hist[(size_t)e];
     if (device_routed) {
         // the resident launch counted every routed pair as a hit
         const size_t n_miss = L->step.miss_experts.size();
@@ -1013,6 +1181,8 @@ extern "C" const char* moe_status_str(moe_status s) {
         case MOE_ECOPY: return "MOE_ECOPY";
         case MOE_ETIMEOUT: return "MOE_ETIMEOUT";
         case MOE_ESTATE: return "MOE_ESTATE";
+        case MOE_EBUSY: return "MOE_EBUSY";
+        case MOE_EIO: return "MOE_EIO";
     }
     return "MOE_UNKNOWN";
 }
@@ -1112,6 +1282,12 @@ extern "C" void moe_layer_destroy(moe_layer* L) {
     cudaStreamSynchronize(L->ctx->copy_stream);
     drain_waits(L);
     free_scratch(L);
+    if (L->store) {
+        release_store_pins(L, true);
+        for (cudaEvent_t e : L->store_events) cudaEventDestroy(e);
+        if (L->store_pinned) cudaHostUnregister(L->store_pinned);
+        store_attach(L->store, false);
+    }
     cudaFree(L->d_router_codes);
     cudaFree(L->d_router_sb);
     cudaFree(L->d_shared);
@@ -1125,8 +1301,12 @@ extern "C" void moe_layer_destroy(moe_layer* L) {
     delete L;
 }
 
-extern "C" moe_status moe_layer_create(moe_ctx* C, const moe_shapes* s, const moe_quant_layout* q, int32_t slots,
-                                       int32_t policy, moe_layer** out) {
+namespace {
+
+// moe_layer_create, with the pinned pool of every routed expert (with_pool)
+// or without it (a layer that streams from an expert store).
+moe_status create_layer(moe_ctx* C, const moe_shapes* s, const moe_quant_layout* q, int32_t slots, int32_t policy,
+                        bool with_pool, moe_layer** out) {
     if (!C || !out) return set_error(MOE_EINVAL, "ctx or out is NULL");
     moe_status st = check_shapes(s);
     if (st != MOE_OK) return st;
@@ -1157,13 +1337,14 @@ extern "C" moe_status moe_layer_create(moe_ctx* C, const moe_shapes* s, const mo
               cudaMemset(L->d_slot_of, 0xFF, (size_t)s->n_experts * sizeof(int32_t)) == cudaSuccess &&
               cudaMalloc(&L->d_ready, n_flags * sizeof(uint32_t)) == cudaSuccess &&
               cudaMemset(L->d_ready, 0, n_flags * sizeof(uint32_t)) == cudaSuccess &&
-              cudaHostAlloc(&L->h_pool, (size_t)s->n_experts * L->ebytes, cudaHostAllocDefault) == cudaSuccess &&
+              (!with_pool ||
+               cudaHostAlloc(&L->h_pool, (size_t)s->n_experts * L->ebytes, cudaHostAllocDefault) == cudaSuccess) &&
               cudaHostAlloc(&L->h_epochs, kEpochRing * sizeof(uint32_t), cudaHostAllocDefault) == cudaSuccess;
     if (!ok) {
         cudaGetLastError();
         moe_layer_destroy(L);
         return set_error(MOE_ENOMEM, "layer allocation failed (%zu B pinned pool, %zu B slots)",
-                         (size_t)s->n_experts * L->ebytes, (size_t)slots * L->ebytes);
+                         with_pool ? (size_t)s->n_experts * L->ebytes : (size_t)0, (size_t)slots * L->ebytes);
     }
     ok = cudaEventCreateWithFlags(&L->ev_done, cudaEventDisableTiming) == cudaSuccess &&
          cudaEventCreateWithFlags(&L->ev_pending, cudaEventDisableTiming) == cudaSuccess;
@@ -1176,12 +1357,74 @@ extern "C" moe_status moe_layer_create(moe_ctx* C, const moe_shapes* s, const mo
     return MOE_OK;
 }
 
+}  // namespace
+
+extern "C" moe_status moe_layer_create(moe_ctx* C, const moe_shapes* s, const moe_quant_layout* q, int32_t slots,
+                                       int32_t policy, moe_layer** out) {
+    return create_layer(C, s, q, slots, policy, true, out);
+}
+
+extern "C" moe_status moe_layer_create_streamed(moe_ctx* C, const moe_shapes* s, const moe_quant_layout* q,
+                                                int32_t slots, int32_t policy, moe_expert_store* store,
+                                                moe_layer** out) {
+    if (!store) return set_error(MOE_EINVAL, "store is NULL");
+    moe_status st = check_shapes(s);
+    if (st != MOE_OK) return st;
+    if (memcmp(&store_shapes(store), s, sizeof(moe_shapes)) != 0)
+        return set_error(MOE_EINVAL, "the store holds experts of other shapes");
+    if (!store_attach(store, true)) return set_error(MOE_EINVAL, "the store already serves a layer");
+    moe_layer* L = nullptr;
+    st = create_layer(C, s, q, slots, policy, false, &L);
+    if (st != MOE_OK) {
+        store_attach(store, false);
+        return st;
+    }
+    size_t bytes = 0;
+    uint8_t* buf = store_buffer(store, &bytes);
+    const cudaError_t e = cudaHostRegister(buf, bytes, cudaHostRegisterDefault);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        moe_layer_destroy(L);
+        store_attach(store, false);
+        return set_error(MOE_ECUDA, "page-locking the store's %zu B tier failed: %s", bytes, cudaGetErrorString(e));
+    }
+    L->store = store;
+    L->store_pinned = buf;
+    L->route_hist.assign((size_t)s->n_experts, 0);
+    *out = L;
+    return MOE_OK;
+}
+
+extern "C" moe_status moe_layer_prefetch(moe_layer* L, int32_t n, int32_t* queued) {
+    if (queued) *queued = 0;
+    if (!L || n < 0) return set_error(MOE_EINVAL, "moe_layer_prefetch: bad arguments");
+    if (!L->store) return set_error(MOE_ESTATE, "moe_layer_prefetch: the layer does not stream from a store");
+    if (n == 0) return MOE_OK;
+    // entries whose copies have finished may take the reads
+    moe_status st = release_store_pins(L, false);
+    if (st != MOE_OK) return st;
+    // experts by routing count, highest first, ties to the lower id
+    std::vector<int32_t> order;
+    for (int e = 0; e < L->sh.n_experts; ++e)
+        if (L->route_hist[(size_t)e] > 0 && L->cache.slot_of(e) < 0 && !store_contains(L->store, e))
+            order.push_back(e);
+    const size_t take = std::min(order.size(), (size_t)n);
+    std::partial_sort(order.begin(), order.begin() + (long)take, order.end(), [&](int32_t a, int32_t b) {
+        const uint32_t ca = L->route_hist[(size_t)a], cb = L->route_hist[(size_t)b];
+        return ca != cb ? ca > cb : a < b;
+    });
+    const int q = store_readahead(L->store, order.data(), (int)take, true);
+    if (queued) *queued = q;
+    return MOE_OK;
+}
+
 extern "C" moe_status moe_layer_set_weights(moe_layer* L, const moe_host_weights* w) {
     if (!L || !w) return set_error(MOE_EINVAL, "layer or weights is NULL");
     const moe_qmatrix* all[] = {&w->router, &w->shared_gate, &w->shared_up, &w->shared_down, &w->gate, &w->up,
                                 &w->down};
-    for (const moe_qmatrix* m : all)
-        if (!m->codes || !m->scale || !m->bias) return set_error(MOE_EINVAL, "a weight pointer is NULL");
+    const int n_needed = L->store ? 4 : 7;  // a streamed layer's routed experts come from its store
+    for (int i = 0; i < n_needed; ++i)
+        if (!all[i]->codes || !all[i]->scale || !all[i]->bias) return set_error(MOE_EINVAL, "a weight pointer is NULL");
     CUDA_TRY(cudaSetDevice(L->ctx->device));
     const moe_shapes& s = L->sh;
     const int d = s.d_model, I = s.d_ff, Is = s.d_ff_shared, E = s.n_experts;
@@ -1209,13 +1452,15 @@ extern "C" moe_status moe_layer_set_weights(moe_layer* L, const moe_host_weights
         repack_qmatrix(u, I, d, dst + qmat_bytes(I, d));
         repack_down(dn, d, I, dst + 2 * qmat_bytes(I, d));
     };
-    unsigned nth = std::max(1u, std::min(16u, std::thread::hardware_concurrency()));
-    std::vector<std::thread> pool;
-    for (unsigned t = 0; t < nth; ++t)
-        pool.emplace_back([&, t] {
-            for (int e = (int)t; e < E; e += (int)nth) one(e);
-        });
-    for (auto& th : pool) th.join();
+    if (L->h_pool) {
+        unsigned nth = std::max(1u, std::min(16u, std::thread::hardware_concurrency()));
+        std::vector<std::thread> pool;
+        for (unsigned t = 0; t < nth; ++t)
+            pool.emplace_back([&, t] {
+                for (int e = (int)t; e < E; e += (int)nth) one(e);
+            });
+        for (auto& th : pool) th.join();
+    }
     L->cache.reset();
     moe_status st = table_upload_sync(L);
     if (st != MOE_OK) return st;
@@ -1251,6 +1496,8 @@ extern "C" moe_status moe_cache_step(moe_layer* L, const int32_t* ids, int32_t n
     CUDA_TRY(cudaSetDevice(L->ctx->device));
     L->slot_before = L->cache.slot_expert;
     if (!L->cache.step(ids, n_ids, L->step)) return set_error(MOE_EINVAL, "moe_cache_step: expert id out of range");
+    if (L->store)
+        for (int e : L->step.distinct) ++L->route_hist[(size_t)e];
     L->stats.steps += 1;
     L->stats.hits += L->step.hits;
     L->stats.misses += L->step.miss_experts.size();

@@ -33,6 +33,26 @@ constexpr int kPromptMaxT = 4096;   // tokens of one layer-major prompt call
 // Records a message for moe_last_error() (thread-local) and returns s.
 moe_status set_error(moe_status s, const char* fmt, ...);
 
+// MOE_OK if the shapes are ones the library supports, else MOE_EINVAL.
+moe_status check_shapes(const moe_shapes* s);
+
+// ---- storage tier (store.cpp) ------------------------------------------------
+//
+// An expert file read into a host tier of H expert buffers. store_acquire
+// returns the expert's bytes (reading them first if needed) and pins its
+// entry; store_release unpins it. store_readahead queues reads for experts not
+// in the tier, into entries nobody pins (never taking an entry read ahead and
+// not yet fetched); it returns how many it queued.
+
+moe_status store_acquire(moe_expert_store* s, int expert, const uint8_t** out);
+moe_status store_release(moe_expert_store* s, int expert);
+int store_readahead(moe_expert_store* s, const int32_t* experts, int n, bool predicted);
+bool store_contains(moe_expert_store* s, int expert);
+uint8_t* store_buffer(moe_expert_store* s, size_t* bytes);
+int store_host_slots(const moe_expert_store* s);
+const moe_shapes& store_shapes(const moe_expert_store* s);
+bool store_attach(moe_expert_store* s, bool on);  // false: already attached
+
 // ---- expert cache ----------------------------------------------------------
 
 struct StepResult {

@@ -43,12 +43,15 @@ typedef enum {
     MOE_ECUDA = 3,    /* a CUDA runtime call failed */
     MOE_ECOPY = 4,    /* a miss copy failed; the slot is left empty */
     MOE_ETIMEOUT = 5, /* a bounded device wait expired */
-    MOE_ESTATE = 6    /* call out of order (e.g. forward before set_weights) */
+    MOE_ESTATE = 6,   /* call out of order (e.g. forward before set_weights) */
+    MOE_EBUSY = 7,    /* every host-tier entry of an expert store is pinned */
+    MOE_EIO = 8       /* a file of the storage tier could not be read or written */
 } moe_status;
 
 typedef struct moe_ctx moe_ctx;
 typedef struct moe_layer moe_layer;
 typedef struct moe_host_cache moe_host_cache;
+typedef struct moe_expert_store moe_expert_store;
 
 /* Layer shapes. d_model, d_ff and d_ff_shared are multiples of 64 (the
  * quantisation group) and of 32; n_experts <= 1024; 1 <= top_k <= min(32,
@@ -284,6 +287,119 @@ void moe_host_cache_destroy(moe_host_cache* c);
  * offsets [n_experts + 1], perm [n_pairs]. Errors: MOE_EINVAL. */
 moe_status moe_group_pairs(const int32_t* ids, int32_t n_pairs, int32_t n_experts, int32_t* offsets,
                            int32_t* perm);
+
+/* ---- storage tier (expert files) ------------------------------------------ */
+
+/* The tier below the pinned host pool: the pages stream routed experts from
+ * SSD, reading the experts a layer needs with pread while the accelerator
+ * computes ([P1] §2.3 "流式部分", "流水线"; §6.2.2 AsyncExpertReader with
+ * request / wait_all), and their I/O notes ([P1] §9.2) ask for one file per
+ * layer with an [offset, size] per expert (item 2), readahead of the experts
+ * routing history makes likely (item 3), and O_DIRECT (item 4).
+ *
+ * File layout (one file per layer, written by moe_store_write):
+ *   bytes [0, 4096): a header (magic "MOEXPRTS", version 1, the layer's
+ *   moe_shapes, the expert blob size, the stride, the data offset 4096);
+ *   expert e at 4096 + e * stride: the expert's blob as the library's slots
+ *   hold it (the repacked layout; moe_expert_bytes(shapes) bytes), zero padded
+ *   to stride = moe_store_expert_stride(shapes), a multiple of 4096.
+ * A store reads such a file into a host tier of host_slots expert buffers
+ * (4096-aligned; page-locked while a layer streams from it) with `readers`
+ * threads, one pread of `stride` bytes per expert. An expert not in the tier
+ * takes an empty entry, else the least recently used entry that is neither
+ * pinned nor being read. */
+
+/* Bytes between consecutive experts in an expert file (the blob size rounded
+ * up to 4096); 0 if shapes is NULL. */
+size_t moe_store_expert_stride(const moe_shapes* shapes);
+
+/* Write one layer's routed experts (w->gate, w->up, w->down in the canonical
+ * layout of moe_host_weights; the other matrices are not read) to `path`,
+ * replacing the file. Blocking; uses a few host threads.
+ * Errors: MOE_EINVAL (shapes, NULL pointers), MOE_EIO (create/write failed). */
+moe_status moe_store_write(const char* path, const moe_shapes* shapes, const moe_host_weights* w);
+
+#define MOE_STORE_DIRECT 1 /* open with O_DIRECT; plain reads if the file system refuses it */
+
+/* Open an expert file for a layer of these shapes (they must equal the
+ * file's). host_slots in [1, n_experts]; readers in [1, 64]; flags: 0 or
+ * MOE_STORE_DIRECT (moe_store_get_stats reports whether direct I/O is on).
+ * Errors: MOE_EINVAL (arguments, not an expert file, other shapes, short
+ * file), MOE_EIO (open/read failed), MOE_ENOMEM. */
+moe_status moe_store_open(const char* path, const moe_shapes* shapes, int32_t host_slots, int32_t readers,
+                          int32_t flags, moe_expert_store** out);
+
+/* Stop the readers (after the reads already queued) and free the tier.
+ * Errors: MOE_ESTATE if a layer still streams from the store (destroy the
+ * layer first); the store is then left open. */
+moe_status moe_store_close(moe_expert_store* store);
+
+/* The expert's bytes in the host tier (*out points at moe_expert_bytes
+ * bytes), reading them first if needed (blocking). The entry stays pinned
+ * (it is never reused) until a matching moe_store_release.
+ * Errors: MOE_EINVAL, MOE_EBUSY (every entry is pinned), MOE_EIO (the read
+ * failed; the entry is freed, and a later fetch retries). */
+moe_status moe_store_fetch(moe_expert_store* store, int32_t expert, const uint8_t** out);
+moe_status moe_store_release(moe_expert_store* store, int32_t expert); /* MOE_EINVAL if not pinned */
+
+/* Readahead ([P1] §9.2 item 3): queue reads of the listed experts that are
+ * not in the tier, in list order, each into an entry that is neither pinned,
+ * being read, nor read ahead and not yet fetched; stops when no such entry is
+ * left. Does not wait. *queued (may be NULL) receives the number queued. */
+moe_status moe_store_prefetch(moe_expert_store* store, const int32_t* experts, int32_t n, int32_t* queued);
+
+/* Block until no read is queued or running. */
+moe_status moe_store_wait_idle(moe_expert_store* store);
+
+typedef struct {
+    uint64_t fetches;        /* fetches (moe_store_fetch and a streamed layer's misses) that returned
+                                the bytes or a read error (not those refused with MOE_EBUSY) */
+    uint64_t tier_hits;      /* fetches that found the expert in the tier, or being read ahead by a
+                                readahead request (a streamed layer's reads of its own call's misses,
+                                queued before their fetches, are not hits) */
+    uint64_t reads;          /* reads finished (fetch-driven and readahead) */
+    uint64_t prefetch_reads; /* reads queued by readahead requests */
+    uint64_t prefetch_used;  /* experts read ahead that a fetch then used */
+    uint64_t bytes_read;
+    uint64_t read_errors;
+    double read_us;          /* summed duration of the reads (they overlap across readers) */
+    double wait_us;          /* time fetches spent blocked on reads */
+    int32_t direct;          /* 1 if the file is read with O_DIRECT */
+    int32_t host_slots, readers;
+} moe_store_stats;
+
+moe_status moe_store_get_stats(moe_expert_store* store, moe_store_stats* out);
+moe_status moe_store_reset_stats(moe_expert_store* store);
+
+/* The tier's table: per entry the expert it holds (-1 = none) and its state
+ * (0 empty, 1 being read, 2 ready, 3 failed); arrays of host_slots entries,
+ * either may be NULL. */
+moe_status moe_store_tier(moe_expert_store* store, int32_t* entry_expert, int32_t* entry_state);
+
+/* A layer whose routed experts stream from `store` instead of a pinned pool
+ * holding all of them: as moe_layer_create, but no pool is allocated; the
+ * store's tier is page-locked (cudaHostRegister) for the layer's lifetime,
+ * and the store may serve no other layer until this one is destroyed. Each
+ * miss copy first fetches the expert from the store (the call queues the
+ * reads of all its misses at once, then copies each one as its read lands);
+ * the entry is released once its copy has finished. moe_layer_set_weights
+ * then loads the router and the shared expert only (the routed pointers may
+ * be NULL). A read that fails ends the call with MOE_ECOPY, the expert's slot
+ * left empty, as a failed copy does.
+ * Errors: as moe_layer_create, plus MOE_EINVAL (the store's shapes differ, or
+ * it already serves a layer) and MOE_ECUDA (page-locking the tier failed). */
+moe_status moe_layer_create_streamed(moe_ctx* ctx, const moe_shapes* shapes, const moe_quant_layout* layout,
+                                     int32_t cache_slots, int32_t policy, moe_expert_store* store,
+                                     moe_layer** out);
+
+/* Readahead from routing history ([P1] §9.2 item 3, §9.5 item 2): a streamed
+ * layer counts, per expert, the cache steps that routed to it; this queues
+ * reads of up to n experts with the highest counts (ties to the lower id)
+ * that are routed at least once, not in the layer's HBM slots and not in the
+ * store's tier. Meant to be called for layer l+1 while layer l runs. Does not
+ * wait. *queued (may be NULL) receives the number queued.
+ * Errors: MOE_EINVAL (NULL layer, n < 0), MOE_ESTATE (not a streamed layer). */
+moe_status moe_layer_prefetch(moe_layer* layer, int32_t n, int32_t* queued);
 
 /* ---- diagnostics -------------------------------------------------------- */
 

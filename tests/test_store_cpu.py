@@ -1,0 +1,259 @@
+"""The storage tier on the host (no GPU): expert files and the host tier.
+
+* moe_store_write lays a layer's routed experts out as the header says: a
+  4096-byte header, then expert e at 4096 + e * stride, stride = the blob size
+  rounded up to 4096, zero padded; each expert's region holds that expert's
+  scale/bias words at the places the blob layout puts them and exactly that
+  expert's 4-bit codes (as a multiset: the blob permutes nibbles in a word);
+* moe_store_fetch returns the file's bytes (read here independently with
+  numpy), with or without O_DIRECT;
+* the tier reuses the least recently used unpinned entry, never a pinned one
+  (MOE_EBUSY when all are pinned), and readahead fills free entries without
+  evicting experts read ahead and not yet used;
+* failures: wrong shapes, foreign or short files, a read past a file that
+  shrank after opening (MOE_EIO; a later fetch retries);
+* several host threads fetching at once get the right bytes.
+"""
+import os
+import threading
+
+import numpy as np
+import pytest
+
+import expert_streaming_ffn_gb300 as moe
+import synth
+
+# d=512, 8 experts, I=192: the blob (165,888 B) is not a multiple of 4096, so
+# every expert carries padding
+SHAPES = synth.Shapes(512, 8, 2, 192, 512, synth.GELU_TANH)
+ALIGN = 4096
+
+
+@pytest.fixture(scope="module")
+def weights():
+    return synth.layer_weights(SHAPES, 3, 5)
+
+
+@pytest.fixture()
+def expert_file(tmp_path, weights):
+    p = str(tmp_path / "layer3.experts")
+    moe.moe_store_write(p, SHAPES, weights)
+    return p
+
+
+def _region(path, e):
+    stride = moe.moe_store_expert_stride(SHAPES)
+    raw = np.fromfile(path, np.uint8)
+    return raw[ALIGN + e * stride: ALIGN + (e + 1) * stride]
+
+
+def _nibbles(codes):
+    c = np.asarray(codes, np.uint8).reshape(-1)
+    return np.bincount(np.concatenate([c & 15, c >> 4]), minlength=16)
+
+
+def _words(scale, bias):
+    return np.asarray(scale, np.uint32) | (np.asarray(bias, np.uint32) << 16)
+
+
+def test_file_layout_header_and_padding(expert_file):
+    eb = moe.moe_expert_bytes(SHAPES)
+    stride = moe.moe_store_expert_stride(SHAPES)
+    assert eb == synth.expert_bytes(SHAPES) == 165888
+    assert stride == 41 * ALIGN and stride % ALIGN == 0 and stride >= eb
+    raw = np.fromfile(expert_file, np.uint8)
+    assert raw.size == ALIGN + SHAPES.n_experts * stride
+    assert bytes(raw[:8]) == b"MOEXPRTS"
+    hdr = raw[:ALIGN]
+    assert int(hdr[8:12].view(np.uint32)[0]) == 1 and int(hdr[12:16].view(np.uint32)[0]) == ALIGN
+    shp = hdr[16:40].view(np.int32)
+    assert list(shp) == [SHAPES.d_model, SHAPES.n_experts, SHAPES.top_k, SHAPES.d_ff, SHAPES.d_ff_shared,
+                         SHAPES.act]
+    assert list(hdr[48:72].view(np.uint64)) == [eb, stride, ALIGN]
+    for e in range(SHAPES.n_experts):
+        assert not _region(expert_file, e)[eb:].any(), "padding must be zero"
+
+
+def test_each_region_holds_its_expert(expert_file, weights):
+    d, I = SHAPES.d_model, SHAPES.d_ff
+    gu = I * d // 2 + I * d // 16  # one gate or up matrix
+    for e in range(SHAPES.n_experts):
+        r = _region(expert_file, e)
+        (gc, gs, gb), (uc, us, ub), (dc, ds, db) = weights.expert(e)
+        for m, (c, s, b) in enumerate([(gc, gs, gb), (uc, us, ub)]):
+            # records of 1152 bytes per (32-row tile, group of 64): 32 lanes x
+            # 2 chunks x 16 code bytes, then one scale|bias word per lane
+            rec = r[m * gu:(m + 1) * gu].reshape(I // 32, d // 64, 1152)
+            words = rec[:, :, 1024:].copy().view(np.uint32)  # [rt][g][lane]
+            want = _words(s, b).reshape(I // 32, 32, d // 64).transpose(0, 2, 1)
+            assert (words == want).all(), (e, m)
+            assert (_nibbles(rec[:, :, :1024]) == _nibbles(c)).all(), (e, m)
+        # down, column-sliced: all codes first, then the words as 128-byte
+        # blocks ordered by (group, row tile)
+        dn = r[2 * gu:2 * gu + d * I // 2 + d * I // 16]
+        words = dn[d * I // 2:].copy().view(np.uint32).reshape(I // 64, d // 32, 32)
+        want = _words(ds, db).reshape(d // 32, 32, I // 64).transpose(2, 0, 1)
+        assert (words == want).all(), e
+        assert (_nibbles(dn[:d * I // 2]) == _nibbles(dc)).all(), e
+
+
+@pytest.mark.parametrize("flags", [0, moe.MOE_STORE_DIRECT])
+def test_fetch_returns_the_files_bytes(expert_file, flags):
+    eb = moe.moe_expert_bytes(SHAPES)
+    st = moe.moe_store_open(expert_file, SHAPES, 3, 2, flags)
+    try:
+        for e in [5, 0, 7, 5, 2]:
+            got = moe.moe_store_fetch(st, e, eb)
+            assert (got == _region(expert_file, e)[:eb]).all(), e
+            moe.moe_store_release(st, e)
+        s = moe.moe_store_get_stats(st)
+        assert s["fetches"] == 5 and s["tier_hits"] == 1 and s["reads"] == 4
+        assert s["bytes_read"] == 4 * moe.moe_store_expert_stride(SHAPES)
+        assert s["direct"] in (0, 1) and (flags or s["direct"] == 0)
+    finally:
+        moe.moe_store_close(st)
+
+
+def test_tier_reuses_least_recently_used_unpinned_entry(expert_file):
+    eb = moe.moe_expert_bytes(SHAPES)
+    st = moe.moe_store_open(expert_file, SHAPES, 2, 1)
+    try:
+        def use(e):
+            moe.moe_store_fetch(st, e, eb)
+            moe.moe_store_release(st, e)
+
+        for e in (0, 1, 0):
+            use(e)
+        use(2)  # evicts 1, the least recently used
+        ex, state = moe.moe_store_tier(st, 2)
+        assert sorted(ex) == [0, 2] and (state == 2).all()
+        use(0)
+        assert moe.moe_store_get_stats(st)["reads"] == 3
+        use(1)  # read again; evicts 2
+        assert moe.moe_store_get_stats(st)["reads"] == 4
+        assert sorted(moe.moe_store_tier(st, 2)[0]) == [0, 1]
+    finally:
+        moe.moe_store_close(st)
+
+
+def test_pinned_entries_are_never_reused(expert_file):
+    eb = moe.moe_expert_bytes(SHAPES)
+    st = moe.moe_store_open(expert_file, SHAPES, 2, 2)
+    try:
+        a = moe.moe_store_fetch(st, 3, eb)
+        moe.moe_store_fetch(st, 4, eb)
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_store_fetch(st, 5, eb)
+        assert ei.value.status == moe.MOE_EBUSY
+        # a fetch of a pinned expert pins it again and succeeds
+        assert (moe.moe_store_fetch(st, 3, eb) == a).all()
+        moe.moe_store_release(st, 3)
+        moe.moe_store_release(st, 3)
+        assert (moe.moe_store_fetch(st, 5, eb) == _region(expert_file, 5)[:eb]).all()
+        assert sorted(moe.moe_store_tier(st, 2)[0]) == [4, 5]
+        with pytest.raises(moe.MoeError):
+            moe.moe_store_release(st, 3)  # no longer in the tier
+        moe.moe_store_release(st, 4)
+        moe.moe_store_release(st, 5)
+    finally:
+        moe.moe_store_close(st)
+
+
+def test_readahead_fills_free_entries_and_keeps_unused_ones(expert_file):
+    eb = moe.moe_expert_bytes(SHAPES)
+    st = moe.moe_store_open(expert_file, SHAPES, 3, 2)
+    try:
+        assert moe.moe_store_prefetch(st, [6, 1]) == 2
+        assert moe.moe_store_prefetch(st, [6]) == 0  # already there
+        moe.moe_store_wait_idle(st)
+        ex, state = moe.moe_store_tier(st, 3)
+        assert sorted(ex[state == 2]) == [1, 6]
+        # the third entry is free; a fourth expert would have to evict an
+        # expert read ahead and not yet used, which readahead never does
+        assert moe.moe_store_prefetch(st, [2, 3]) == 1
+        moe.moe_store_wait_idle(st)
+        assert (moe.moe_store_fetch(st, 6, eb) == _region(expert_file, 6)[:eb]).all()
+        moe.moe_store_release(st, 6)
+        s = moe.moe_store_get_stats(st)
+        assert s["prefetch_reads"] == 3 and s["prefetch_used"] == 1 and s["tier_hits"] == 1
+        # 6 has been used, so it may now make room
+        assert moe.moe_store_prefetch(st, [3]) == 1
+        moe.moe_store_wait_idle(st)
+        assert sorted(moe.moe_store_tier(st, 3)[0]) == [1, 2, 3]
+    finally:
+        moe.moe_store_close(st)
+
+
+def test_open_rejects_bad_files_and_arguments(tmp_path, expert_file):
+    other = synth.Shapes(512, 8, 2, 256, 512, synth.GELU_TANH)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_store_open(expert_file, other, 2, 1)
+    assert ei.value.status == moe.MOE_EINVAL
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_store_open(str(tmp_path / "absent"), SHAPES, 2, 1)
+    assert ei.value.status == moe.MOE_EIO
+    junk = tmp_path / "junk"
+    junk.write_bytes(b"\0" * 8192)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_store_open(str(junk), SHAPES, 2, 1)
+    assert ei.value.status == moe.MOE_EINVAL
+    short = tmp_path / "short"
+    short.write_bytes(open(expert_file, "rb").read()[:-1])
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_store_open(str(short), SHAPES, 2, 1)
+    assert ei.value.status == moe.MOE_EINVAL
+    for slots, readers, flags in [(0, 1, 0), (9, 1, 0), (2, 0, 0), (2, 65, 0), (2, 1, 2)]:
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_store_open(expert_file, SHAPES, slots, readers, flags)
+        assert ei.value.status == moe.MOE_EINVAL
+
+
+def test_read_failure_is_reported_and_retried(tmp_path, weights):
+    p = str(tmp_path / "shrinks.experts")
+    moe.moe_store_write(p, SHAPES, weights)
+    eb = moe.moe_expert_bytes(SHAPES)
+    stride = moe.moe_store_expert_stride(SHAPES)
+    st = moe.moe_store_open(p, SHAPES, 2, 1)
+    try:
+        os.truncate(p, ALIGN + 4 * stride)  # experts 4..7 are gone
+        assert (moe.moe_store_fetch(st, 3, eb) == np.fromfile(p, np.uint8)[ALIGN + 3 * stride:][:eb]).all()
+        moe.moe_store_release(st, 3)
+        for _ in range(2):  # the failed entry is freed; the next fetch reads again
+            with pytest.raises(moe.MoeError) as ei:
+                moe.moe_store_fetch(st, 6, eb)
+            assert ei.value.status == moe.MOE_EIO
+        s = moe.moe_store_get_stats(st)
+        assert s["read_errors"] == 2 and s["reads"] == 3
+        assert 6 not in moe.moe_store_tier(st, 2)[0]
+    finally:
+        moe.moe_store_close(st)
+
+
+def test_concurrent_fetches_get_their_bytes(expert_file):
+    eb = moe.moe_expert_bytes(SHAPES)
+    want = [_region(expert_file, e)[:eb] for e in range(SHAPES.n_experts)]
+    st = moe.moe_store_open(expert_file, SHAPES, 4, 3)
+    errors = []
+
+    def worker(seed):
+        rng = np.random.default_rng(seed)
+        try:
+            for e in rng.integers(0, SHAPES.n_experts, 40):
+                got = moe.moe_store_fetch(st, int(e), eb)
+                if not (got == want[e]).all():
+                    errors.append(int(e))
+                moe.moe_store_release(st, int(e))
+        except Exception as ex:  # noqa: BLE001
+            errors.append(repr(ex))
+
+    try:
+        th = [threading.Thread(target=worker, args=(i,)) for i in range(4)]
+        for t in th:
+            t.start()
+        for t in th:
+            t.join()
+        assert not errors, errors
+        s = moe.moe_store_get_stats(st)
+        assert s["fetches"] == 160 and s["read_errors"] == 0
+    finally:
+        moe.moe_store_close(st)
