@@ -520,11 +520,12 @@ moe_status pin_until_copied(moe_layer* L, std::vector<int> experts) {
 
 // issue_miss_copies for a layer that streams from an expert store: the same
 // destinations, flags, parts and failure handling, but each expert's source
-// is its entry in the store's host tier. The reads of every miss are queued
-// first (as many as the tier has free entries), then each copy is issued as
-// soon as its read lands, so reads, copies and the kernels waiting on the
-// flags overlap. An entry stays pinned until its last copy has finished.
-// Nothing is merged: tier entries are not consecutive experts.
+// is its entry in the store's host tier. Misses already in the tier are
+// copied first; the reads of the others are queued at once (as many as the
+// tier has entries to give), and each copy is issued as soon as its read
+// lands, so reads, copies and the kernels waiting on the flags overlap. An
+// entry stays pinned until its last copy has finished. Nothing is merged:
+// tier entries are not consecutive experts.
 moe_status issue_store_copies(moe_layer* L, const StepResult& r, bool with_bypass, uint32_t epoch,
                               std::vector<MissFlags>* ready_of_miss, bool split) {
     moe_ctx* C = L->ctx;
@@ -543,15 +544,17 @@ moe_status issue_store_copies(moe_layer* L, const StepResult& r, bool with_bypas
         const uint8_t* src;
     };
     std::vector<Copy> copies;
-    std::vector<int32_t> wanted;
     int nb = 0;
     for (size_t i = 0; i < r.miss_experts.size(); ++i) {
         const int slot = r.miss_slots[i];
         if (slot < 0 && !with_bypass) continue;
         uint8_t* dst = slot >= 0 ? L->d_slots + (size_t)slot * L->ebytes : C->staging + (size_t)(nb++) * L->ebytes;
         copies.push_back(Copy{i, dst, nullptr});
-        wanted.push_back(r.miss_experts[i]);
     }
+    std::stable_partition(copies.begin(), copies.end(),
+                          [&](const Copy& c) { return store_ready(L->store, r.miss_experts[c.i]); });
+    std::vector<int32_t> wanted;
+    for (const Copy& c : copies) wanted.push_back(r.miss_experts[c.i]);
     store_readahead(L->store, wanted.data(), (int)wanted.size(), false);
     const bool flags = ready_of_miss != nullptr;
     // a split copy reads its entry twice, so every entry of the call stays
@@ -564,14 +567,18 @@ moe_status issue_store_copies(moe_layer* L, const StepResult& r, bool with_bypas
                                cudaMemcpyHostToDevice, C->copy_stream);
     };
     std::vector<int> held;  // entries fetched but not yet behind a recorded event
+    int cur_part = 0;
     auto fail_from = [&](size_t k, moe_status code, const char* why) {
-        for (size_t j = copies[k].i; j < r.miss_experts.size(); ++j)
-            if (r.miss_slots[j] >= 0) L->cache.evict(r.miss_slots[j]);
+        // the copies not known good: from k on, or all of them while the
+        // first part of a split copy is still being issued (none has its down bytes)
+        for (size_t j = split && cur_part == 0 ? 0 : k; j < copies.size(); ++j)
+            if (r.miss_slots[copies[j].i] >= 0) L->cache.evict(r.miss_slots[copies[j].i]);
         pin_until_copied(L, held);  // the copies already issued may still read them
         return set_error(code, "copy of expert %d (slot %d) failed: %s", r.miss_experts[copies[k].i],
                          r.miss_slots[copies[k].i], why);
     };
     for (int part = 0; part < parts; ++part) {
+        cur_part = part;
         const size_t off = part == 0 ? 0 : gu_bytes;
         const size_t len = !split ? L->ebytes : part == 0 ? gu_bytes : L->ebytes - gu_bytes;
         for (size_t k = 0; k < copies.size(); ++k) {
@@ -664,9 +671,13 @@ moe_status issue_miss_copies(moe_layer* L, const StepResult& r, bool with_bypass
         return cudaMemcpyAsync(L->d_ready + flag, L->h_epochs + epoch % kEpochRing, sizeof(uint32_t),
                                cudaMemcpyHostToDevice, C->copy_stream);
     };
+    int cur_part = 0;
     auto fail_from = [&](size_t k, cudaError_t ce, bool injected) {
         if (!injected) cudaGetLastError();
-        for (size_t j = copies[k].i; j < r.miss_experts.size(); ++j)
+        // the copies not known good: from k on, or all of them while the first
+        // part of a split copy is still being issued (none has its down bytes)
+        const size_t first = split && flags && cur_part == 0 ? 0 : copies[k].i;
+        for (size_t j = first; j < r.miss_experts.size(); ++j)
             if (r.miss_slots[j] >= 0) L->cache.evict(r.miss_slots[j]);
         return set_error(MOE_ECOPY, "copy of expert %d (slot %d) failed: %s", r.miss_experts[copies[k].i],
                          r.miss_slots[copies[k].i], injected ? "injected failure" : cudaGetErrorString(ce));
@@ -680,6 +691,7 @@ moe_status issue_miss_copies(moe_layer* L, const StepResult& r, bool with_bypass
     // failure armed, which names one expert's copy.
     const bool merge = !split && C->fail_copy_at < 0;
     for (int part = 0; part < parts; ++part) {
+        cur_part = part;
         const size_t off = part == 0 ? 0 : gu_bytes;
         const size_t len = !split ? L->ebytes : part == 0 ? gu_bytes : L->ebytes - gu_bytes;
         for (size_t k = 0; k < copies.size();) {

@@ -42,12 +42,16 @@ moe_status check_shapes(const moe_shapes* s);
 // returns the expert's bytes (reading them first if needed) and pins its
 // entry; store_release unpins it. store_readahead queues reads for experts not
 // in the tier, into entries nobody pins (never taking an entry read ahead and
-// not yet fetched); it returns how many it queued.
+// not yet fetched); with predicted (a guess from history) only into entries
+// whose experts were fetched no more often, behind every fetch's read; without
+// it (the reads of a call's own misses) never displacing an expert of the
+// list. It returns how many it queued.
 
 moe_status store_acquire(moe_expert_store* s, int expert, const uint8_t** out);
 moe_status store_release(moe_expert_store* s, int expert);
 int store_readahead(moe_expert_store* s, const int32_t* experts, int n, bool predicted);
-bool store_contains(moe_expert_store* s, int expert);
+bool store_contains(moe_expert_store* s, int expert);  // ready or being read
+bool store_ready(moe_expert_store* s, int expert);
 uint8_t* store_buffer(moe_expert_store* s, size_t* bytes);
 int store_host_slots(const moe_expert_store* s);
 const moe_shapes& store_shapes(const moe_expert_store* s);

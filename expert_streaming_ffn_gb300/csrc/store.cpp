@@ -21,9 +21,13 @@
 // 4096-aligned buffer, which O_DIRECT requires.
 //
 // The host tier is H entries of `stride` bytes. An entry is empty, being
-// read, ready, or failed. A fetch of an expert that is not in the tier takes
-// an empty entry, else the least recently used ready entry that nobody pins
-// (entries being read are never taken), and queues its read. A fetch that
+// read, ready, or failed. The store counts every expert's fetches (its
+// history, kept across evictions). A fetch of an expert that is not in the
+// tier takes an empty entry, else, among the entries nobody pins and nobody
+// is reading, the one whose expert has the fewest fetches (ties: the least
+// recently used), and queues its read. Readahead takes an entry only if its
+// expert has no more fetches than the expert read ahead, never one read ahead
+// and not yet fetched, and its reads wait behind every read a fetch needs. A fetch that
 // finds a failed read it did not ask for (readahead's) reads once more; a
 // read that fails for the fetch that asked for it is reported (MOE_EIO) and
 // its entry freed. A fetched entry
@@ -101,7 +105,10 @@ struct moe_expert_store {
     std::vector<int> where;  // expert -> entry, -1 if not in the tier
     std::mutex mu;
     std::condition_variable cv_job, cv_done;
-    std::deque<int> jobs;  // entries to read, in request order
+    std::deque<int> jobs;     // entries to read for fetches, in request order
+    std::deque<int> jobs_ra;  // entries to read ahead, taken only when `jobs` is empty
+    std::vector<uint32_t> freq;  // fetches per expert
+    std::vector<uint8_t> keep;   // experts whose entries must not be taken (during one readahead call)
     std::vector<std::thread> readers;
     bool stop = false;
     uint64_t tick = 0;
@@ -118,10 +125,11 @@ void reader_loop(moe_expert_store* s) {
         int e;
         {
             std::unique_lock<std::mutex> lk(s->mu);
-            s->cv_job.wait(lk, [&] { return s->stop || !s->jobs.empty(); });
-            if (s->jobs.empty()) return;  // stop, and nothing left to read
-            i = s->jobs.front();
-            s->jobs.pop_front();
+            s->cv_job.wait(lk, [&] { return s->stop || !s->jobs.empty() || !s->jobs_ra.empty(); });
+            std::deque<int>& q = !s->jobs.empty() ? s->jobs : s->jobs_ra;
+            if (q.empty()) return;  // stop, and nothing left to read
+            i = q.front();
+            q.pop_front();
             e = s->ent[(size_t)i].expert;
         }
         uint8_t* dst = s->buf + (size_t)i * s->stride;
@@ -157,18 +165,30 @@ void reader_loop(moe_expert_store* s) {
     }
 }
 
-// An entry to (re)use: the lowest empty one, else the least recently used
-// ready or failed entry that nobody pins; with keep_predicted, entries read
-// ahead and not yet fetched are kept. -1 if none. Caller holds the mutex.
-int pick_entry(const moe_expert_store* s, bool keep_predicted) {
+// An entry to (re)use: the lowest empty one, else, among the ready or failed
+// entries nobody pins, the one whose expert has the fewest fetches, ties to
+// the least recently used. For readahead of expert `ahead` (>= 0), entries
+// read ahead and not yet fetched are kept, and an entry whose expert has more
+// fetches than `ahead` is not taken; with keep_predicted, entries read ahead
+// and not yet fetched are kept too. Entries of experts marked in `keep` are
+// never taken. -1 if none. Caller holds the mutex.
+int pick_entry(const moe_expert_store* s, int ahead, bool keep_predicted) {
     int best = -1;
     for (int i = 0; i < s->H; ++i) {
         const Entry& en = s->ent[(size_t)i];
         if (en.state == kEmpty) return i;
         if (en.state == kReading || en.pins > 0) continue;
-        if (keep_predicted && en.predicted) continue;
-        if (best < 0 || en.used < s->ent[(size_t)best].used) best = i;
+        if ((ahead >= 0 || keep_predicted) && en.predicted) continue;
+        if (s->keep[(size_t)en.expert]) continue;
+        if (best < 0) {
+            best = i;
+            continue;
+        }
+        const Entry& b = s->ent[(size_t)best];
+        const uint32_t fi = s->freq[(size_t)en.expert], fb = s->freq[(size_t)b.expert];
+        if (fi < fb || (fi == fb && en.used < b.used)) best = i;
     }
+    if (best >= 0 && ahead >= 0 && s->freq[(size_t)s->ent[(size_t)best].expert] > s->freq[(size_t)ahead]) return -1;
     return best;
 }
 
@@ -184,7 +204,7 @@ void assign(moe_expert_store* s, int i, int e, bool predicted) {
     en.demand = !predicted;
     en.err = 0;
     s->where[(size_t)e] = i;
-    s->jobs.push_back(i);
+    (predicted ? s->jobs_ra : s->jobs).push_back(i);
     s->cv_job.notify_one();
 }
 
@@ -210,6 +230,7 @@ moe_status store_acquire(moe_expert_store* s, int e, const uint8_t** out) {
                 en.demand = false;
                 en.pins += 1;
                 s->st.fetches += 1;
+                s->freq[(size_t)e] += 1;
                 en.used = ++s->tick;
                 *out = s->buf + (size_t)i * s->stride;
                 return MOE_OK;
@@ -218,6 +239,7 @@ moe_status store_acquire(moe_expert_store* s, int e, const uint8_t** out) {
                 // a read queued earlier (readahead) failed: read again for this fetch
                 en.state = kReading;
                 en.err = 0;
+                en.predicted = false;
                 s->jobs.push_back(i);
                 s->cv_job.notify_one();
                 queued = true;
@@ -238,7 +260,7 @@ moe_status store_acquire(moe_expert_store* s, int e, const uint8_t** out) {
             s->st.wait_us += us_between(t0, std::chrono::steady_clock::now());
             continue;
         }
-        const int v = pick_entry(s, false);
+        const int v = pick_entry(s, -1, false);
         if (v >= 0) {
             assign(s, v, e, false);
             queued = true;
@@ -265,16 +287,33 @@ moe_status store_release(moe_expert_store* s, int e) {
 int store_readahead(moe_expert_store* s, const int32_t* experts, int n, bool predicted) {
     std::lock_guard<std::mutex> g(s->mu);
     int queued = 0;
+    // reads for fetches that follow must not displace one another (or an
+    // expert of the list already in the tier)
+    if (!predicted)
+        for (int j = 0; j < n; ++j)
+            if (experts[j] >= 0 && experts[j] < s->E) s->keep[(size_t)experts[j]] = 1;
     for (int j = 0; j < n; ++j) {
         const int e = experts[j];
         if (e < 0 || e >= s->E || s->where[(size_t)e] >= 0) continue;
-        const int v = pick_entry(s, true);
-        if (v < 0) break;
+        const int v = pick_entry(s, predicted ? e : -1, true);
+        if (v < 0) {
+            if (predicted) continue;  // the next expert may still find an entry it is worth
+            break;
+        }
         assign(s, v, e, predicted);
         ++queued;
     }
+    if (!predicted)
+        for (int j = 0; j < n; ++j)
+            if (experts[j] >= 0 && experts[j] < s->E) s->keep[(size_t)experts[j]] = 0;
     if (predicted) s->st.prefetch_reads += (uint64_t)queued;
     return queued;
+}
+
+bool store_ready(moe_expert_store* s, int e) {
+    std::lock_guard<std::mutex> g(s->mu);
+    const int i = s->where[(size_t)e];
+    return i >= 0 && s->ent[(size_t)i].state == kReady;
 }
 
 bool store_contains(moe_expert_store* s, int e) {
@@ -415,6 +454,8 @@ extern "C" moe_status moe_store_open(const char* path, const moe_shapes* s, int3
     S->buf = (uint8_t*)buf;
     S->ent.assign((size_t)host_slots, Entry{});
     S->where.assign((size_t)s->n_experts, -1);
+    S->freq.assign((size_t)s->n_experts, 0);
+    S->keep.assign((size_t)s->n_experts, 0);
     S->st.direct = direct ? 1 : 0;
     S->st.host_slots = host_slots;
     S->st.readers = readers;
@@ -465,7 +506,7 @@ extern "C" moe_status moe_store_prefetch(moe_expert_store* S, const int32_t* exp
 extern "C" moe_status moe_store_wait_idle(moe_expert_store* S) {
     if (!S) return set_error(MOE_EINVAL, "moe_store_wait_idle: store is NULL");
     std::unique_lock<std::mutex> lk(S->mu);
-    S->cv_done.wait(lk, [&] { return S->jobs.empty() && !any_reading(S); });
+    S->cv_done.wait(lk, [&] { return S->jobs.empty() && S->jobs_ra.empty() && !any_reading(S); });
     return MOE_OK;
 }
 

@@ -7,9 +7,10 @@
   expert's 4-bit codes (as a multiset: the blob permutes nibbles in a word);
 * moe_store_fetch returns the file's bytes (read here independently with
   numpy), with or without O_DIRECT;
-* the tier reuses the least recently used unpinned entry, never a pinned one
-  (MOE_EBUSY when all are pinned), and readahead fills free entries without
-  evicting experts read ahead and not yet used;
+* the tier reuses the unpinned entry whose expert was fetched least often
+  (ties: least recently used), never a pinned one (MOE_EBUSY when all are
+  pinned); readahead fills free entries, never evicts an expert read ahead
+  and not yet used, and displaces only experts fetched no more often;
 * failures: wrong shapes, foreign or short files, a read past a file that
   shrank after opening (MOE_EIO; a later fetch retries);
 * several host threads fetching at once get the right bytes.
@@ -114,7 +115,7 @@ def test_fetch_returns_the_files_bytes(expert_file, flags):
         moe.moe_store_close(st)
 
 
-def test_tier_reuses_least_recently_used_unpinned_entry(expert_file):
+def test_tier_evicts_the_least_fetched_then_least_recent_entry(expert_file):
     eb = moe.moe_expert_bytes(SHAPES)
     st = moe.moe_store_open(expert_file, SHAPES, 2, 1)
     try:
@@ -122,16 +123,21 @@ def test_tier_reuses_least_recently_used_unpinned_entry(expert_file):
             moe.moe_store_fetch(st, e, eb)
             moe.moe_store_release(st, e)
 
-        for e in (0, 1, 0):
+        def tier():
+            return sorted(moe.moe_store_tier(st, 2)[0].tolist())
+
+        for e in (0, 0, 0, 1):  # 0 fetched 3 times, 1 once (and more recently)
             use(e)
-        use(2)  # evicts 1, the least recently used
-        ex, state = moe.moe_store_tier(st, 2)
-        assert sorted(ex) == [0, 2] and (state == 2).all()
-        use(0)
+        use(2)  # evicts 1, the fewest fetches, though 0 was used less recently
+        assert tier() == [0, 2]
+        use(0)  # 0: four fetches
         assert moe.moe_store_get_stats(st)["reads"] == 3
-        use(1)  # read again; evicts 2
-        assert moe.moe_store_get_stats(st)["reads"] == 4
-        assert sorted(moe.moe_store_tier(st, 2)[0]) == [0, 1]
+        for e in (2, 2, 2):  # 2 now has four fetches too, and is the more recent
+            use(e)
+        use(4)  # a tie on fetches: the least recently used goes
+        assert tier() == [2, 4]
+        s = moe.moe_store_get_stats(st)
+        assert s["reads"] == 4 and s["fetches"] == 10 and s["tier_hits"] == 6
     finally:
         moe.moe_store_close(st)
 
@@ -176,10 +182,36 @@ def test_readahead_fills_free_entries_and_keeps_unused_ones(expert_file):
         moe.moe_store_release(st, 6)
         s = moe.moe_store_get_stats(st)
         assert s["prefetch_reads"] == 3 and s["prefetch_used"] == 1 and s["tier_hits"] == 1
-        # 6 has been used, so it may now make room
-        assert moe.moe_store_prefetch(st, [3]) == 1
+        # 6 has been used, but fetched once: 3 (never fetched) may not displace it
+        assert moe.moe_store_prefetch(st, [3]) == 0
+    finally:
+        moe.moe_store_close(st)
+
+
+def test_readahead_only_displaces_experts_fetched_no_more_often(expert_file):
+    eb = moe.moe_expert_bytes(SHAPES)
+    st = moe.moe_store_open(expert_file, SHAPES, 2, 1)
+    try:
+        def use(e):
+            moe.moe_store_fetch(st, e, eb)
+            moe.moe_store_release(st, e)
+
+        def tier():
+            return sorted(moe.moe_store_tier(st, 2)[0].tolist())
+
+        for e in (0, 1, 1):  # fetches: 0 once, 1 twice
+            use(e)
+        assert moe.moe_store_prefetch(st, [2]) == 0  # 2 has no fetches; 0 has one
+        for e in (2, 2):  # a fetch may displace 0; then 2 has two fetches
+            use(e)
+        assert tier() == [1, 2]
+        assert moe.moe_store_prefetch(st, [0]) == 0  # 0 has one fetch, the others two
+        use(0)  # 1 and 2 tie at two fetches: 1, the least recent, goes
+        assert tier() == [0, 2]
+        assert moe.moe_store_prefetch(st, [1]) == 1  # 1 (two fetches) may displace 2 (two)
         moe.moe_store_wait_idle(st)
-        assert sorted(moe.moe_store_tier(st, 3)[0]) == [1, 2, 3]
+        assert tier() == [0, 1]
+        assert moe.moe_store_get_stats(st)["prefetch_reads"] == 1
     finally:
         moe.moe_store_close(st)
 
