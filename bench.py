@@ -419,7 +419,7 @@ def run_ours(args, world, rank, local):
         prefill = run_prefill(args, ctx, dev, stream, seed)
 
     storage = None
-    if not args.no_storage and args.storage_layers > 0:
+    if not args.no_storage and args.storage_layers > 0 and world == 1:
         try:
             storage = run_storage(args, ctx, dev, stream, seed)
             storage["pinned_pool_ms_per_layer_token"] = ms_max / args.steps / n_layers
