@@ -129,31 +129,36 @@ def test_tiny_degenerate_caches_and_top_k(ctx, slots, k):
 
 
 def test_decode_2816_two_layers(ctx):
+    """decode_2816: layer 0 for all 64 decode steps of the workload (ids,
+    gates and the cache table checked at every step, y at the first, a middle
+    and the last), and layer 17 for 8 steps."""
     s = synth.SHAPES_2816
     wl = synth.WORKLOADS["decode_2816"]
-    for layer in (0, 17):
+    for layer, steps in ((0, wl.steps), (17, 8)):
         r = Rig(ctx, s, layer, wl.cache_slots)
         zb = synth.zipf_bias(s, layer, wl.zipf_s)
         try:
-            for step in range(8):
+            for step in range(steps):
                 x = synth.tokens(s, layer, step, 1, True)
-                r.forward(x, zb, check_y=step in (0, 7))
+                r.forward(x, zb, check_y=step in (0, steps // 2, steps - 1))
             st = moe.moe_layer_stats(r.h)
-            assert st["hits"] > 0 and st["misses"] > 0
+            assert st["steps"] == steps and st["hits"] > 0 and st["misses"] > 0
         finally:
             r.close()
 
 
-@pytest.mark.parametrize("T,policy", [(1, moe.LFU), (8, moe.LRU)])
+@pytest.mark.parametrize("policy", [moe.LFU, moe.LRU])
+@pytest.mark.parametrize("T", [1, 8])
 def test_decode_2048_silu(ctx, T, policy):
+    """decode_2048 (SiLU, 64 slots) at batches 1 and 8 under both policies."""
     s = synth.SHAPES_2048
     wl = synth.WORKLOADS["decode_2048"]
     r = Rig(ctx, s, 3, wl.cache_slots, policy)
     zb = synth.zipf_bias(s, 3, wl.zipf_s)
     try:
-        for step in range(5):
+        for step in range(12):
             x = synth.tokens(s, 3, step, T, True)
-            r.forward(x, zb, check_y=step == 4, y_tokens=[0, T - 1])
+            r.forward(x, zb, check_y=step in (0, 11), y_tokens=[0, T - 1])
     finally:
         r.close()
 
@@ -166,6 +171,23 @@ def test_prefill_chunk_2816(ctx):
         r.forward(x, None, y_tokens=[0, 61, 127])
         st = moe.moe_layer_stats(r.h)
         assert st["bypass"] > 0  # a 128-token chunk touches far more than 16 experts
+    finally:
+        r.close()
+
+
+@pytest.mark.parametrize("layer", [0, 1, 29])
+def test_prefill_prompt_as_chunks_2816(ctx, layer):
+    """prefill_2816: the 1024-token prompt as 8 chunks of 128 through a fresh
+    16-slot cache, uniform routing; ids, gates and the cache table after every
+    chunk, y on tokens of the first and the last chunk."""
+    s = synth.SHAPES_2816
+    wl = synth.WORKLOADS["prefill_2816"]
+    r = Rig(ctx, s, layer, wl.cache_slots)
+    try:
+        x = synth.tokens(s, layer, 0, wl.tokens * wl.steps, True)
+        r.forward(x, None, y_tokens=[0, 127, 896, 1023])
+        st = moe.moe_layer_stats(r.h)
+        assert st["steps"] == wl.steps and st["bypass"] > 0
     finally:
         r.close()
 
