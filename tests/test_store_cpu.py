@@ -289,3 +289,113 @@ def test_concurrent_fetches_get_their_bytes(expert_file):
         assert s["fetches"] == 160 and s["read_errors"] == 0
     finally:
         moe.moe_store_close(st)
+
+
+class _TierModel:
+    """The host tier's rules restated on their own: fetch counts per expert;
+    a fetch takes an empty entry, else the unpinned entry whose expert has the
+    fewest fetches (ties: least recently used); readahead also keeps entries
+    read ahead and not yet fetched, and takes an entry only if its expert has
+    no more fetches than the one read ahead. Reads finish at once here (the
+    test waits for the store's readers after every request)."""
+
+    def __init__(self, H, E):
+        self.ent = [{"e": -1, "pins": 0, "used": 0, "pred": False} for _ in range(H)]
+        self.freq = [0] * E
+        self.tick = 0
+        self.stats = dict(fetches=0, tier_hits=0, reads=0, prefetch_reads=0, prefetch_used=0)
+
+    def _where(self, e):
+        return next((i for i, x in enumerate(self.ent) if x["e"] == e), None)
+
+    def _pick(self, ahead=None):
+        for i, x in enumerate(self.ent):
+            if x["e"] < 0:
+                return i
+        ok = [i for i, x in enumerate(self.ent) if x["pins"] == 0 and not (ahead is not None and x["pred"])]
+        if not ok:
+            return None
+        best = min(ok, key=lambda i: (self.freq[self.ent[i]["e"]], self.ent[i]["used"]))
+        if ahead is not None and self.freq[self.ent[best]["e"]] > self.freq[ahead]:
+            return None
+        return best
+
+    def _assign(self, i, e, pred):
+        self.tick += 1
+        self.ent[i] = {"e": e, "pins": 0, "used": self.tick, "pred": pred}
+        self.stats["reads"] += 1
+
+    def fetch(self, e):
+        i = self._where(e)
+        hit = i is not None
+        if not hit:
+            i = self._pick()
+            if i is None:
+                return False  # every entry pinned
+            self._assign(i, e, False)
+        x = self.ent[i]
+        self.stats["tier_hits"] += hit
+        self.stats["prefetch_used"] += x["pred"]
+        x["pred"] = False
+        x["pins"] += 1
+        self.tick += 1
+        x["used"] = self.tick
+        self.freq[e] += 1
+        self.stats["fetches"] += 1
+        return True
+
+    def release(self, e):
+        self.ent[self._where(e)]["pins"] -= 1
+
+    def prefetch(self, experts):
+        q = 0
+        for e in experts:
+            if self._where(e) is not None:
+                continue
+            i = self._pick(ahead=e)
+            if i is None:
+                continue
+            self._assign(i, e, True)
+            q += 1
+        self.stats["prefetch_reads"] += q
+        return q
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+def test_tier_follows_its_rules_on_random_requests(expert_file, seed):
+    H, E = 3, SHAPES.n_experts
+    eb = moe.moe_expert_bytes(SHAPES)
+    want = [_region(expert_file, e)[:eb] for e in range(E)]
+    rng = np.random.default_rng(seed)
+    st = moe.moe_store_open(expert_file, SHAPES, H, 2)
+    model = _TierModel(H, E)
+    held = []
+    try:
+        for step in range(300):
+            op = rng.random()
+            if op < 0.45:
+                e = int(rng.integers(0, E))
+                ok = model.fetch(e)
+                try:
+                    got = moe.moe_store_fetch(st, e, eb)
+                    assert ok and (got == want[e]).all(), (step, e)
+                    held.append(e)
+                except moe.MoeError as ex:
+                    assert not ok and ex.status == moe.MOE_EBUSY, (step, e)
+            elif op < 0.8 and held:
+                e = held.pop(int(rng.integers(0, len(held))))
+                model.release(e)
+                moe.moe_store_release(st, e)
+            else:
+                ask = [int(v) for v in rng.integers(0, E, int(rng.integers(1, 4)))]
+                assert moe.moe_store_prefetch(st, ask) == model.prefetch(ask), (step, ask)
+                moe.moe_store_wait_idle(st)
+            ex, state = moe.moe_store_tier(st, H)
+            assert ex.tolist() == [x["e"] for x in model.ent], (step, ex, model.ent)
+            assert all(s in (0, 2) for s in state.tolist())
+            got = moe.moe_store_get_stats(st)
+            assert {k: got[k] for k in model.stats} == model.stats, step
+        for e in held:
+            moe.moe_store_release(st, e)
+    finally:
+        moe.moe_store_close(st)
