@@ -70,6 +70,10 @@ def parse():
     ap.add_argument("--storage-readers", type=int, default=8)
     ap.add_argument("--storage-readahead", type=int, default=4)
     ap.add_argument("--storage-dir", default=None, help="where the expert files go (default: the temp dir)")
+    ap.add_argument("--stress", action="store_true",
+                    help="run the stress sweep (2816 shapes, uniform routing) and print its JSON (not the bench line)")
+    ap.add_argument("--stress-layers", type=int, default=8)
+    ap.add_argument("--stress-steps", type=int, default=16)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
@@ -809,6 +813,103 @@ def run_storage(args, ctx, dev, stream, seed):
     return out
 
 
+def run_stress(args, ctx, dev, stream, seed):
+    """stress_2816: the 2816 shapes with uniform routing (no bias), decode
+    batches of 1, 4, 16 and 64 tokens against caches of 8, 16 and 64 slots
+    per layer, and a 4096-token prompt in chunks of 128 per cache size.
+    --stress-layers layers (the workload names 48; each holds an 856 MB
+    pinned pool), fresh caches per point, --stress-steps timed steps after as
+    many warm-up steps. Per point: tokens/s, weight bytes the kernels read
+    from HBM and bytes copied host-to-device per token, the hit rate, and the
+    exposed copy time per token (the miss launches' wait for their copies,
+    from a second, event-timed pass over the same steps)."""
+    import torch
+
+    import expert_streaming_ffn_gb300 as moe
+    import synth
+
+    wl = synth.WORKLOADS["stress_2816"]
+    s = wl.shapes
+    L = args.stress_layers
+    K = args.stress_steps
+    ws, w = [], None
+    for l in range(L):
+        w = synth.layer_weights(s, l, seed, reuse=None)
+        ws.append(w)
+    sptr = stream.cuda_stream
+    row = s.d_model * 2
+    points = []
+    for S in (8, 16, 64):
+        layers = []
+        for l in range(L):
+            h = moe.moe_layer_create(ctx, s, S, wl.policy)
+            moe.moe_layer_set_weights(h, ws[l])
+            layers.append(h)
+        for T in (1, 4, 16, 64):
+            xs_np = np.empty((2 * K, L, T, s.d_model), np.uint16)
+            for st in range(2 * K):
+                for l in range(L):
+                    xs_np[st, l] = synth.tokens(s, l, 1000 * T + st, T, wl.rms_normalise, seed)
+            x_dev = torch.from_numpy(xs_np.view(np.int16)).view(torch.bfloat16).to(dev)
+            y_dev = torch.empty((L, T, s.d_model), dtype=torch.float32, device=dev)
+
+            def step(st):
+                base = x_dev.data_ptr() + st * L * T * row
+                for l in range(L):
+                    moe.moe_forward_ptr(layers[l], base + l * T * row, T, None, y_dev[l].data_ptr(), sptr)
+
+            def run(profile):
+                for h in layers:
+                    moe.moe_cache_reset(h)
+                for st in range(K):
+                    step(st)
+                torch.cuda.synchronize(dev)
+                for h in layers:
+                    moe.moe_layer_reset_stats(h)
+                moe.moe_ctx_set_profiling(ctx, profile)
+                ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                ev0.record(stream)
+                for st in range(K, 2 * K):
+                    step(st)
+                ev1.record(stream)
+                torch.cuda.synchronize(dev)
+                moe.moe_ctx_set_profiling(ctx, False)
+                return ev0.elapsed_time(ev1), [moe.moe_layer_stats(h) for h in layers]
+
+            ms, stats = run(False)
+            _, pstats = run(True)
+            tokens = K * T
+            hits = sum(x["hits"] for x in stats)
+            misses = sum(x["misses"] for x in stats)
+            points.append({
+                "slots": S, "batch": T, "tok_s": tokens / (ms * 1e-3), "ms_per_layer_step": ms / K / L,
+                "hit_rate": hits / (hits + misses) if hits + misses else None,
+                "bypass_per_layer_step": sum(x["bypass"] for x in stats) / K / L,
+                "hbm_MB_per_token": sum(x["bytes_resident"] for x in stats) / tokens / 1e6,
+                "h2d_MB_per_token": sum(x["bytes_h2d"] for x in stats) / tokens / 1e6,
+                "exposed_copy_us_per_token": sum(x["exposed_copy_us"] for x in pstats) / tokens,
+            })
+            del x_dev, y_dev
+        # the 4096-token prompt in chunks of 128, from a fresh cache
+        P = 4096
+        x = torch.from_numpy(synth.tokens(s, 0, 7, P, wl.rms_normalise, seed).view(np.int16)) \
+            .view(torch.bfloat16).to(dev)
+        y = torch.empty((P, s.d_model), dtype=torch.float32, device=dev)
+        moe.moe_cache_reset(layers[0])
+        moe.moe_layer_reset_stats(layers[0])
+        ms, _, st = _prefill_pass(ctx, dev, stream, layers[:1], [x], y)
+        st = st[0]
+        points.append({
+            "slots": S, "prefill_tokens": P, "tok_s": P / (ms * 1e-3), "ms_per_layer": ms,
+            "hit_rate": st["hits"] / max(1, st["hits"] + st["misses"]),
+            "hbm_MB_per_token": st["bytes_resident"] / P / 1e6, "h2d_MB_per_token": st["bytes_h2d"] / P / 1e6,
+            "exposed_copy_us_per_token": st["exposed_copy_us"] / P,
+        })
+        for h in layers:
+            moe.moe_layer_destroy(h)
+    return {"workload": "stress_2816", "layers": L, "steps": K, "points": points}
+
+
 def main():
     args = parse()
     world, rank, local = dist_init()
@@ -826,6 +927,18 @@ def main():
         moe.moe_ctx_destroy(ctx)
         if rank == 0:
             print(json.dumps({"prefill": out}), flush=True)
+    elif args.stress:
+        import torch
+
+        import expert_streaming_ffn_gb300 as moe
+
+        torch.cuda.set_device(local)
+        moe.load()
+        ctx = moe.moe_ctx_create(local)
+        out = run_stress(args, ctx, torch.device("cuda", local), torch.cuda.current_stream(), 1000 * rank)
+        moe.moe_ctx_destroy(ctx)
+        if rank == 0:
+            print(json.dumps({"stress": out}), flush=True)
     elif args.storage_only:
         import torch
 
