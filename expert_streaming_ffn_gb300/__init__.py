@@ -108,6 +108,7 @@ SIGNATURES = [
     ("moe_store_release", _i32, [_vp, _i32]),
     ("moe_store_prefetch", _i32, [_vp, _vp, _i32, _P(_i32)]),
     ("moe_store_wait_idle", _i32, [_vp]),
+    ("moe_store_set_read_chunk", _i32, [_vp, _sz]),
     ("moe_store_get_stats", _i32, [_vp, _P(moe_store_stats)]),
     ("moe_store_reset_stats", _i32, [_vp]),
     ("moe_store_tier", _i32, [_vp, _vp, _vp]),
@@ -400,6 +401,11 @@ def moe_store_prefetch(store: int, experts) -> int:
     _check(load().moe_store_prefetch(store, _hptr(e) if e.size else None, e.size, ctypes.byref(q)),
            "moe_store_prefetch")
     return q.value
+
+
+def moe_store_set_read_chunk(store: int, nbytes: int) -> None:
+    """Read experts as pieces of nbytes (a multiple of 4096; 0 = whole) spread over the readers."""
+    _check(load().moe_store_set_read_chunk(store, nbytes), "moe_store_set_read_chunk")
 
 
 def moe_store_wait_idle(store: int) -> None:

@@ -18,7 +18,10 @@
 //   4096 + e * stride       expert e: expert_blob_bytes bytes, zero padded to
 //                           stride = the blob size rounded up to 4096
 // Every read is one pread of `stride` bytes at a 4096-aligned offset into a
-// 4096-aligned buffer, which O_DIRECT requires.
+// 4096-aligned buffer, which O_DIRECT requires; with a read chunk set
+// (moe_store_set_read_chunk, a multiple of 4096), one pread per chunk of it,
+// taken by as many readers as are free, and the entry is ready when the last
+// piece lands.
 //
 // The host tier is H entries of `stride` bytes. An entry is empty, being
 // read, ready, or failed. The store counts every expert's fetches (its
@@ -81,7 +84,17 @@ struct Entry {
     uint64_t used = 0;        // tick of the last fetch (or of the read's start)
     bool predicted = false;   // read by a readahead request and not fetched since
     bool demand = false;      // queued ahead for a fetch that follows (not a tier hit)
-    int err = 0;              // errno of a failed read
+    int err = 0;              // errno of a failed read (the first failed piece's)
+    int pending = 0;          // pieces of the read not yet finished
+    size_t piece = 0;         // bytes per piece of the read in flight
+    bool started = false;     // a piece has started (t0 is set)
+    std::chrono::steady_clock::time_point t0;
+};
+
+// One piece of an expert's read: bytes [piece * chunk, ...) of entry `entry`.
+struct Job {
+    int entry;
+    int piece;
 };
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -105,8 +118,9 @@ struct moe_expert_store {
     std::vector<int> where;  // expert -> entry, -1 if not in the tier
     std::mutex mu;
     std::condition_variable cv_job, cv_done;
-    std::deque<int> jobs;     // entries to read for fetches, in request order
-    std::deque<int> jobs_ra;  // entries to read ahead, taken only when `jobs` is empty
+    std::deque<moe::Job> jobs;     // pieces to read for fetches, in request order
+    std::deque<moe::Job> jobs_ra;  // pieces to read ahead, taken only when `jobs` is empty
+    size_t chunk = 0;              // bytes per piece of a read (a multiple of 4096); 0 = whole expert
     std::vector<uint32_t> freq;  // fetches per expert
     std::vector<uint8_t> keep;   // experts whose entries must not be taken (during one readahead call)
     std::vector<std::thread> readers;
@@ -121,24 +135,31 @@ namespace {
 
 void reader_loop(moe_expert_store* s) {
     for (;;) {
-        int i;
+        Job job;
         int e;
+        size_t begin, len;
         {
             std::unique_lock<std::mutex> lk(s->mu);
             s->cv_job.wait(lk, [&] { return s->stop || !s->jobs.empty() || !s->jobs_ra.empty(); });
-            std::deque<int>& q = !s->jobs.empty() ? s->jobs : s->jobs_ra;
+            std::deque<Job>& q = !s->jobs.empty() ? s->jobs : s->jobs_ra;
             if (q.empty()) return;  // stop, and nothing left to read
-            i = q.front();
+            job = q.front();
             q.pop_front();
-            e = s->ent[(size_t)i].expert;
+            Entry& en = s->ent[(size_t)job.entry];
+            e = en.expert;
+            begin = (size_t)job.piece * en.piece;
+            len = std::min(en.piece, s->stride - begin);
+            if (!en.started) {
+                en.started = true;
+                en.t0 = std::chrono::steady_clock::now();
+            }
         }
-        uint8_t* dst = s->buf + (size_t)i * s->stride;
-        const off_t off = (off_t)(s->data_offset + (size_t)e * s->stride);
-        const auto t0 = std::chrono::steady_clock::now();
+        uint8_t* dst = s->buf + (size_t)job.entry * s->stride + begin;
+        const off_t off = (off_t)(s->data_offset + (size_t)e * s->stride + begin);
         size_t done = 0;
         int err = 0;
-        while (done < s->stride) {
-            const ssize_t r = pread(s->fd, dst + done, s->stride - done, off + (off_t)done);
+        while (done < len) {
+            const ssize_t r = pread(s->fd, dst + done, len - done, off + (off_t)done);
             if (r < 0) {
                 if (errno == EINTR) continue;
                 err = errno;
@@ -150,19 +171,37 @@ void reader_loop(moe_expert_store* s) {
             }
             done += (size_t)r;
         }
-        const double us = us_between(t0, std::chrono::steady_clock::now());
+        bool finished = false;
         {
             std::lock_guard<std::mutex> g(s->mu);
-            Entry& en = s->ent[(size_t)i];
-            en.state = err ? kFailed : kReady;
-            en.err = err;
-            s->st.reads += 1;
-            s->st.read_us += us;
-            if (!err) s->st.bytes_read += s->stride;
-            else s->st.read_errors += 1;
+            Entry& en = s->ent[(size_t)job.entry];
+            if (err && !en.err) en.err = err;
+            if (--en.pending == 0) {
+                finished = true;
+                en.state = en.err ? kFailed : kReady;
+                s->st.reads += 1;
+                s->st.read_us += us_between(en.t0, std::chrono::steady_clock::now());
+                if (!en.err) s->st.bytes_read += s->stride;
+                else s->st.read_errors += 1;
+            }
         }
-        s->cv_done.notify_all();
+        if (finished) s->cv_done.notify_all();
     }
+}
+
+// Queue the read of entry i (state already kReading) as its pieces. Caller
+// holds the mutex.
+void queue_read(moe_expert_store* s, int i, bool predicted) {
+    Entry& en = s->ent[(size_t)i];
+    en.piece = s->chunk ? s->chunk : s->stride;
+    const int pieces = (int)((s->stride + en.piece - 1) / en.piece);
+    en.pending = pieces;
+    en.started = false;
+    en.err = 0;
+    std::deque<Job>& q = predicted ? s->jobs_ra : s->jobs;
+    for (int p = 0; p < pieces; ++p) q.push_back(Job{i, p});
+    if (pieces == 1) s->cv_job.notify_one();
+    else s->cv_job.notify_all();
 }
 
 // An entry to (re)use: the lowest empty one, else, among the ready or failed
@@ -202,10 +241,8 @@ void assign(moe_expert_store* s, int i, int e, bool predicted) {
     en.used = ++s->tick;
     en.predicted = predicted;
     en.demand = !predicted;
-    en.err = 0;
     s->where[(size_t)e] = i;
-    (predicted ? s->jobs_ra : s->jobs).push_back(i);
-    s->cv_job.notify_one();
+    queue_read(s, i, predicted);
 }
 
 bool any_reading(const moe_expert_store* s) {
@@ -238,10 +275,8 @@ moe_status store_acquire(moe_expert_store* s, int e, const uint8_t** out) {
             if (en.state == kFailed && !queued) {
                 // a read queued earlier (readahead) failed: read again for this fetch
                 en.state = kReading;
-                en.err = 0;
                 en.predicted = false;
-                s->jobs.push_back(i);
-                s->cv_job.notify_one();
+                queue_read(s, i, false);
                 queued = true;
                 continue;
             }
@@ -500,6 +535,14 @@ extern "C" moe_status moe_store_prefetch(moe_expert_store* S, const int32_t* exp
     if (!S || (!experts && n > 0) || n < 0) return set_error(MOE_EINVAL, "moe_store_prefetch: bad arguments");
     const int q = store_readahead(S, experts, n, true);
     if (queued) *queued = q;
+    return MOE_OK;
+}
+
+extern "C" moe_status moe_store_set_read_chunk(moe_expert_store* S, size_t bytes) {
+    if (!S) return set_error(MOE_EINVAL, "moe_store_set_read_chunk: store is NULL");
+    if (bytes % kAlign != 0) return set_error(MOE_EINVAL, "read chunk %zu is not a multiple of 4096", bytes);
+    std::lock_guard<std::mutex> g(S->mu);
+    S->chunk = bytes >= S->stride ? 0 : bytes;
     return MOE_OK;
 }
 

@@ -348,6 +348,13 @@ moe_status moe_store_release(moe_expert_store* store, int32_t expert); /* MOE_EI
  * left. Does not wait. *queued (may be NULL) receives the number queued. */
 moe_status moe_store_prefetch(moe_expert_store* store, const int32_t* experts, int32_t n, int32_t* queued);
 
+/* Read each expert as pieces of `bytes` (a multiple of 4096), which the
+ * reader threads take in parallel, instead of as one pread of the whole
+ * padded expert (bytes = 0, the default, or bytes >= the stride). Applies to
+ * reads queued after the call. Errors: MOE_EINVAL (NULL, not a multiple of
+ * 4096). */
+moe_status moe_store_set_read_chunk(moe_expert_store* store, size_t bytes);
+
 /* Block until no read is queued or running. */
 moe_status moe_store_wait_idle(moe_expert_store* store);
 

@@ -12,7 +12,9 @@
   pinned); readahead fills free entries, never evicts an expert read ahead
   and not yet used, and displaces only experts fetched no more often;
 * failures: wrong shapes, foreign or short files, a read past a file that
-  shrank after opening (MOE_EIO; a later fetch retries);
+  shrank after opening (MOE_EIO; a later fetch retries), a read cut short
+  inside an expert (the entry fails whole, also when read in pieces);
+* reads split into pieces over several readers give the same bytes;
 * several host threads fetching at once get the right bytes.
 """
 import os
@@ -98,10 +100,14 @@ def test_each_region_holds_its_expert(expert_file, weights):
         assert (_nibbles(dn[:d * I // 2]) == _nibbles(dc)).all(), e
 
 
+@pytest.mark.parametrize("chunk", [0, 4096, 65536])
 @pytest.mark.parametrize("flags", [0, moe.MOE_STORE_DIRECT])
-def test_fetch_returns_the_files_bytes(expert_file, flags):
+def test_fetch_returns_the_files_bytes(expert_file, flags, chunk):
+    # whole-expert reads, and reads in pieces of 4 KiB (41 of them) and 64 KiB
+    # (two full pieces and a 36 KiB tail) spread over the readers
     eb = moe.moe_expert_bytes(SHAPES)
     st = moe.moe_store_open(expert_file, SHAPES, 3, 2, flags)
+    moe.moe_store_set_read_chunk(st, chunk)
     try:
         for e in [5, 0, 7, 5, 2]:
             got = moe.moe_store_fetch(st, e, eb)
@@ -240,12 +246,14 @@ def test_open_rejects_bad_files_and_arguments(tmp_path, expert_file):
         assert ei.value.status == moe.MOE_EINVAL
 
 
-def test_read_failure_is_reported_and_retried(tmp_path, weights):
+@pytest.mark.parametrize("chunk", [0, 65536])
+def test_read_failure_is_reported_and_retried(tmp_path, weights, chunk):
     p = str(tmp_path / "shrinks.experts")
     moe.moe_store_write(p, SHAPES, weights)
     eb = moe.moe_expert_bytes(SHAPES)
     stride = moe.moe_store_expert_stride(SHAPES)
-    st = moe.moe_store_open(p, SHAPES, 2, 1)
+    st = moe.moe_store_open(p, SHAPES, 2, 3)
+    moe.moe_store_set_read_chunk(st, chunk)
     try:
         os.truncate(p, ALIGN + 4 * stride)  # experts 4..7 are gone
         assert (moe.moe_store_fetch(st, 3, eb) == np.fromfile(p, np.uint8)[ALIGN + 3 * stride:][:eb]).all()
@@ -261,10 +269,47 @@ def test_read_failure_is_reported_and_retried(tmp_path, weights):
         moe.moe_store_close(st)
 
 
-def test_concurrent_fetches_get_their_bytes(expert_file):
+@pytest.mark.parametrize("chunk", [0, 4096, 65536])
+def test_a_read_cut_short_inside_an_expert_fails_whole(tmp_path, weights, chunk):
+    # the file ends 100 KiB into expert 2: with pieces, some of its pieces
+    # land and some fail; the entry must fail as a whole, never be served
+    p = str(tmp_path / "cut.experts")
+    moe.moe_store_write(p, SHAPES, weights)
+    eb = moe.moe_expert_bytes(SHAPES)
+    stride = moe.moe_store_expert_stride(SHAPES)
+    st = moe.moe_store_open(p, SHAPES, 2, 4)
+    moe.moe_store_set_read_chunk(st, chunk)
+    try:
+        os.truncate(p, ALIGN + 2 * stride + 100 * 1024)
+        assert (moe.moe_store_fetch(st, 1, eb) == np.fromfile(p, np.uint8)[ALIGN + stride:][:eb]).all()
+        moe.moe_store_release(st, 1)
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_store_fetch(st, 2, eb)
+        assert ei.value.status == moe.MOE_EIO
+        s = moe.moe_store_get_stats(st)
+        assert s["reads"] == 2 and s["read_errors"] == 1 and s["bytes_read"] == stride
+    finally:
+        moe.moe_store_close(st)
+
+
+def test_read_chunk_must_be_page_multiple(expert_file):
+    st = moe.moe_store_open(expert_file, SHAPES, 2, 1)
+    try:
+        for bad in (1, 4095, 6000):
+            with pytest.raises(moe.MoeError) as ei:
+                moe.moe_store_set_read_chunk(st, bad)
+            assert ei.value.status == moe.MOE_EINVAL
+        moe.moe_store_set_read_chunk(st, 10 * 2 ** 20)  # above the stride: whole-expert reads
+    finally:
+        moe.moe_store_close(st)
+
+
+@pytest.mark.parametrize("chunk", [0, 8192])
+def test_concurrent_fetches_get_their_bytes(expert_file, chunk):
     eb = moe.moe_expert_bytes(SHAPES)
     want = [_region(expert_file, e)[:eb] for e in range(SHAPES.n_experts)]
     st = moe.moe_store_open(expert_file, SHAPES, 4, 3)
+    moe.moe_store_set_read_chunk(st, chunk)
     errors = []
 
     def worker(seed):
@@ -361,13 +406,14 @@ class _TierModel:
         return q
 
 
-@pytest.mark.parametrize("seed", [0, 1, 2, 3])
-def test_tier_follows_its_rules_on_random_requests(expert_file, seed):
+@pytest.mark.parametrize("seed,chunk", [(0, 0), (1, 0), (2, 65536), (3, 16384)])
+def test_tier_follows_its_rules_on_random_requests(expert_file, seed, chunk):
     H, E = 3, SHAPES.n_experts
     eb = moe.moe_expert_bytes(SHAPES)
     want = [_region(expert_file, e)[:eb] for e in range(E)]
     rng = np.random.default_rng(seed)
     st = moe.moe_store_open(expert_file, SHAPES, H, 2)
+    moe.moe_store_set_read_chunk(st, chunk)
     model = _TierModel(H, E)
     held = []
     try:
