@@ -711,10 +711,12 @@ def run_storage(args, ctx, dev, stream, seed):
     where the file system allows it) into a host tier of
     --storage-host-slots experts, then copied to the layer's 16 HBM slots.
     --storage-layers layers, one token per step, Zipf(1.1) routing as in the
-    decode bench. Two runs from fresh stores and caches: `demand` (reads only
-    when a miss needs them) and `readahead` (before each layer, the next
-    layer's --storage-readahead most-routed experts that are in neither its
-    slots nor its tier are read ahead)."""
+    decode bench. Three runs from fresh stores and caches: `demand` (reads
+    only when a miss needs them, one pread per expert), `demand_1MiB_pieces`
+    (the same, each expert read as 1 MiB pieces spread over the readers) and
+    `readahead` (before each layer, the next layer's --storage-readahead
+    most-routed experts that are in neither its slots nor its tier are read
+    ahead)."""
     import shutil
     import tempfile
     import types
@@ -752,10 +754,12 @@ def run_storage(args, ctx, dev, stream, seed):
         y_dev = torch.empty((L, s.d_model), dtype=torch.float32, device=dev)
         row = s.d_model * 2
         sptr = stream.cuda_stream
-        for mode, pf in (("demand", 0), ("readahead", args.storage_readahead)):
+        for mode, pf, chunk in (("demand", 0, 0), ("demand_1MiB_pieces", 0, 1 << 20),
+                                ("readahead", args.storage_readahead, 0)):
             stores, layers = [], []
             for l in range(L):
                 stores.append(moe.moe_store_open(paths[l], s, H, args.storage_readers, moe.MOE_STORE_DIRECT))
+                moe.moe_store_set_read_chunk(stores[-1], chunk)
                 layers.append(moe.moe_layer_create_streamed(ctx, s, wl.cache_slots, stores[-1], wl.policy))
                 resident = types.SimpleNamespace(router=synth.router_weights(s, l, seed),
                                                  shared=synth.ffn_weights(s, l, 0, seed, shared=True))
