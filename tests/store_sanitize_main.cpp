@@ -1,12 +1,13 @@
-// A race check of the expert store (csrc/store.cpp) under ThreadSanitizer:
-// several threads fetch, release and read ahead at random against one store,
-// while its reader threads fill the tier, and every fetched expert is
-// compared with the file's bytes. Built with g++ -fsanitize=thread by
-// test_store_tsan.py together with store.cpp alone, so the few library
-// functions store.cpp calls are defined here (the file is written by the
-// library beforehand; nothing here repacks weights).
+// A check of the expert store (csrc/store.cpp) under the sanitizers: several
+// threads fetch, release and read ahead at random against one store, while
+// its reader threads fill the tier, and every fetched expert is compared with
+// the file's bytes. Built with g++ -fsanitize=thread, and with
+// -fsanitize=address,undefined, by test_store_sanitizers.py together with
+// store.cpp alone, so the few library functions store.cpp calls are defined
+// here (the file is written by the library beforehand; nothing here repacks
+// weights).
 //
-//   store_tsan <expert file> <read chunk bytes>
+//   store_sanitize <expert file> <read chunk bytes>
 #include <fcntl.h>
 #include <stdarg.h>
 #include <stdio.h>
