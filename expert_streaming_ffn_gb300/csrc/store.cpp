@@ -30,14 +30,16 @@
 // is reading, the one whose expert has the fewest fetches (ties: the least
 // recently used), and queues its read. Readahead takes an entry only if its
 // expert has no more fetches than the expert read ahead, never one read ahead
-// and not yet fetched, and its reads wait behind every read a fetch needs. A fetch that
-// finds a failed read it did not ask for (readahead's) reads once more; a
-// read that fails for the fetch that asked for it is reported (MOE_EIO) and
-// its entry freed. A fetched entry
-// stays pinned until released: the layer releases it once the host-to-device
-// copy that reads it has finished. Reads run on the reader threads; the tier's
-// table is guarded by one mutex, and a reader writes only the buffer of the
-// entry it was given, which no one else touches until the entry is ready.
+// and not yet fetched, and its reads wait behind every read a fetch needs.
+// A fetch that finds a failed read it did not ask for (readahead's) reads
+// once more; a read that fails for the fetch that asked for it is reported
+// (MOE_EIO) and its entry freed. A fetched entry stays pinned until released:
+// the layer releases it once the host-to-device copy that reads it has
+// finished.
+//
+// Reads run on the reader threads. The tier's table is guarded by one mutex;
+// a reader writes only the piece of the entry's buffer it was given, outside
+// the mutex, and no one else touches that buffer until the entry is ready.
 #include <errno.h>
 #include <fcntl.h>
 #include <stdlib.h>
