@@ -25,8 +25,11 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "oracle.c")
-_LIB_PATH = os.path.join(_HERE, "_build", "liboracle.so")
+# MOE_ORACLE_SOURCE may name another copy of oracle.c (the mutation test plants
+# one mistake in a scratch copy to check that the pins catch it); it is built
+# beside that copy. Unset, this directory's oracle.c is used.
+_SRC = os.environ.get("MOE_ORACLE_SOURCE") or os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(os.path.dirname(_SRC), "_build", "liboracle.so")
 _lib = None
 _lock = threading.Lock()
 
