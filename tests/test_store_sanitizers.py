@@ -1,9 +1,12 @@
-"""The expert store under the sanitizers (no GPU): store.cpp built alone with
+"""The expert store and the host cache manager under the sanitizers (no GPU):
+store.cpp and host_cache.cpp built alone with
 g++ -fsanitize=thread (and, separately, -fsanitize=address,undefined) and
 driven by tests/store_sanitize_main.cpp from four threads (fetch, release,
 readahead) against its own reader threads, with whole-expert reads and with
-reads in pieces. A data race, a memory error, undefined behaviour, a wrong
-byte or a lost fetch fails the test."""
+reads in pieces; the cache manager on random steps of up to 512 ids under
+both policies with its invariants checked. A data race, a memory error,
+undefined behaviour, a wrong byte, a broken invariant or a lost fetch fails
+the test."""
 import os
 import shutil
 import subprocess
@@ -39,6 +42,7 @@ def test_store_under_sanitizers(tmp_path, sanitizer, options):
     cmd = ["g++", "-std=c++17", "-O1", "-g", flag, "-fno-sanitize-recover=undefined"
            if "undefined" in sanitizer else "-O1", "-I", os.path.join(ROOT, "include"),
            "-I", "/usr/local/cuda/include", os.path.join(ROOT, "expert_streaming_ffn_gb300", "csrc", "store.cpp"),
+           os.path.join(ROOT, "expert_streaming_ffn_gb300", "csrc", "host_cache.cpp"),
            os.path.join(ROOT, "tests", "store_sanitize_main.cpp"), "-o", exe, "-lpthread"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
