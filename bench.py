@@ -11,10 +11,12 @@ combine, for every layer.
 
 Prints one JSON line. Metric: decode tokens/s (whole job); also the achieved
 HBM bandwidth of the dominant kernel against the measured peak, the prefill
-chunk rate and expert TFLOP/s, the CPU oracle as a baseline, and the same
-decode metric end to end with host buffers.
+chunk rate and expert TFLOP/s, 4 layers streamed from expert files (the
+storage tier), the CPU oracle as a baseline, and the same decode metric end
+to end with host buffers.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --prefill-only | --storage-only | --stress   (one leg, its own JSON)
 
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
 (the layer does not shard); value = all ranks' tokens / the slowest rank's time.
