@@ -305,9 +305,12 @@ moe_status moe_group_pairs(const int32_t* ids, int32_t n_pairs, int32_t n_expert
  *   to stride = moe_store_expert_stride(shapes), a multiple of 4096.
  * A store reads such a file into a host tier of host_slots expert buffers
  * (4096-aligned; page-locked while a layer streams from it) with `readers`
- * threads, one pread of `stride` bytes per expert. An expert not in the tier
- * takes an empty entry, else the least recently used entry that is neither
- * pinned nor being read. */
+ * threads, one pread of `stride` bytes per expert (or one per piece, see
+ * moe_store_set_read_chunk). The store counts each expert's fetches, across
+ * evictions. A fetched expert not in the tier takes an empty entry, else, of
+ * the entries neither pinned nor being read, the one whose expert was
+ * fetched least often (ties: least recently used) ([P1] §9.5 item 1 prefers
+ * frequency to recency for MoE experts). 
 
 /* Bytes between consecutive experts in an expert file (the blob size rounded
  * up to 4096); 0 if shapes is NULL. */
@@ -342,10 +345,12 @@ moe_status moe_store_close(moe_expert_store* store);
 moe_status moe_store_fetch(moe_expert_store* store, int32_t expert, const uint8_t** out);
 moe_status moe_store_release(moe_expert_store* store, int32_t expert); /* MOE_EINVAL if not pinned */
 
-/* Readahead ([P1] §9.2 item 3): queue reads of the listed experts that are
- * not in the tier, in list order, each into an entry that is neither pinned,
- * being read, nor read ahead and not yet fetched; stops when no such entry is
- * left. Does not wait. *queued (may be NULL) receives the number queued. */
+/* Readahead ([P1] §9.2 item 3): for each listed expert not in the tier, in
+ * list order, queue its read into an entry that is empty, or else neither
+ * pinned, being read, nor read ahead and not yet fetched, and whose expert
+ * was fetched no more often than the listed one (an expert with no such
+ * entry is skipped). These reads start only when no read a fetch needs is
+ * waiting. Does not wait. *queued (may be NULL) receives the number queued. */
 moe_status moe_store_prefetch(moe_expert_store* store, const int32_t* experts, int32_t n, int32_t* queued);
 
 /* Read each expert as pieces of `bytes` (a multiple of 4096), which the
@@ -400,11 +405,12 @@ moe_status moe_layer_create_streamed(moe_ctx* ctx, const moe_shapes* shapes, con
                                      moe_layer** out);
 
 /* Readahead from routing history ([P1] §9.2 item 3, §9.5 item 2): a streamed
- * layer counts, per expert, the cache steps that routed to it; this queues
- * reads of up to n experts with the highest counts (ties to the lower id)
- * that are routed at least once, not in the layer's HBM slots and not in the
- * store's tier. Meant to be called for layer l+1 while layer l runs. Does not
- * wait. *queued (may be NULL) receives the number queued.
+ * layer counts, per expert, the cache steps that routed to it; this offers
+ * the store's readahead (moe_store_prefetch) up to n experts with the highest
+ * counts (ties to the lower id) that are routed at least once, not in the
+ * layer's HBM slots and not in the store's tier. Meant to be called for layer
+ * l+1 while layer l runs. Does not wait. *queued (may be NULL) receives the
+ * number of reads queued.
  * Errors: MOE_EINVAL (NULL layer, n < 0), MOE_ESTATE (not a streamed layer). */
 moe_status moe_layer_prefetch(moe_layer* layer, int32_t n, int32_t* queued);
 
