@@ -310,7 +310,7 @@ moe_status moe_group_pairs(const int32_t* ids, int32_t n_pairs, int32_t n_expert
  * evictions. A fetched expert not in the tier takes an empty entry, else, of
  * the entries neither pinned nor being read, the one whose expert was
  * fetched least often (ties: least recently used) ([P1] §9.5 item 1 prefers
- * frequency to recency for MoE experts). 
+ * frequency to recency for MoE experts). */
 
 /* Bytes between consecutive experts in an expert file (the blob size rounded
  * up to 4096); 0 if shapes is NULL. */
