@@ -50,6 +50,24 @@ moe_status set_error(moe_status s, const char* fmt, ...) {
     return s;
 }
 
+cudaError_t ensure_smem_attr(const void* kernel, size_t bytes) {
+    struct Done {
+        const void* kernel;
+        int device;
+    };
+    static std::mutex mu;
+    static std::vector<Done> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Done& x : done)
+        if (x.kernel == kernel && x.device == dev) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) done.push_back(Done{kernel, dev});
+    return e;
+}
+
 // One 32-bit word of 8 codes (elements k0..k7 of the canonical row, byte j =
 // k_2j | k_2j+1 << 4) in the device order: nibble i holds element
 // [0,2,4,6,1,3,5,7][i], so that masking with 0x000F000F (and the same on the
@@ -1483,6 +1501,7 @@ extern "C" moe_status moe_layer_set_weights(moe_layer* L, const moe_host_weights
 extern "C" moe_status moe_route(moe_layer* L, const void* x, int32_t T, const float* zbias, int32_t* ids,
                                 float* gates, void* stream) {
     if (!L || !x || !ids || !gates || T < 1) return set_error(MOE_EINVAL, "moe_route: bad arguments");
+    if (reinterpret_cast<uintptr_t>(x) & 15) return set_error(MOE_EINVAL, "moe_route: x must be 16-byte aligned");
     if (!L->loaded) return set_error(MOE_ESTATE, "moe_route before moe_layer_set_weights");
     CUDA_TRY(cudaSetDevice(L->ctx->device));
     cudaStream_t s = (cudaStream_t)stream;
@@ -1539,6 +1558,7 @@ extern "C" moe_status moe_cache_step(moe_layer* L, const int32_t* ids, int32_t n
 extern "C" moe_status moe_forward(moe_layer* L, const void* x, int32_t T, const float* zbias, float* y,
                                   int32_t* ids_out, float* gates_out, void* stream) {
     if (!L || !x || !y || T < 1) return set_error(MOE_EINVAL, "moe_forward: bad arguments");
+    if (reinterpret_cast<uintptr_t>(x) & 15) return set_error(MOE_EINVAL, "moe_forward: x must be 16-byte aligned");
     if (!L->loaded) return set_error(MOE_ESTATE, "moe_forward before moe_layer_set_weights");
     CUDA_TRY(cudaSetDevice(L->ctx->device));
     cudaStream_t s = (cudaStream_t)stream;
@@ -1561,6 +1581,8 @@ extern "C" moe_status moe_forward(moe_layer* L, const void* x, int32_t T, const 
 extern "C" moe_status moe_forward_prompt(moe_layer* L, const void* x, int32_t T, const float* zbias, float* y,
                                          int32_t* ids_out, float* gates_out, void* stream) {
     if (!L || !x || !y || T < 1 || T > kPromptMaxT) return set_error(MOE_EINVAL, "moe_forward_prompt: bad arguments");
+    if (reinterpret_cast<uintptr_t>(x) & 15)
+        return set_error(MOE_EINVAL, "moe_forward_prompt: x must be 16-byte aligned");
     if (!L->loaded) return set_error(MOE_ESTATE, "moe_forward_prompt before moe_layer_set_weights");
     CUDA_TRY(cudaSetDevice(L->ctx->device));
     moe_status st = ensure_scratch(L, std::max(T, L->cap_T));
@@ -1692,6 +1714,8 @@ moe_status noalloc_scratch(int device, NoAllocScratch* out) {
 extern "C" moe_status moe_route_noalloc(moe_layer* L, const void* x, int32_t T, const float* zbias, int32_t* ids,
                                         float* gates, void* stream) {
     if (!L || !x || !ids || !gates || T < 1) return set_error(MOE_EINVAL, "moe_route_noalloc: bad arguments");
+    if (reinterpret_cast<uintptr_t>(x) & 15)
+        return set_error(MOE_EINVAL, "moe_route_noalloc: x must be 16-byte aligned");
     if (!L->loaded) return set_error(MOE_ESTATE, "moe_route_noalloc before moe_layer_set_weights");
     if (T > kNoAllocMaxT || (long)T * L->sh.n_experts > kNoAllocLogits)
         return set_error(MOE_EINVAL,
@@ -1705,6 +1729,7 @@ extern "C" moe_status moe_route_noalloc(moe_layer* L, const void* x, int32_t T, 
     RouterParams p{static_cast<const uint16_t*>(x), T, L->sh.d_model, L->sh.n_experts, L->sh.top_k,
                    L->d_router_codes, L->d_router_sb, zbias, sc.logits, sc.counters, ids, gates, nullptr, 0};
     CUDA_TRY(launch_router(p, (cudaStream_t)stream));
+    // counted, but never timed: a timing record would create CUDA events
     ++L->ctx->launches;
     return MOE_OK;
 }

@@ -317,15 +317,10 @@ __global__ void combine_kernel(const float* __restrict__ o, const float* __restr
 }  // namespace
 
 cudaError_t launch_router(const RouterParams& p, cudaStream_t s, bool pdl) {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(router_kernel<kRouterTB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kRouterTB * kMaxDModel * 2);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(router_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDModel * 2);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    cudaError_t e = ensure_smem_attr((const void*)router_kernel<kRouterTB>, (size_t)kRouterTB * kMaxDModel * 2);
+    if (e != cudaSuccess) return e;
+    e = ensure_smem_attr((const void*)router_kernel<1>, (size_t)kMaxDModel * 2);
+    if (e != cudaSuccess) return e;
     const size_t sm = (size_t)std::min(kRouterTB, p.T) * p.d * 2;
     cudaLaunchAttribute la;
     if (p.T == 1) {

@@ -5,23 +5,36 @@
 //   [P3] "BigMoeOnEdge：端侧 MoE 专家流式推理原理与实测"
 //
 // FFN_e(x) = W_down,e (act(W_gate,e x) * (W_up,e x)) ([P1] §2.4 cb2) over int4
-// affine group-64 weights ([P1] §2.1, §2.5), fp32 accumulation, for every
-// (token, rank) pair routed to each expert, and y[t] = shared(x_t) +
-// sum_r g[t][r] FFN_{e_r}(x_t) ([P1] §6.2.3 fusion of the shared and the
-// weighted routed outputs; [P3] "每个 token、每层都要重新路由": y = sum_j w_j
-// Expert_j(x)).
+// affine group-64 weights ([P1] §2.1, §2.5), for every (token, rank) pair
+// routed to each expert, and y[t] = shared(x_t) + sum_r g[t][r] FFN_{e_r}(x_t)
+// ([P1] §6.2.3 fusion of the shared and the weighted routed outputs; [P3]
+// "每个 token、每层都要重新路由": y = sum_j w_j Expert_j(x)).
 //
 // Work unit: 32 consecutive intermediate rows c of one item (an expert with
 // up to kFfnMaxNT of its pairs). A unit computes its slice of h,
 //   h_j = act(W_gate[j] . x) * (W_up[j] . x),   j = 32c .. 32c + 31,
 // then multiplies the matching 32 columns of W_down by that slice and adds
-// gate * partial into y with fp32 atomic adds (y is zero on entry). Units
-// never wait on one another: a unit's down columns stream through the same
-// shared-memory ring right behind its gate/up rows, and its h never leaves the
-// SM. The down matrix is stored column-sliced so that those columns are one
-// contiguous run of codes plus one of scales. The sum over units lands in y
-// in whatever order the atomics arrive, so y can differ between calls in the
-// last bits of fp32.
+// its gate-weighted share into y with fp32 atomic adds (y is zero on entry).
+// Units never wait on one another: a unit's down columns stream through the
+// same shared-memory ring right behind its gate/up rows, and its h never
+// leaves the SM. The down matrix is stored column-sliced so that those
+// columns are one contiguous run of codes plus one of scales. The sum over
+// units lands in y in whatever order the atomics arrive, so y can differ
+// between calls in the last bits of fp32.
+//
+// Dot products on the tensor cores, with the 4-bit codes exact. A word of 8
+// codes masked into the mantissa of fp16 1024.0 gives, per 16-bit half,
+// 1024 + q (nibble in bits 0-3) or 1024 + 16 q (nibble in bits 4-7): one
+// logic op per two codes, no conversion and no rounding. Those halves are the
+// A operand of mma.sync m16n8k16 (16 weight rows x 16 inputs); the B operand
+// holds the token rows (8 columns: up to 8 tokens) in fp16, scaled per row by
+// a power of two 2^s so that the largest magnitude lands in [2^14, 2^15), and
+// divided by 16 where the codes carry the factor 16. The products are exact
+// and accumulate in fp32. Per group of 64 inputs the accumulator starts at
+// -1024 * (sum of the group's B values), which removes the offset, so it ends
+// at sum_i q_i x~_i; the affine part is then s * that + b * sum_i x~_i, and
+// 2^-s undoes the scaling. For the down projection the B operand is h in two
+// fp16 parts, h~ = hi + lo (22 significant bits), in neighbouring columns.
 //
 // Ready state ([P3] "读取完成后，算子才可以使用切片"): an expert whose bytes are
 // still being copied into its slot carries the index of a ready flag and the
@@ -47,50 +60,65 @@ namespace moe {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kRecord = 1152;                     // gate/up: 64 inputs x 32 rows of codes, then 32 scale/bias words
-constexpr int kHalf = 512;                        // down: codes of 32 rows x 32 inputs
-constexpr int kSbBlock = 128;                     // down: scale/bias words of 32 rows
-constexpr int kBarCons = 1;                       // named barrier of the consumer warps
-constexpr int kStageCap = 64 * 1024;              // bytes of staged inputs per CTA
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+constexpr int kRecord = 1152;  // gate/up: 64 inputs x 32 rows of codes, then 32 scale/bias words
+constexpr int kHalf = 512;     // down: codes of 32 rows x 32 inputs
+constexpr int kSbBlock = 128;  // down: scale/bias words of 32 rows
+constexpr int kBarCons = 1;    // named barrier of the consumer warps
 
 __device__ __forceinline__ float2 unpack_sb(uint32_t w) {
     __half2 h = *reinterpret_cast<__half2*>(&w);
     return __half22float2(h);
 }
 
-// 4-bit codes to floats without a conversion: the word masked to the nibble
-// at position p, read as an fp32 bit pattern, is the subnormal q * 16^p *
-// 2^-149 (exact; nibbles 0..5 lie in the mantissa field). The inputs it
-// multiplies are staged as x * 2^(kStageExp - 4p), so the fused multiply-add
-// forms q * x * 2^(kStageExp - 149) exactly before its one rounding, a normal
-// number for any |q x| above 2^-77; the sums are scaled back by the exact
-// power of two kDotUnscale. Nibbles 5..7 are taken from the word shifted
-// right by 12, so the positions used are p = 0,1,2,3,4,2,3,4.
-constexpr int kStageExp = 100;  // staged |x| may reach 2^27 before overflow
-constexpr float kDotUnscale = 562949953421312.0f;  // 2^(149 - kStageExp) = 2^49
-
-template <uint32_t kMask>
-__device__ __forceinline__ float nibble_code(uint32_t v) {
-    return __uint_as_float(v & kMask);
+// Two codes as an fp16 pair: (w & mask) | 0x64006400.
+__device__ __forceinline__ uint32_t magic_pair(uint32_t w, uint32_t mask) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(w), "r"(mask), "r"(0x64006400u));
+    return r;
 }
 
-__device__ __forceinline__ void codes8(uint32_t v, float2 (&o)[4]) {
-    // v >> 12 as the high word of v * 2^20: an integer multiply-add, which
-    // runs beside the logic unit that the eight extractions keep busy
-    const uint32_t w = __umulhi(v, 1u << 20);
-    o[0] = make_float2(nibble_code<0xFu>(v), nibble_code<0xF0u>(v));
-    o[1] = make_float2(nibble_code<0xF00u>(v), nibble_code<0xF000u>(v));
-    o[2] = make_float2(nibble_code<0xF0000u>(v), nibble_code<0xF00u>(w));
-    o[3] = make_float2(nibble_code<0xF000u>(w), nibble_code<0xF0000u>(w));
+// The 8 codes of a word (nibble i holds element [0,2,4,6,1,3,5,7][i] of its
+// run of 8) as four fp16 pairs of consecutive elements: p[0] = elements 0,1
+// as 1024 + q; p[1] = 2,3 as 1024 + 16 q; p[2] = 4,5 as 1024 + q; p[3] = 6,7
+// as 1024 + 16 q.
+__device__ __forceinline__ void codes16(uint32_t w, uint32_t (&p)[4]) {
+    const uint32_t w8 = w >> 8;
+    p[0] = magic_pair(w, 0x000F000Fu);
+    p[1] = magic_pair(w, 0x00F000F0u);
+    p[2] = magic_pair(w8, 0x000F000Fu);
+    p[3] = magic_pair(w8, 0x00F000F0u);
 }
 
-// The staging factor 2^(kStageExp - 4p) for slot s of a run of 8 (p = 0,1,2,3,4,2,3,4).
-__device__ __forceinline__ float pos_scale(int s) {
-    const int p = s < 5 ? s : s - 3;
-    return __int_as_float((127 + kStageExp - 4 * p) << 23);
+// d += A * B, m16n8k16, fp16 operands, fp32 accumulators.
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 16 weight rows x 32 inputs: lane (g, t) = (lane / 4, lane % 4) brings word t
+// (inputs 8t .. 8t+7) of rows g and g + 8; b is its 16-byte B fragment, the
+// 8 inputs of column g at word t as [x0, x1, x2/16, x3/16, x4, x5, x6/16, x7/16].
+// Two MMAs: inputs 8t + {0,1,2,3} of every t, then 8t + {4,5,6,7}.
+__device__ __forceinline__ void dot16x32(float (&d)[4], uint32_t wg, uint32_t wg8, const uint4& b) {
+    uint32_t pg[4], ph[4];
+    codes16(wg, pg);
+    codes16(wg8, ph);
+    mma_f16(d, pg[0], ph[0], pg[1], ph[1], b.x, b.y);
+    mma_f16(d, pg[2], ph[2], pg[3], ph[3], b.z, b.w);
+}
+
+// 2^e as a float (|e| <= 126).
+__device__ __forceinline__ float exp2i(int e) { return __int_as_float((127 + e) << 23); }
+
+// The power of two that brings a largest magnitude m (m >= 0, as fp32 bits)
+// into [2^14, 2^15): fp16 then holds every value, below 65504.
+__device__ __forceinline__ int range_shift(uint32_t mbits) {
+    if (mbits == 0) return 0;
+    const int e = (int)(mbits >> 23) - 127;  // floor(log2 m) for normal m
+    return max(-100, min(100, 14 - e));
 }
 
 __device__ __forceinline__ float act_fn(float z, int act) {
@@ -115,89 +143,6 @@ __device__ __forceinline__ bool wait_value(const uint32_t* p, uint32_t want, vol
             if (abort && *abort) return false;
             if (ptx::globaltimer() - t0 > ptx::kWaitLimitNs) return false;
         }
-    }
-}
-
-// Word w of C 16-byte chunks (C = 1 or 2), by selects rather than an indexed
-// (local-memory) access when w is not a compile-time constant.
-template <int C>
-__device__ __forceinline__ uint32_t word_at(const uint4 (&c)[C], int w) {
-    const uint4 v = (C == 1 || w < 4) ? c[0] : c[C - 1];
-    const int k = w & 3;
-    return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
-}
-
-// Sum over the 8 C code words of C chunks (8 inputs each, for M matrices that
-// share the same inputs) of q * x for NT rows of x; xs points at the staged
-// inputs of the first word of the first row, rows `stride` apart. Each
-// (matrix, row) pair keeps two partial sums so the fused multiply-add chains
-// stay short.
-template <int NT, int M, int C>
-__device__ __forceinline__ void words_dot(const uint4 (&c)[M][C], const float* xs, int stride,
-                                          float (&out)[M][NT]) {
-    constexpr int W = 4 * C;
-    constexpr int A = 2;  // independent accumulators per (matrix, row); four measured no faster
-    float2 acc[M][NT][A];
-#pragma unroll
-    for (int m = 0; m < M; ++m)
-#pragma unroll
-        for (int j = 0; j < NT; ++j)
-#pragma unroll
-            for (int u = 0; u < A; ++u) acc[m][j][u] = make_float2(0.0f, 0.0f);
-    // with several rows of x, a full unroll would keep every word's activations
-    // live at once; two words at a time keeps the register count in bounds
-#pragma unroll(NT <= 2 ? W : 2)
-    for (int w = 0; w < W; ++w) {
-        float2 q[M][4];
-#pragma unroll
-        for (int m = 0; m < M; ++m) codes8(word_at<C>(c[m], w), q[m]);
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            const uint32_t xp = ptx::smem_addr(xs + j * stride + w * 8);
-            const float4 a = ptx::lds_f4(xp), b = ptx::lds_f4(xp + 16);
-#pragma unroll
-            for (int m = 0; m < M; ++m) {
-                acc[m][j][0] = __ffma2_rn(q[m][0], make_float2(a.x, a.y), acc[m][j][0]);
-                acc[m][j][1] = __ffma2_rn(q[m][1], make_float2(a.z, a.w), acc[m][j][1]);
-                acc[m][j][0] = __ffma2_rn(q[m][2], make_float2(b.x, b.y), acc[m][j][0]);
-                acc[m][j][1] = __ffma2_rn(q[m][3], make_float2(b.z, b.w), acc[m][j][1]);
-            }
-        }
-    }
-#pragma unroll
-    for (int m = 0; m < M; ++m)
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            const float2 s = __fadd2_rn(acc[m][j][0], acc[m][j][1]);
-            out[m][j] = (s.x + s.y) * kDotUnscale;
-        }
-}
-
-// As words_dot for one matrix and one 16-byte chunk (32 inputs), with the
-// position-scaled inputs already in registers (few rows of x only).
-template <int NT>
-__device__ __forceinline__ void chunk_dot_reg(const uint4 c, const float (&h)[NT][32], float (&out)[NT]) {
-    float2 acc[NT][2];
-#pragma unroll
-    for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = make_float2(0.0f, 0.0f);
-    const uint32_t words[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-        float2 q[4];
-        codes8(words[w], q);
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            const float* x = h[j] + 8 * w;
-            acc[j][0] = __ffma2_rn(q[0], make_float2(x[0], x[1]), acc[j][0]);
-            acc[j][1] = __ffma2_rn(q[1], make_float2(x[2], x[3]), acc[j][1]);
-            acc[j][0] = __ffma2_rn(q[2], make_float2(x[4], x[5]), acc[j][0]);
-            acc[j][1] = __ffma2_rn(q[3], make_float2(x[6], x[7]), acc[j][1]);
-        }
-    }
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-        const float2 s = __fadd2_rn(acc[j][0], acc[j][1]);
-        out[j] = (s.x + s.y) * kDotUnscale;
     }
 }
 
@@ -244,26 +189,127 @@ struct Shape {
     static constexpr int kDnTiles = kStageBytes / (kHalf + kSbBlock);  // down row tiles a stage can hold
 };
 
+// Shared memory after the ring and its barriers, for d_model d:
+//   xs   [NT][2d + 64 bytes]   token rows as B fragments (fp16), rows 64 bytes
+//                              apart modulo 128 so that a warp's loads of
+//                              eight rows meet no bank conflict
+//   kx   [d/64][4] float4      per group and lane t: -1024 * B sum and the
+//                              sum of x~ for tokens 2t and 2t+1
+//   red  [C][2][32][NT] f32    per-warp gate and up sums of the unit
+//   hb   [NPASS][8][4] uint4   B fragments of the unit's h (hi, lo columns)
+//   kh   [8] float4            per token: -1024 * B sum of hi, of lo, the
+//                              sum of h~, and 2^-s
+//   wmax [C][NT] u32           per-warp largest |x| (bf16 magnitude bits)
+//   xinv [NT] f32              2^-s of each staged token row
+template <int NT, int C>
+struct Smem {
+    static constexpr int kPass = (NT + 3) / 4;
+    static constexpr size_t ring = (size_t)Shape<C>::kStages * Shape<C>::kStageBytes + 16 * Shape<C>::kStages;
+    static __host__ __device__ size_t xstride(int d) { return 2 * (size_t)d + 64; }
+    static __host__ __device__ size_t xs(int) { return ring; }
+    static __host__ __device__ size_t kx(int d) { return xs(d) + NT * xstride(d); }
+    static __host__ __device__ size_t red(int d) { return kx(d) + (size_t)(d / 64) * 64; }
+    static __host__ __device__ size_t hb(int d) { return red(d) + (size_t)C * 2 * 32 * NT * 4; }
+    static __host__ __device__ size_t kh(int d) { return hb(d) + (size_t)kPass * 512; }
+    static __host__ __device__ size_t wmax(int d) { return kh(d) + 8 * 16; }
+    static __host__ __device__ size_t xinv(int d) { return wmax(d) + (size_t)C * NT * 4; }
+    static __host__ __device__ size_t total(int d) { return xinv(d) + NT * 4; }
+};
+
+// Stages the unit's token rows (rows row[0..nt-1] of x) as B fragments, with
+// the per-group sums, for every consumer thread (tid < 32 C). Pass 1 copies
+// the raw bf16 rows into shared memory and finds each row's largest
+// magnitude; pass 2 converts in place to fp16 at the row's scale.
+template <int NT, int C>
+__device__ __forceinline__ void stage_rows(const FfnArgs& a, const int (&row)[NT], int nt, unsigned char* smem,
+                                           int warp, int lane) {
+    using S = Smem<NT, C>;
+    const int d = a.d, nf = d >> 3;  // 16-byte fragments per row
+    const size_t xstride = S::xstride(d);
+    unsigned char* xs = smem + S::xs(d);
+    float* kx = reinterpret_cast<float*>(smem + S::kx(d));
+    uint32_t* wmax = reinterpret_cast<uint32_t*>(smem + S::wmax(d));
+    float* xinv = reinterpret_cast<float*>(smem + S::xinv(d));
+    const int tid = warp * 32 + lane;
+#pragma unroll
+    for (int q = 0; q < NT; ++q) {
+        if (q >= nt) continue;
+        const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)row[q] * d);
+        const uint32_t dst = ptx::smem_addr(xs + q * xstride);
+        uint32_t m2 = 0;  // two bf16 magnitudes, maxed lane-wise
+        for (int f = tid; f < nf; f += 32 * C) {
+            const uint4 v = __ldg(src + f);
+            ptx::sts_u4(dst + 16 * f, v);
+            m2 = __vmaxu2(m2, v.x & 0x7fff7fffu);
+            m2 = __vmaxu2(m2, v.y & 0x7fff7fffu);
+            m2 = __vmaxu2(m2, v.z & 0x7fff7fffu);
+            m2 = __vmaxu2(m2, v.w & 0x7fff7fffu);
+        }
+        uint32_t m = max(m2 & 0xffffu, m2 >> 16);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) m = max(m, __shfl_xor_sync(kFull, m, off));
+        if (lane == 0) wmax[warp * NT + q] = m;
+    }
+    ptx::named_sync(kBarCons, C * 32);
+#pragma unroll
+    for (int q = 0; q < NT; ++q) {
+        if (q >= nt) continue;
+        uint32_t m = 0;
+        for (int w = 0; w < C; ++w) m = max(m, wmax[w * NT + q]);
+        const int sh = range_shift(m << 16);  // bf16 bits -> fp32 bits
+        const float sc = exp2i(sh), sc16 = exp2i(sh - 4);
+        if (tid == 0) xinv[q] = exp2i(-sh);
+        const uint32_t base = ptx::smem_addr(xs + q * xstride);
+        // one fragment per lane; the 8 fragments of a group sit in 8 neighbouring lanes
+        for (int f0 = warp * 32; f0 < nf; f0 += 32 * C) {
+            const int f = f0 + lane;
+            float bsum = 0.0f, xsum = 0.0f;
+            if (f < nf) {
+                const uint4 v = ptx::lds_u4(base + 16 * f);
+                const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+                uint32_t out[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    // slots 2j, 2j+1; slots 2,3 and 6,7 (j odd) carry the factor 1/16
+                    const float lo = __uint_as_float(in[j] << 16), hi = __uint_as_float(in[j] & 0xffff0000u);
+                    const float s = (j & 1) ? sc16 : sc;
+                    const __half2 h = __floats2half2_rn(lo * s, hi * s);
+                    const float2 hf = __half22float2(h);
+                    bsum += hf.x + hf.y;
+                    xsum += (j & 1) ? 16.0f * (hf.x + hf.y) : hf.x + hf.y;
+                    out[j] = *reinterpret_cast<const uint32_t*>(&h);
+                }
+                ptx::sts_u4(base + 16 * f, make_uint4(out[0], out[1], out[2], out[3]));
+            }
+#pragma unroll
+            for (int off = 4; off >= 1; off >>= 1) {
+                bsum += __shfl_xor_sync(kFull, bsum, off);
+                xsum += __shfl_xor_sync(kFull, xsum, off);
+            }
+            if (f < nf && (f & 7) == 0) {
+                float* e = kx + ((f >> 3) * 4 + (q >> 1)) * 4 + (q & 1);
+                e[0] = -1024.0f * bsum;
+                e[2] = xsum;
+            }
+        }
+    }
+}
+
 template <int NT, int C, class L>
-__global__ void __launch_bounds__(Shape<C>::kThreads, (C <= 11 && NT == 1) ? 2 : 1)
+__global__ void __launch_bounds__(Shape<C>::kThreads, 1)
     ffn_kernel(const __grid_constant__ FfnArgs a, const __grid_constant__ L list) {
     constexpr int kCons = C;
     constexpr int kStages = Shape<C>::kStages;
     constexpr int kStageBytes = Shape<C>::kStageBytes;
     constexpr int kDnTiles = Shape<C>::kDnTiles;
+    using S = Smem<NT, C>;
+    constexpr int kPass = S::kPass;
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* ring = smem;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
     uint64_t* empty = full + kStages;
-    const int xs_stride = a.xs_stride;  // staged inputs per warp and row (a multiple of 64)
-    const int cpw = xs_stride / 64;     // staged groups per warp
-    float* xsw = reinterpret_cast<float*>(empty + kStages);  // [kCons][NT][xs_stride], position-scaled x
-    float* red = xsw + kCons * NT * xs_stride;               // [kCons][NT][2][32] per-warp gate/up sums
-    float* hs = red + kCons * NT * 2 * 32;                   // [NT][32] position-scaled h of the unit
-    float* xsumw = hs + NT * 32;                             // [kCons][NT][cpw] sums of staged groups
-    float* hsum = xsumw + kCons * NT * cpw;                  // [NT] sums of the unit's h
     __shared__ int abort_flag;
-    __shared__ int staged_key[kCons][2 + kFfnMaxNT];  // per warp: first group, rows, row indices
+    __shared__ int staged_key[1 + kFfnMaxNT];  // rows staged in xs: count, then row indices
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G1 = a.d >> 6, tiles_d = a.d >> 5;
@@ -279,13 +325,13 @@ __global__ void __launch_bounds__(Shape<C>::kThreads, (C <= 11 && NT == 1) ? 2 :
             ptx::mbar_init(empty + i, kCons);
         }
         abort_flag = 0;
+        staged_key[0] = -1;
         ptx::fence_mbar_init();
         if (tr) {
             tr[0] = ptx::globaltimer();
             for (int i = 1; i < kFfnTracePoints; ++i) tr[i] = 0;
         }
     }
-    if (threadIdx.x < kCons * 32 && lane == 0) staged_key[warp][0] = -1;
     __syncthreads();
     volatile int* abortp = &abort_flag;
     // the next kernel may start now: it waits for this one before it writes
@@ -394,15 +440,19 @@ __global__ void __launch_bounds__(Shape<C>::kThreads, (C <= 11 && NT == 1) ? 2 :
     // ---------------- consumers ----------------
     // Every consumer warp walks the same units and stages, whatever fails, so
     // the named barriers always see all of them.
+    const int g = lane >> 2, t = lane & 3;  // MMA fragment coordinates
+    const size_t xstride = S::xstride(a.d);
+    const uint32_t xs_a = ptx::smem_addr(smem + S::xs(a.d));
+    const uint32_t kx_a = ptx::smem_addr(smem + S::kx(a.d));
+    float* red = reinterpret_cast<float*>(smem + S::red(a.d));
+    unsigned char* hb = smem + S::hb(a.d);
+    float4* kh = reinterpret_cast<float4*>(smem + S::kh(a.d));
+    const float* xinv = reinterpret_cast<const float*>(smem + S::xinv(a.d));
     int slot = 0;
     uint32_t phase = 0;
-    float* xme = xsw + warp * NT * xs_stride;
-    float* xsme = xsumw + warp * NT * cpw;
-    int* key = staged_key[warp];
-    const int kchunk = a.kchunk;  // groups per staging pass, a multiple of kCons
     auto take_stage = [&]() -> const unsigned char* {
         // a sleeping wait: spinning would take issue slots from the warps
-        // (of this and the other resident CTA) that have data to work on
+        // that have data to work on
         const bool ok = ptx::mbar_wait_sleep(full + slot, phase, abortp);
         if (tr && warp == 0 && lane == 0 && tr[1] == 0) tr[1] = ptx::globaltimer();
         if (!ok && lane == 0 && !*abortp) {
@@ -432,83 +482,61 @@ __global__ void __launch_bounds__(Shape<C>::kThreads, (C <= 11 && NT == 1) ? 2 :
         int row[NT];
 #pragma unroll
         for (int q = 0; q < NT; ++q) row[q] = (q < nt ? list.pair[it.pb + q] : 0) / x_div;
+        // ---- the unit's token rows as B fragments, unless staged already ----
+        {
+            bool same = staged_key[0] == nt;
+#pragma unroll
+            for (int q = 0; q < NT; ++q) same = same && (q >= nt || staged_key[1 + q] == row[q]);
+            if (!same) {
+                stage_rows<NT, C>(a, row, nt, smem, warp, lane);
+                if (warp == 0 && lane == 0) {
+                    staged_key[0] = nt;
+#pragma unroll
+                    for (int q = 0; q < NT; ++q)
+                        if (q < nt) staged_key[1 + q] = row[q];
+                }
+                ptx::named_sync(kBarCons, kCons * 32);
+            }
+        }
         // ---- gate/up of rows 32c .. 32c+31 ----
-        float tot[2][NT];
+        // tot[m][rb][.]: matrix m, rows 16 rb + g (0, 1) and 16 rb + g + 8
+        // (2, 3), tokens 2t (0, 2) and 2t + 1 (1, 3)
+        float tot[2][2][4];
 #pragma unroll
         for (int m = 0; m < 2; ++m)
 #pragma unroll
-            for (int q = 0; q < NT; ++q) tot[m][q] = 0.0f;
-        // this warp's offsets within a stage, and its staged group of the pass
-        const uint32_t cb0 = ptx::smem_addr(ring) + warp * kRecord + lane * 16;
-        const uint32_t sb0 = ptx::smem_addr(ring) + warp * kRecord + 1024 + lane * 4;
-        int g0 = 0, i = 0;  // first group of the current staging pass, and the stage's index in it
-        for (int s0 = 0; s0 < G1; s0 += kCons, ++i) {
-            if (s0 == g0 + kchunk) {
-                g0 = s0;
-                i = 0;
-            }
-            if (i == 0) {
-                // this warp's groups of the pass, g0 + warp + kCons i, staged as
-                // position-scaled fp32 unless the same rows and pass are staged already
-                bool same = key[0] == g0 && key[1] == nt;
+            for (int rb = 0; rb < 2; ++rb)
 #pragma unroll
-                for (int q = 0; q < NT; ++q) same = same && (q >= nt || key[2 + q] == row[q]);
-                if (!same) {
-                    const int gend = min(g0 + kchunk, G1);
-                    const int ngw = gend > g0 + warp ? (gend - g0 - warp + kCons - 1) / kCons : 0;
+                for (int v = 0; v < 4; ++v) tot[m][rb][v] = 0.0f;
+        const uint32_t xrow = xs_a + (uint32_t)(min(g, nt - 1) * xstride) + t * 16;
+        for (int s0 = 0; s0 < G1; s0 += kCons) {
+            const unsigned char* st = take_stage();
+            const int grp = s0 + warp;
+            if (st && grp < G1) {
+                const uint32_t xa = xrow + grp * 128;
+                const uint4 xb[2] = {ptx::lds_u4(xa), ptx::lds_u4(xa + 64)};
+                const float4 k4 = ptx::lds_f4(kx_a + (grp * 4 + t) * 16);  // -K(2t), -K(2t+1), X(2t), X(2t+1)
+                const uint32_t rec0 = ptx::smem_addr(st) + warp * kRecord;
 #pragma unroll
-                    for (int q = 0; q < NT; ++q) {
-                        if (q >= nt) continue;
-                        const uint16_t* xr = a.x + (size_t)row[q] * a.d + 2 * lane;
-                        // up to 8 groups' loads in flight at once, then their sums and stores
-                        for (int i0 = 0; i0 < ngw; i0 += 8) {
-                            uint32_t r[8];
+                for (int m = 0; m < 2; ++m) {
+                    const uint32_t rec = rec0 + m * kCons * kRecord;
 #pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                if (i0 + j < ngw)
-                                    r[j] = __ldg(reinterpret_cast<const uint32_t*>(xr + (size_t)(g0 + warp + kCons * (i0 + j)) * 64));
+                    for (int rb = 0; rb < 2; ++rb) {
+                        float dd[4] = {k4.x, k4.y, k4.x, k4.y};
 #pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                if (i0 + j >= ngw) continue;
-                                const int i = i0 + j;
-                                const float v0 = bf16_lo(r[j]), v1 = bf16_hi(r[j]);
-                                float sum = v0 + v1;
-#pragma unroll
-                                for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
-                                // elements 2m and 2m+1 of each run of 8 sit at nibbles m and 4+m of the code word
-                                float* xo = xme + q * xs_stride + i * 64 + 8 * (lane >> 2);
-                                const int m = lane & 3;
-                                xo[m] = v0 * pos_scale(m);
-                                xo[4 + m] = v1 * pos_scale(4 + m);
-                                if (lane == 0) xsme[q * cpw + i] = sum;
-                            }
+                        for (int c = 0; c < 2; ++c) {
+                            const uint32_t wa = rec + c * 512 + rb * 256 + 4 * lane;
+                            dot16x32(dd, ptx::lds_u32(wa), ptx::lds_u32(wa + 128), xb[c]);
+                        }
+                        const float2 f0 = unpack_sb(ptx::lds_u32(rec + 1024 + (16 * rb + g) * 4));
+                        const float2 f1 = unpack_sb(ptx::lds_u32(rec + 1024 + (16 * rb + g + 8) * 4));
+                        tot[m][rb][0] = fmaf(f0.x, dd[0], fmaf(f0.y, k4.z, tot[m][rb][0]));
+                        tot[m][rb][2] = fmaf(f1.x, dd[2], fmaf(f1.y, k4.z, tot[m][rb][2]));
+                        if (NT > 1) {
+                            tot[m][rb][1] = fmaf(f0.x, dd[1], fmaf(f0.y, k4.w, tot[m][rb][1]));
+                            tot[m][rb][3] = fmaf(f1.x, dd[3], fmaf(f1.y, k4.w, tot[m][rb][3]));
                         }
                     }
-                    if (lane == 0) {
-                        key[0] = g0;
-                        key[1] = nt;
-#pragma unroll
-                        for (int q = 0; q < NT; ++q)
-                            if (q < nt) key[2 + q] = row[q];
-                    }
-                    __syncwarp();
-                }
-            }
-            const unsigned char* st = take_stage();
-            if (st && s0 + warp < G1) {
-                const uint32_t so = (uint32_t)(st - ring);  // the stage's offset in the ring
-                const uint32_t cb = cb0 + so, sbp = sb0 + so;
-                const uint4 words[2][2] = {{ptx::lds_u4(cb), ptx::lds_u4(cb + 512)},
-                                           {ptx::lds_u4(cb + kCons * kRecord), ptx::lds_u4(cb + kCons * kRecord + 512)}};
-                const float2 fg = unpack_sb(ptx::lds_u32(sbp));
-                const float2 fu = unpack_sb(ptx::lds_u32(sbp + kCons * kRecord));
-                float pr[2][NT];
-                words_dot<NT, 2, 2>(words, xme + i * 64, xs_stride, pr);
-#pragma unroll
-                for (int q = 0; q < NT; ++q) {
-                    const float xq = ptx::lds_f32(ptx::smem_addr(xsme + q * cpw + i));
-                    tot[0][q] += fmaf(fg.x, pr[0][q], fg.y * xq);
-                    tot[1][q] += fmaf(fu.x, pr[1][q], fu.y * xq);
                 }
             }
             release_stage();
@@ -517,25 +545,52 @@ __global__ void __launch_bounds__(Shape<C>::kThreads, (C <= 11 && NT == 1) ? 2 :
 #pragma unroll
         for (int m = 0; m < 2; ++m)
 #pragma unroll
-            for (int q = 0; q < NT; ++q) red[((warp * NT + q) * 2 + m) * 32 + lane] = tot[m][q];
+            for (int rb = 0; rb < 2; ++rb)
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const int tok = 2 * t + (v & 1);
+                    const int r = 16 * rb + g + 8 * (v >> 1);
+                    if ((NT > 1 || (v & 1) == 0) && tok < nt) red[((warp * 2 + m) * 32 + r) * NT + tok] = tot[m][rb][v];
+                }
         ptx::named_sync(kBarCons, kCons * 32);
-        if (warp < NT) {
+        if (warp < nt) {
             const int q = warp;
             float vg = 0.0f, vu = 0.0f;
 #pragma unroll
             for (int w = 0; w < kCons; ++w) {
-                vg += red[((w * NT + q) * 2 + 0) * 32 + lane];
-                vu += red[((w * NT + q) * 2 + 1) * 32 + lane];
+                vg += red[((w * 2 + 0) * 32 + lane) * NT + q];
+                vu += red[((w * 2 + 1) * 32 + lane) * NT + q];
             }
-            const float h = q < nt ? act_fn(vg, a.act) * vu : 0.0f;
-            float sum = h;
+            float gw = 1.0f;
+            if (un.fam != 0) {
+                ptx::pdl_wait();  // the gates were written by the router launch
+                gw = __ldg(a.gates + list.pair[it.pb + q]);
+            }
+            const float xi = xinv[q];
+            const float h = act_fn(vg * xi, a.act) * (vu * xi) * gw;
+            uint32_t mb = __float_as_uint(fabsf(h));
 #pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(kFull, sum, off);
-            // input lane of the down chunk: run lane / 8, element e = lane % 8 at slot e / 2 (+4 if odd)
+            for (int off = 16; off >= 1; off >>= 1) mb = max(mb, __shfl_xor_sync(kFull, mb, off));
+            const int sh = range_shift(mb);
+            const float ht = h * exp2i(sh);
+            const __half hi = __float2half_rn(ht);
+            const __half lo = __float2half_rn(ht - __half2float(hi));
             const int e = lane & 7;
-            const int sl = (e >> 1) + 4 * (e & 1);
-            hs[q * 32 + 8 * (lane >> 3) + sl] = h * pos_scale(sl);
-            if (lane == 0) hsum[q] = sum;
+            const bool scaled = (e & 2) != 0;  // slots 2, 3, 6, 7 carry the factor 1/16
+            const __half bhi = scaled ? __float2half_rn(__half2float(hi) * 0.0625f) : hi;
+            const __half blo = scaled ? __float2half_rn(__half2float(lo) * 0.0625f) : lo;
+            // column 2 (q % 4) holds hi, the next one lo, in pass q / 4
+            __half* frag = reinterpret_cast<__half*>(hb) + (((q >> 2) * 8 + 2 * (q & 3)) * 4 + (lane >> 3)) * 8 + e;
+            frag[0] = bhi;
+            frag[32] = blo;  // next column: 4 fragments of 8 halves further
+            float shi = __half2float(bhi), slo = __half2float(blo), hs = __half2float(hi) + __half2float(lo);
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) {
+                shi += __shfl_xor_sync(kFull, shi, off);
+                slo += __shfl_xor_sync(kFull, slo, off);
+                hs += __shfl_xor_sync(kFull, hs, off);
+            }
+            if (lane == 0) kh[q] = make_float4(-1024.0f * shi, -1024.0f * slo, hs, exp2i(-sh));
         }
         ptx::named_sync(kBarCons, kCons * 32);
         if (tr && first_unit && warp == 0 && lane == 0) tr[2] = ptx::globaltimer();
@@ -544,52 +599,43 @@ __global__ void __launch_bounds__(Shape<C>::kThreads, (C <= 11 && NT == 1) ? 2 :
         // add, wait until the previous kernel (and so everything before it)
         // has finished
         if (first_unit) ptx::pdl_wait();
-        // the gates were written by the router launch: read after the wait
-        float gate[NT];
+        uint4 hbv[kPass];
+        float4 khv[kPass];
+        float* yp[kPass];
 #pragma unroll
-        for (int q = 0; q < NT; ++q)
-            gate[q] = q < nt ? (un.fam == 0 ? 1.0f : __ldg(a.gates + list.pair[it.pb + q])) : 0.0f;
-        constexpr bool kHReg = NT <= 2;  // h of the unit in registers for the whole down pass
-        float hq[NT];
-        float hr[kHReg ? NT : 1][32];
-#pragma unroll
-        for (int q = 0; q < NT; ++q) hq[q] = hsum[q];
-        if (kHReg) {
-#pragma unroll
-            for (int q = 0; q < (kHReg ? NT : 1); ++q)
-#pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    const float4 v = *reinterpret_cast<const float4*>(hs + q * 32 + j);
-                    hr[q][j] = v.x;
-                    hr[q][j + 1] = v.y;
-                    hr[q][j + 2] = v.z;
-                    hr[q][j + 3] = v.w;
-                }
+        for (int p = 0; p < kPass; ++p) {
+            hbv[p] = ptx::lds_u4(ptx::smem_addr(hb) + ((p * 8 + g) * 4 + t) * 16);
+            const int tok = 4 * p + t;
+            khv[p] = kh[tok];
+            yp[p] = tok < nt ? a.y + (size_t)(list.pair[it.pb + tok] / x_div) * a.d : nullptr;
         }
-        // this lane's output element of row tile 0 in each token's y row
-        float* yq[NT];
-#pragma unroll
-        for (int q = 0; q < NT; ++q) yq[q] = a.y + (size_t)row[q] * a.d + lane;
-        const uint32_t dc0 = ptx::smem_addr(ring) + lane * 16;
-        const uint32_t ds0 = ptx::smem_addr(ring) + kDnTiles * kHalf + lane * 4;
         for (int r0 = 0; r0 < tiles_d; r0 += dn_per) {
             const int n = min(dn_per, tiles_d - r0);
             const unsigned char* st = take_stage();
             if (st) {
-                const uint32_t so = (uint32_t)(st - ring);
+                const uint32_t so = ptx::smem_addr(st);
                 for (int i = warp; i < n; i += kCons) {
-                    const uint4 words[1][1] = {{ptx::lds_u4(dc0 + so + i * kHalf)}};
-                    const float2 f = unpack_sb(ptx::lds_u32(ds0 + so + i * kSbBlock));
-                    float pr[1][NT];
-                    if constexpr (kHReg) {
-                        chunk_dot_reg<NT>(words[0][0], hr, pr[0]);
-                    } else {
-                        words_dot<NT, 1, 1>(words, hs, 32, pr);
-                    }
-                    const int col = 32 * (r0 + i);
+                    const uint32_t tile = so + i * kHalf + 4 * lane;
+                    const uint32_t sbt = so + kDnTiles * kHalf + i * kSbBlock + g * 4;
 #pragma unroll
-                    for (int q = 0; q < NT; ++q)
-                        if (q < nt) atomicAdd(yq[q] + col, gate[q] * fmaf(f.x, pr[0][q], f.y * hq[q]));
+                    for (int rb = 0; rb < 2; ++rb) {
+                        uint32_t pg[4], ph[4];
+                        codes16(ptx::lds_u32(tile + rb * 256), pg);
+                        codes16(ptx::lds_u32(tile + rb * 256 + 128), ph);
+                        const float2 f0 = unpack_sb(ptx::lds_u32(sbt + rb * 64));
+                        const float2 f1 = unpack_sb(ptx::lds_u32(sbt + rb * 64 + 32));
+                        const int col = 32 * (r0 + i) + 16 * rb + g;
+#pragma unroll
+                        for (int p = 0; p < kPass; ++p) {
+                            float dd[4] = {khv[p].x, khv[p].y, khv[p].x, khv[p].y};
+                            mma_f16(dd, pg[0], ph[0], pg[1], ph[1], hbv[p].x, hbv[p].y);
+                            mma_f16(dd, pg[2], ph[2], pg[3], ph[3], hbv[p].z, hbv[p].w);
+                            if (yp[p]) {
+                                atomicAdd(yp[p] + col, khv[p].w * fmaf(f0.x, dd[0] + dd[1], f0.y * khv[p].z));
+                                atomicAdd(yp[p] + col + 8, khv[p].w * fmaf(f1.x, dd[2] + dd[3], f1.y * khv[p].z));
+                            }
+                        }
+                    }
                 }
             }
             release_stage();
@@ -611,48 +657,33 @@ int sms() {
     return n;
 }
 
-// Shared memory: ring, barriers, per-warp staged inputs (NT rows of
-// `xs_stride` inputs), the cross-warp sums, h, and the group and h sums.
 template <int NT, int C>
-size_t ffn_smem(int xs_stride) {
-    return (size_t)Shape<C>::kStages * Shape<C>::kStageBytes + 2 * Shape<C>::kStages * sizeof(uint64_t) +
-           sizeof(float) * ((size_t)C * NT * xs_stride + (size_t)C * NT * 64 + NT * 32 +
-                            (size_t)C * NT * (xs_stride / 64) + NT);
+size_t ffn_smem(int d) {
+    return Smem<NT, C>::total(d);
 }
-
-// Staged groups per warp and pass: all of a row's when they fit kStageCap.
-constexpr int groups_per_warp_cap(int nt, int c) { return kStageCap / (4 * 64 * nt * c); }
 
 template <int NT, int C, class L>
 cudaError_t ffn_launch(FfnArgs a, const L& list, cudaStream_t s, bool pdl) {
     constexpr int kThreads = Shape<C>::kThreads;
-    const int cap = groups_per_warp_cap(NT, C);
-    static bool attr = false;
-    if (!attr) {
-        const int worst = ffn_smem<NT, C>(std::min(cap, (kMaxDModel / 64 + C - 1) / C) * 64);
-        cudaError_t e = cudaFuncSetAttribute(ffn_kernel<NT, C, L>, cudaFuncAttributeMaxDynamicSharedMemorySize, worst);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
-    const int G1 = a.d / 64;
-    const int gpw = std::min((G1 + C - 1) / C, cap);
-    a.xs_stride = gpw * 64;
-    a.kchunk = gpw * C;
+    cudaError_t e = ensure_smem_attr((const void*)ffn_kernel<NT, C, L>, ffn_smem<NT, C>(kMaxDModel));
+    if (e != cudaSuccess) return e;
     int units = 0;
     for (int f = 0; f < kFfnFams; ++f) {
         if (a.fam[f].n_items && (a.fam[f].inter % 32 || a.fam[f].x_div < 1)) return cudaErrorInvalidValue;
         units += a.fam[f].n_items * (a.fam[f].inter / 32);
     }
-    if (a.fam[0].n_items + a.fam[1].n_items != list.n_items || a.d % 256 || units == 0) return cudaErrorInvalidValue;
+    if (a.fam[0].n_items + a.fam[1].n_items != list.n_items || a.d % 256 || units == 0 ||
+        (reinterpret_cast<uintptr_t>(a.x) & 15))
+        return cudaErrorInvalidValue;
     // resident CTAs per SM at this launch's shared memory (cached per size)
-    const size_t smem = ffn_smem<NT, C>(a.xs_stride);
+    const size_t smem = ffn_smem<NT, C>(a.d);
     static size_t occ_smem[4] = {0, 0, 0, 0};
     static int occ_val[4] = {0, 0, 0, 0};
     int per_sm = 0;
     for (int i = 0; i < 4 && !per_sm; ++i)
         if (occ_smem[i] == smem) per_sm = occ_val[i];
     if (!per_sm) {
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ffn_kernel<NT, C, L>, kThreads, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ffn_kernel<NT, C, L>, kThreads, smem);
         if (e != cudaSuccess) return e;
         if (per_sm < 1) return cudaErrorInvalidConfiguration;
         for (int i = 3; i > 0; --i) {
@@ -675,9 +706,8 @@ cudaError_t launch_ffn(const FfnArgs& a, const L& list, cudaStream_t s, bool pdl
     if (list.n_items == 0) return cudaSuccess;
     int m = 0;
     for (int i = 0; i < list.n_items; ++i) m = std::max(m, (int)list.item[i].np);
-    // one row per item: 16 consumer warps (one CTA per SM); more rows need more
-    // registers per thread than 17 warps leave (at most 96 when one SM
-    // sub-partition holds five of them), and get 8
+    // one row per item: 16 consumer warps (one CTA per SM); more rows stage
+    // more token rows in shared memory and get 8 (a smaller ring)
     if (m <= 1) return ffn_launch<1, 16>(a, list, s, pdl);
     if (m <= 2) return ffn_launch<2, 8>(a, list, s, pdl);
     if (m <= 4) return ffn_launch<4, 8>(a, list, s, pdl);

@@ -840,11 +840,9 @@ cudaError_t launch_pf_gather(const uint16_t* x, int T, int d, const int32_t* pai
 
 cudaError_t launch_pf_gemm(const PfArgs& a, int phase, const void* b0, const void* b1, const int rows[2],
                            cudaStream_t s, int* launched) {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(pf_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    {
+        cudaError_t e = ensure_smem_attr((const void*)pf_gemm_kernel, kSmemBytes);
         if (e != cudaSuccess) return e;
-        attr = true;
     }
     if ((phase != 1 && phase != 2) || a.n_items < 1 || a.n_fam0 < 0 || a.n_fam0 > a.n_items || a.d % kTileM ||
         a.inter[0] % 64 || a.inter[1] % 64)

@@ -33,6 +33,11 @@ constexpr int kPromptMaxT = 4096;   // tokens of one layer-major prompt call
 // Records a message for moe_last_error() (thread-local) and returns s.
 moe_status set_error(moe_status s, const char* fmt, ...);
 
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per (kernel, device); thread-safe. The limit is a per-device
+// property of a kernel, so every device that launches it needs its own call.
+cudaError_t ensure_smem_attr(const void* kernel, size_t bytes);
+
 // MOE_OK if the shapes are ones the library supports, else MOE_EINVAL.
 moe_status check_shapes(const moe_shapes* s);
 
@@ -197,8 +202,6 @@ struct FfnArgs {
     float* y;            // [T][d] fp32, zero on entry: every unit adds its share
     const uint32_t* ready;
     unsigned* err;
-    int xs_stride;  // set by the launcher: staged inputs per warp and row
-    int kchunk;     // set by the launcher: gate/up groups staged at a time
     // optional diagnostics: per CTA, %globaltimer at kFfnTracePoints moments
     // (start, first weights landed, first unit's h ready, first unit done,
     // end); null = off

@@ -25,6 +25,8 @@
  *     from different threads.
  *   - Numeric formats: bf16 = bfloat16 bit patterns, f16 = IEEE binary16 bit
  *     patterns, both as uint16_t.
+ *   - Token rows x (bf16, device) must start on a 16-byte boundary (the
+ *     kernels read them 16 bytes at a time); a misaligned x gives MOE_EINVAL.
  */
 #ifndef MOE_H_
 #define MOE_H_
@@ -183,6 +185,9 @@ moe_status moe_route(moe_layer* layer, const void* x_bf16, int32_t T, const floa
  * Overlapping calls race: the scratch is shared by every layer on a device,
  * so two calls that may run at the same time (other streams, other threads)
  * corrupt each other's logits. Calls ordered on one stream are safe.
+ * Not timed: with moe_ctx_set_profiling on, these launches are counted by
+ * moe_ctx_launches but get no timing record in moe_ctx_kernel_times (a
+ * record would create CUDA events, and the call creates nothing).
  * Arguments, layouts and outputs as for moe_route.
  * Errors: MOE_EINVAL (bad arguments or over the limits), MOE_ESTATE (no
  * weights), MOE_ECUDA (the set-up lookup or the launch failed). */
