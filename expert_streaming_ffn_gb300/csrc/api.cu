@@ -34,6 +34,7 @@
 #include <new>
 #include <string>
 #include <thread>
+#include <type_traits>
 #include <vector>
 
 #include "moe_internal.h"
@@ -88,8 +89,9 @@ uint32_t device_nibble_order(const uint8_t* b) {
 // Device layout of one [N][K] int4 matrix: 32-row tiles, each a run of K/64
 // records, one per group of 64 inputs. Record (rt, g), at (rt * K/64 + g) *
 // 1152: the codes of chunk 2g for rows rt*32 + lane (16 bytes per lane), the
-// codes of chunk 2g+1 likewise, then one word per lane: fp16 scale | fp16 bias
-// << 16. So a row tile's consecutive groups are one contiguous copy.
+// codes of chunk 2g+1 likewise, then one word per row: fp16 scale | fp16 bias
+// << 16, row `lane` at position sb_pos(lane). So a row tile's consecutive
+// groups are one contiguous copy.
 void repack_qmatrix(const moe_qmatrix& m, int N, int K, uint8_t* dst) {
     const int G = K / 64;
     for (int n = 0; n < N; ++n) {
@@ -102,7 +104,7 @@ void repack_qmatrix(const moe_qmatrix& m, int N, int K, uint8_t* dst) {
                 for (int w = 0; w < 4; ++w) o[w] = device_nibble_order(src + (size_t)(2 * g + h) * 16 + 4 * w);
             }
             const size_t i = (size_t)n * G + g;
-            reinterpret_cast<uint32_t*>(rec + 1024)[lane] = (uint32_t)m.scale[i] | ((uint32_t)m.bias[i] << 16);
+            reinterpret_cast<uint32_t*>(rec + 1024)[sb_pos(lane)] = (uint32_t)m.scale[i] | ((uint32_t)m.bias[i] << 16);
         }
     }
 }
@@ -119,7 +121,7 @@ void repack_down(const moe_qmatrix& m, int N, int K, uint8_t* dst) {
         }
         for (int g = 0; g < G; ++g) {
             const size_t i = (size_t)n * G + g;
-            reinterpret_cast<uint32_t*>(sb)[((size_t)g * RT + rt) * 32 + lane] =
+            reinterpret_cast<uint32_t*>(sb)[((size_t)g * RT + rt) * 32 + sb_pos(lane)] =
                 (uint32_t)m.scale[i] | ((uint32_t)m.bias[i] << 16);
         }
     }
@@ -305,6 +307,11 @@ struct moe_layer {
     std::deque<StorePin> store_pins;  // in copy-stream order
     std::vector<cudaEvent_t> store_events;  // free events for store_pins
     std::vector<uint32_t> route_hist;
+    // the last one-token call's resident FFN launch, for moe_layer_replay_resident
+    bool record_resident = false;
+    bool have_resident = false;
+    FfnArgs resident_args{};
+    FfnSmall resident_list{};
 
     moe_layer(int E, int S_, int pol) : cache(E, S_, pol) {}
 };
@@ -793,6 +800,14 @@ moe_status launch_items(moe_layer* L, const std::vector<Item>& items, FfnArgs a,
         a.fam[0].n_items = n_fam[0];
         a.fam[1].n_items = n_fam[1];
         a.span = L->ctx->trace_span(kind, L->id, L->seq);
+        if constexpr (std::is_same<List, FfnSmall>::value) {
+            if (L->record_resident && i == 0 && j == items.size()) {
+                L->resident_args = a;
+                L->resident_args.span = nullptr;
+                L->resident_list = l;
+                L->have_resident = true;
+            }
+        }
         {
             Prof p(L->ctx, s, kind, bytes, flops);
             CUDA_TRY(launch_ffn(a, l, s, true));
@@ -869,7 +884,10 @@ moe_status run_resident_on_device(moe_layer* L, const uint16_t* x, float* y, cud
     a.slots = L->d_slots;
     a.ebytes = L->ebytes;
     *prof_index = L->ctx->profiling ? (long)L->ctx->prof.size() : -1;
-    return launch_items_any(L, items, a, K_FFN, s);
+    L->record_resident = true;
+    const moe_status st = launch_items_any(L, items, a, K_FFN, s);
+    L->record_resident = false;
+    return st;
 }
 
 // The routed experts of a decode call, added into y (which already holds the
@@ -1658,6 +1676,22 @@ extern "C" moe_status moe_ctx_launches(moe_ctx* C, uint64_t* out) {
 extern "C" moe_status moe_ctx_inject_copy_failure(moe_ctx* C, int64_t nth) {
     if (!C) return set_error(MOE_EINVAL, "ctx is NULL");
     C->fail_copy_at = nth < 0 ? -1 : C->copies_issued + nth;
+    return MOE_OK;
+}
+
+extern "C" moe_status moe_layer_replay_resident(moe_layer* L, void* stream, double* bytes) {
+    if (!L) return set_error(MOE_EINVAL, "layer is NULL");
+    if (!L->have_resident) return set_error(MOE_ESTATE, "moe_layer_replay_resident: no one-token call yet");
+    CUDA_TRY(cudaSetDevice(L->ctx->device));
+    // the routed items read the experts of the last routing that are resident now
+    double by = (double)L->shared_bytes;
+    const int k = L->sh.top_k;
+    if ((int)L->h_ids.size() < k) return set_error(MOE_ESTATE, "moe_layer_replay_resident: no routing recorded");
+    for (int p = 0; p < k; ++p)
+        if (L->cache.slot_of(L->h_ids[p]) >= 0) by += (double)L->ebytes;
+    CUDA_TRY(launch_ffn(L->resident_args, L->resident_list, (cudaStream_t)stream, true));
+    ++L->ctx->launches;
+    if (bytes) *bytes = by;
     return MOE_OK;
 }
 

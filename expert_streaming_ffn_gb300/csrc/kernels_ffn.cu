@@ -98,16 +98,54 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// d = A * B + c, m16n8k16, fp16 operands, fp32 accumulators.
+__device__ __forceinline__ void mma_f16c(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1, float c0, float c1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%10, %11, %10, %11};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
+}
+
 // 16 weight rows x 32 inputs: lane (g, t) = (lane / 4, lane % 4) brings word t
 // (inputs 8t .. 8t+7) of rows g and g + 8; b is its 16-byte B fragment, the
 // 8 inputs of column g at word t as [x0, x1, x2/16, x3/16, x4, x5, x6/16, x7/16].
-// Two MMAs: inputs 8t + {0,1,2,3} of every t, then 8t + {4,5,6,7}.
+// Two MMAs: inputs 8t + {0,1,2,3} of every t, then 8t + {4,5,6,7}. The
+// accumulators start at (c0, c1) for the columns 2t, 2t + 1 of both rows.
+__device__ __forceinline__ void dot16x32c(float (&d)[4], uint32_t wg, uint32_t wg8, const uint4& b, float c0,
+                                          float c1) {
+    uint32_t pg[4], ph[4];
+    codes16(wg, pg);
+    codes16(wg8, ph);
+    mma_f16c(d, pg[0], ph[0], pg[1], ph[1], b.x, b.y, c0, c1);
+    mma_f16(d, pg[2], ph[2], pg[3], ph[3], b.z, b.w);
+}
 __device__ __forceinline__ void dot16x32(float (&d)[4], uint32_t wg, uint32_t wg8, const uint4& b) {
     uint32_t pg[4], ph[4];
     codes16(wg, pg);
     codes16(wg8, ph);
     mma_f16(d, pg[0], ph[0], pg[1], ph[1], b.x, b.y);
     mma_f16(d, pg[2], ph[2], pg[3], ph[3], b.z, b.w);
+}
+
+// Four 8x8 matrices of 16-bit elements (rows of 16 bytes; lanes 8j..8j+7 give
+// the row addresses of matrix j): lane (g, t) receives word t of row g of
+// each, i.e. the MMA fragment words of 8 weight rows per matrix.
+template <int OFF>
+__device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4+%5];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr), "n"(OFF)
+                 : "memory");
+}
+template <int OFF>
+__device__ __forceinline__ uint4 lds4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4+%5];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr), "n"(OFF)
+                 : "memory");
+    return v;
 }
 
 // 2^e as a float (|e| <= 126).
@@ -198,7 +236,7 @@ struct Shape {
 //   red  [C][2][32][NT] f32    per-warp gate and up sums of the unit
 //   hb   [NPASS][8][4] uint4   B fragments of the unit's h (hi, lo columns)
 //   kh   [8] float4            per token: -1024 * B sum of hi, of lo, the
-//                              sum of h~, and 2^-s
+//                              sum of h~ times 2^-s, and 2^-s
 //   wmax [C][NT] u32           per-warp largest |x| (bf16 magnitude bits)
 //   xinv [NT] f32              2^-s of each staged token row
 template <int NT, int C>
@@ -441,6 +479,9 @@ __global__ void __launch_bounds__(Shape<C>::kThreads, 1)
     // Every consumer warp walks the same units and stages, whatever fails, so
     // the named barriers always see all of them.
     const int g = lane >> 2, t = lane & 3;  // MMA fragment coordinates
+    // this lane's ldmatrix row in a gate/up record: matrix lane / 8 is (chunk
+    // lane / 16, rows 0-7 or 8-15), row lane % 8 of it
+    const uint32_t lm_off = (lane >> 4) * 512 + ((lane >> 3) & 1) * 128 + (lane & 7) * 16;
     const size_t xstride = S::xstride(a.d);
     const uint32_t xs_a = ptx::smem_addr(smem + S::xs(a.d));
     const uint32_t kx_a = ptx::smem_addr(smem + S::kx(a.d));
@@ -513,23 +554,30 @@ __global__ void __launch_bounds__(Shape<C>::kThreads, 1)
             const unsigned char* st = take_stage();
             const int grp = s0 + warp;
             if (st && grp < G1) {
+                // this warp's gate and up records: the code words of rows
+                // 16 rb + g and 16 rb + g + 8 of both chunks (ldmatrix), and
+                // the scale words of rows g, g + 8, g + 16, g + 24
+                const uint32_t rec = ptx::smem_addr(st) + warp * kRecord;
+                uint32_t wd[2][2][4];
+                uint4 sbv[2];
+                ldsm4<0>(rec + lm_off, wd[0][0]);
+                ldsm4<256>(rec + lm_off, wd[0][1]);
+                ldsm4<kCons * kRecord>(rec + lm_off, wd[1][0]);
+                ldsm4<kCons * kRecord + 256>(rec + lm_off, wd[1][1]);
+                sbv[0] = lds4<1024>(rec + 16 * g);
+                sbv[1] = lds4<kCons * kRecord + 1024>(rec + 16 * g);
                 const uint32_t xa = xrow + grp * 128;
-                const uint4 xb[2] = {ptx::lds_u4(xa), ptx::lds_u4(xa + 64)};
+                const uint4 xb0 = lds4<0>(xa), xb1 = lds4<64>(xa);
                 const float4 k4 = ptx::lds_f4(kx_a + (grp * 4 + t) * 16);  // -K(2t), -K(2t+1), X(2t), X(2t+1)
-                const uint32_t rec0 = ptx::smem_addr(st) + warp * kRecord;
 #pragma unroll
                 for (int m = 0; m < 2; ++m) {
-                    const uint32_t rec = rec0 + m * kCons * kRecord;
 #pragma unroll
                     for (int rb = 0; rb < 2; ++rb) {
-                        float dd[4] = {k4.x, k4.y, k4.x, k4.y};
-#pragma unroll
-                        for (int c = 0; c < 2; ++c) {
-                            const uint32_t wa = rec + c * 512 + rb * 256 + 4 * lane;
-                            dot16x32(dd, ptx::lds_u32(wa), ptx::lds_u32(wa + 128), xb[c]);
-                        }
-                        const float2 f0 = unpack_sb(ptx::lds_u32(rec + 1024 + (16 * rb + g) * 4));
-                        const float2 f1 = unpack_sb(ptx::lds_u32(rec + 1024 + (16 * rb + g + 8) * 4));
+                        float dd[4];
+                        dot16x32c(dd, wd[m][rb][0], wd[m][rb][1], xb0, k4.x, k4.y);
+                        dot16x32(dd, wd[m][rb][2], wd[m][rb][3], xb1);
+                        const float2 f0 = unpack_sb(rb ? sbv[m].z : sbv[m].x);
+                        const float2 f1 = unpack_sb(rb ? sbv[m].w : sbv[m].y);
                         tot[m][rb][0] = fmaf(f0.x, dd[0], fmaf(f0.y, k4.z, tot[m][rb][0]));
                         tot[m][rb][2] = fmaf(f1.x, dd[2], fmaf(f1.y, k4.z, tot[m][rb][2]));
                         if (NT > 1) {
@@ -590,7 +638,7 @@ __global__ void __launch_bounds__(Shape<C>::kThreads, 1)
                 slo += __shfl_xor_sync(kFull, slo, off);
                 hs += __shfl_xor_sync(kFull, hs, off);
             }
-            if (lane == 0) kh[q] = make_float4(-1024.0f * shi, -1024.0f * slo, hs, exp2i(-sh));
+            if (lane == 0) kh[q] = make_float4(-1024.0f * shi, -1024.0f * slo, hs * exp2i(-sh), exp2i(-sh));
         }
         ptx::named_sync(kBarCons, kCons * 32);
         if (tr && first_unit && warp == 0 && lane == 0) tr[2] = ptx::globaltimer();
@@ -615,24 +663,26 @@ __global__ void __launch_bounds__(Shape<C>::kThreads, 1)
             if (st) {
                 const uint32_t so = ptx::smem_addr(st);
                 for (int i = warp; i < n; i += kCons) {
-                    const uint32_t tile = so + i * kHalf + 4 * lane;
-                    const uint32_t sbt = so + kDnTiles * kHalf + i * kSbBlock + g * 4;
+                    // rows 0-7, 8-15, 16-23, 24-31 of the tile: 16 bytes per row
+                    uint32_t wd[4];
+                    ldsm4<0>(so + i * kHalf + lane * 16, wd);
+                    const uint4 sbv = lds4<0>(so + kDnTiles * kHalf + i * kSbBlock + 16 * g);
 #pragma unroll
                     for (int rb = 0; rb < 2; ++rb) {
                         uint32_t pg[4], ph[4];
-                        codes16(ptx::lds_u32(tile + rb * 256), pg);
-                        codes16(ptx::lds_u32(tile + rb * 256 + 128), ph);
-                        const float2 f0 = unpack_sb(ptx::lds_u32(sbt + rb * 64));
-                        const float2 f1 = unpack_sb(ptx::lds_u32(sbt + rb * 64 + 32));
+                        codes16(wd[2 * rb], pg);
+                        codes16(wd[2 * rb + 1], ph);
+                        const float2 f0 = unpack_sb(rb ? sbv.z : sbv.x);
+                        const float2 f1 = unpack_sb(rb ? sbv.w : sbv.y);
                         const int col = 32 * (r0 + i) + 16 * rb + g;
 #pragma unroll
                         for (int p = 0; p < kPass; ++p) {
-                            float dd[4] = {khv[p].x, khv[p].y, khv[p].x, khv[p].y};
-                            mma_f16(dd, pg[0], ph[0], pg[1], ph[1], hbv[p].x, hbv[p].y);
+                            float dd[4];
+                            mma_f16c(dd, pg[0], ph[0], pg[1], ph[1], hbv[p].x, hbv[p].y, khv[p].x, khv[p].y);
                             mma_f16(dd, pg[2], ph[2], pg[3], ph[3], hbv[p].z, hbv[p].w);
                             if (yp[p]) {
-                                atomicAdd(yp[p] + col, khv[p].w * fmaf(f0.x, dd[0] + dd[1], f0.y * khv[p].z));
-                                atomicAdd(yp[p] + col + 8, khv[p].w * fmaf(f1.x, dd[2] + dd[3], f1.y * khv[p].z));
+                                atomicAdd(yp[p] + col, fmaf(f0.x * khv[p].w, dd[0] + dd[1], f0.y * khv[p].z));
+                                atomicAdd(yp[p] + col + 8, fmaf(f1.x * khv[p].w, dd[2] + dd[3], f1.y * khv[p].z));
                             }
                         }
                     }

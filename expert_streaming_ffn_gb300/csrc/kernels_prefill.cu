@@ -594,8 +594,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int codes_off = phase == 1 ? tile_raw * kUnit * kRecord + hh * 512 + rlane * 16
                                          : hh * 2048 + tile_raw * 512 + rlane * 16;
         const int codes_step = phase == 1 ? kRecord : 4096;
-        const int sb_off = phase == 1 ? tile_raw * kUnit * kRecord + 1024 + rlane * 4
-                                      : kUnit * 4096 + tile_raw * 128 + rlane * 4;
+        const int sb_off = phase == 1 ? tile_raw * kUnit * kRecord + 1024 + sb_pos(rlane) * 4
+                                      : kUnit * 4096 + tile_raw * 128 + sb_pos(rlane) * 4;
         const int sb_step = phase == 1 ? kRecord : 512;
         const int swz = rho & 7;
         int r = 0, s = 0;

@@ -101,10 +101,15 @@ void group_pairs(const int32_t* ids, int n_pairs, int n_experts, int32_t* offset
 //   codes: 16-byte chunk c (codes 32c..32c+31 of the row, canonical nibble
 //          order) of row n at ((rt * K/32 + c) * 32 + lane) * 16;
 //   sb:    (scale, bias) of group g as one 32-bit word (scale in the low half)
-//          at N*K/2 + ((rt * K/64 + g) * 32 + lane) * 4.
+//          at N*K/2 + ((rt * K/64 + g) * 32 + sb_pos(lane)) * 4.
 // An expert blob is [gate (I x d)][up (I x d)][down (d x I)]; its size equals
 // the canonical byte count, 27 * I * d / 16. Gate and up use this tiled
 // format, down the column-sliced one below.
+
+// Within each block of 32 scale/bias words (one per row of a 32-row tile),
+// row r's word sits at position 4 (r % 8) + r / 8, so that rows g, g + 8,
+// g + 16 and g + 24 (the rows of one MMA fragment lane) are 16 contiguous bytes.
+MOE_HD inline int sb_pos(int r) { return 4 * (r & 7) + (r >> 3); }
 
 MOE_HD inline size_t qmat_bytes(int N, int K) { return (size_t)N * (size_t)K / 2 + (size_t)N * (size_t)K / 16; }
 MOE_HD inline size_t expert_blob_bytes(int d, int inter) { return 2 * qmat_bytes(inter, d) + qmat_bytes(d, inter); }
@@ -116,7 +121,7 @@ void repack_qmatrix(const moe_qmatrix& m, int N, int K, uint8_t* dst);
 // so that the 32 columns one decode work unit needs are contiguous:
 //   codes: 16-byte chunk c of row n at ((c * N/32 + rt) * 32 + lane) * 16,
 //          i.e. 512-byte half-records ordered by (chunk, row tile);
-//   sb:    the word of group g of row n at N*K/2 + ((g * N/32 + rt) * 32 + lane) * 4,
+//   sb:    the word of group g of row n at N*K/2 + ((g * N/32 + rt) * 32 + sb_pos(lane)) * 4,
 //          i.e. 128-byte blocks ordered by (group, row tile).
 // Same size as the tiled format.
 void repack_down(const moe_qmatrix& m, int N, int K, uint8_t* dst);

@@ -129,9 +129,9 @@ def test_tiny_degenerate_caches_and_top_k(ctx, slots, k):
 
 
 def test_decode_2816_two_layers(ctx):
-    """decode_2816: layer 0 for all 64 decode steps of the workload (ids,
-    gates and the cache table checked at every step, y at the first, a middle
-    and the last), and layer 17 for 8 steps."""
+    """decode_2816: layer 0 for all 64 decode steps of the workload, with ids,
+    gates, the cache table and y checked at every step; and layer 17 for 8
+    steps."""
     s = synth.SHAPES_2816
     wl = synth.WORKLOADS["decode_2816"]
     for layer, steps in ((0, wl.steps), (17, 8)):
@@ -140,7 +140,7 @@ def test_decode_2816_two_layers(ctx):
         try:
             for step in range(steps):
                 x = synth.tokens(s, layer, step, 1, True)
-                r.forward(x, zb, check_y=step in (0, steps // 2, steps - 1))
+                r.forward(x, zb, check_y=True)
             st = moe.moe_layer_stats(r.h)
             assert st["steps"] == steps and st["hits"] > 0 and st["misses"] > 0
         finally:
@@ -150,15 +150,74 @@ def test_decode_2816_two_layers(ctx):
 @pytest.mark.parametrize("policy", [moe.LFU, moe.LRU])
 @pytest.mark.parametrize("T", [1, 8])
 def test_decode_2048_silu(ctx, T, policy):
-    """decode_2048 (SiLU, 64 slots) at batches 1 and 8 under both policies."""
+    """decode_2048 (SiLU, 64 slots) at batches 1 and 8 under both policies:
+    two layers for 64 steps each, long enough for the 64-slot cache to fill
+    and evict. Ids, gates and the cache table are checked at every step, y
+    on the first and last token of steps 0, 31 and 63."""
     s = synth.SHAPES_2048
     wl = synth.WORKLOADS["decode_2048"]
-    r = Rig(ctx, s, 3, wl.cache_slots, policy)
-    zb = synth.zipf_bias(s, 3, wl.zipf_s)
+    for layer in (3, 22):
+        r = Rig(ctx, s, layer, wl.cache_slots, policy)
+        zb = synth.zipf_bias(s, layer, wl.zipf_s)
+        try:
+            for step in range(64):
+                x = synth.tokens(s, layer, step, T, True)
+                r.forward(x, zb, check_y=step in (0, 31, 63), y_tokens=[0, T - 1])
+            st = moe.moe_layer_stats(r.h)
+            assert st["steps"] == 64 and st["misses"] > wl.cache_slots  # the slots filled and then evicted
+        finally:
+            r.close()
+
+
+def _tied_router(s, layer, tied):
+    """The layer's weights with router rows tied[1:] made copies of row tied[0]:
+    those experts get bit-identical logits for every input."""
+    w = synth.layer_weights(s, layer)
+    codes, scale, bias = (a.copy() for a in w.router)
+    for e in tied[1:]:
+        codes[e], scale[e], bias[e] = codes[tied[0]], scale[tied[0]], bias[tied[0]]
+    w.router = (codes, scale, bias)
+    return w
+
+
+@pytest.mark.parametrize("shapes,T", [(synth.SHAPES_TINY, 1), (synth.SHAPES_TINY, 37),
+                                      (synth.SHAPES_2816, 1), (synth.SHAPES_2816, 37)])
+def test_tied_logits_pick_the_lowest_expert_id(ctx, shapes, T):
+    """Equal logits go to the lower expert id first. Three router rows are made
+    identical; with a large equal bias on them they outrank every other expert,
+    so for top-2 the ids must be exactly [a, b] and for top-8 the first three
+    [a, b, c] with equal gates. Without the bias the tied experts compete with
+    the rest and the ids must still equal the oracle's stable order."""
+    s = shapes
+    tied = [3, 9, 14] if s.n_experts == 16 else [3, 9, 20]
+    w = _tied_router(s, 7, tied)
+    r = Rig(ctx, s, 7, 4 if s.n_experts == 16 else 16, weights=w)
     try:
-        for step in range(12):
-            x = synth.tokens(s, 3, step, T, True)
-            r.forward(x, zb, check_y=step in (0, 11), y_tokens=[0, T - 1])
+        xb = synth.tokens(s, 7, 0, T, s.n_experts != 16)
+        lg = oracle.router_logits(xb, w.router, s.n_experts, None)
+        assert (lg[:, tied[1:]] == lg[:, tied[:1]]).all()  # the ties are exact
+        zb = np.zeros(s.n_experts, np.float32)
+        zb[tied] = 40.0
+        ids, _ = r.forward(xb, zb, check_y=False)
+        n = min(s.top_k, len(tied))
+        assert (ids[:, :n] == np.array(tied[:n])).all(), ids[:, :n]
+        x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+        rid, rg = moe.moe_route(r.h, x, s.top_k, torch.from_numpy(zb).cuda())
+        torch.cuda.synchronize()
+        rg = rg.cpu().numpy()
+        assert (rid.cpu().numpy()[:, :n] == np.array(tied[:n])).all()
+        assert (rg[:, 1:n] == rg[:, :1]).all()  # equal logits, equal gates
+        # without the bias, and with a small one that puts the tie mid-rank:
+        # ties wherever the shared logit makes the top-k
+        zmid = np.zeros(s.n_experts, np.float32)
+        zmid[tied] = 1.5
+        for step in range(1, 7):
+            xb = synth.tokens(s, 7, step, T, s.n_experts != 16)
+            ids, _ = r.forward(xb, zmid if step % 2 else None, check_y=False)
+            both = np.isin(ids, tied).sum(axis=1) >= 2
+            for row in ids[both]:
+                pos = [int(np.where(row == e)[0][0]) for e in tied if e in row]
+                assert pos == sorted(pos)
     finally:
         r.close()
 

@@ -59,6 +59,10 @@ def _words(scale, bias):
     return np.asarray(scale, np.uint32) | (np.asarray(bias, np.uint32) << 16)
 
 
+# position of row r's scale word within a 32-word block: 4 (r % 8) + r // 8
+SB_ROW = np.array([4 * (r % 8) + r // 8 for r in range(32)])
+
+
 def test_file_layout_header_and_padding(expert_file):
     eb = moe.moe_expert_bytes(SHAPES)
     stride = moe.moe_store_expert_stride(SHAPES)
@@ -87,14 +91,14 @@ def test_each_region_holds_its_expert(expert_file, weights):
             # records of 1152 bytes per (32-row tile, group of 64): 32 lanes x
             # 2 chunks x 16 code bytes, then one scale|bias word per lane
             rec = r[m * gu:(m + 1) * gu].reshape(I // 32, d // 64, 1152)
-            words = rec[:, :, 1024:].copy().view(np.uint32)  # [rt][g][lane]
+            words = rec[:, :, 1024:].copy().view(np.uint32)[:, :, SB_ROW]  # [rt][g][row]
             want = _words(s, b).reshape(I // 32, 32, d // 64).transpose(0, 2, 1)
             assert (words == want).all(), (e, m)
             assert (_nibbles(rec[:, :, :1024]) == _nibbles(c)).all(), (e, m)
         # down, column-sliced: all codes first, then the words as 128-byte
         # blocks ordered by (group, row tile)
         dn = r[2 * gu:2 * gu + d * I // 2 + d * I // 16]
-        words = dn[d * I // 2:].copy().view(np.uint32).reshape(I // 64, d // 32, 32)
+        words = dn[d * I // 2:].copy().view(np.uint32).reshape(I // 64, d // 32, 32)[:, :, SB_ROW]
         want = _words(ds, db).reshape(d // 32, 32, I // 64).transpose(2, 0, 1)
         assert (words == want).all(), e
         assert (_nibbles(dn[:d * I // 2]) == _nibbles(dc)).all(), e
