@@ -48,8 +48,10 @@ def parse():
     # ~0.1-0.5 s of sparse copies after setup or idle (measured: the same steps
     # replayed run 2-4x faster), and LFU counts need steps to settle: the
     # default warm-up covers both, so the timed steps measure the steady state.
-    ap.add_argument("--steps", type=int, default=256)
-    ap.add_argument("--warmup", type=int, default=256)
+    ap.add_argument("--steps", type=int, default=128)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--prime-steps", type=int, default=256,
+                    help="untimed steps on other inputs that warm the caches before every pass")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (testing only)")
     ap.add_argument("--prefill-layers", type=int, default=2)
@@ -76,6 +78,13 @@ def parse():
                     help="run the stress sweep (2816 shapes, uniform routing) and print its JSON (not the bench line)")
     ap.add_argument("--stress-layers", type=int, default=8)
     ap.add_argument("--stress-steps", type=int, default=16)
+    ap.add_argument("--no-legs", action="store_true",
+                    help="skip the decode_2048, all-resident and stress legs of the default line")
+    ap.add_argument("--no-stress", action="store_true", help="skip the stress subset of the default line")
+    ap.add_argument("--resident-layers", type=int, default=8)
+    ap.add_argument("--layers-2048", type=int, default=40)
+    ap.add_argument("--stress-layers-line", type=int, default=4)
+    ap.add_argument("--stress-steps-line", type=int, default=6)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
@@ -285,35 +294,278 @@ def oracle_all_cores(wl, seconds: float):
     return sum(n / t for n, t in res), P
 
 
+def workload_config(wl, n_layers: int, slots: int, world: int, resident: bool = False) -> dict:
+    """The `config` object of a decode bench line (both arms)."""
+    s = wl.shapes
+    return {"workload": wl.name + (" (every expert resident)" if resident else ""),
+            "layers": n_layers, "tokens_per_step": wl.tokens, "d_model": s.d_model,
+            "experts": s.n_experts, "top_k": s.top_k, "d_ff": s.d_ff, "d_ff_shared": s.d_ff_shared,
+            "cache_slots": slots, "policy": "LFU" if wl.policy == 0 else "LRU", "zipf_s": wl.zipf_s,
+            "l2": "inputs larger than L2: 1.23 GB of weights read per token vs 129 MiB L2",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
+def _oracle_step_worker(task):
+    """One forked worker's share of a reference step: the given layer-tokens
+    (x of (step, layer)) through layer 0's weights."""
+    import synth
+
+    step, layers = task
+    L, zb, wl = _ORACLE_STATE
+    for layer in layers:
+        L.forward(synth.tokens(wl.shapes, layer, step, 1, wl.rms_normalise, wl.seed), zb)
+    return len(layers)
+
+
 def run_reference(args, world, rank):
-    """The reference arm: the CPU oracle as it stands, on the host cores (one
-    forked single-threaded copy per core, as cpu_baseline)."""
+    """The reference arm: the CPU oracle as it stands, on the host cores.
+
+    A step is one token through the workload's layers, split over one forked
+    single-threaded copy of the oracle per core (each copy takes every P-th
+    layer-token). Each layer-token runs the oracle's whole layer (router,
+    top-k, shared expert, the 8 routed experts, combine) on layer 0's weights
+    with the x of its own (step, layer); the per-layer work does not depend
+    on which layer's weights it reads. When --warmup + --steps whole tokens
+    would take more than about two minutes, a step is a bounded sample of
+    fewer layer-tokens, and the rate is scaled to tokens. Only rank 0 runs."""
+    import multiprocessing
+
+    import oracle
     import synth
 
     if rank != 0:
         return
+    global _ORACLE_STATE
     wl = synth.WORKLOADS["decode_2816"]
+    s = wl.shapes
     n_layers = args.layers or wl.n_layers
-    warm = oracle_layer_tokens(1, 0.0, wl, layers=(0,)) if args.warmup > 0 else []
-    seconds = float(min(60, max(10, args.steps)))
-    rate, P = oracle_all_cores(wl, seconds)  # layer-tokens per second over P cores
-    tok_s = rate / n_layers
-    sample = (f"{P} forked single-threaded copies of the oracle, each running whole layer-tokens of decode_2816 "
-              f"(layer 0) for {seconds:g} s; layer-tokens per second over all copies, divided by {n_layers} "
-              f"layers per token")
+    w = synth.layer_weights(s, 0, wl.seed)
+    zb = synth.zipf_bias(s, 0, wl.zipf_s, wl.zipf_beta, wl.seed) if wl.zipf_s else None
+    _ORACLE_STATE = (oracle.Layer(w, s), zb, wl)
+    P = os.cpu_count() or 1
+    t = time.perf_counter()
+    _ORACLE_STATE[0].forward(synth.tokens(s, 0, 0, 1, wl.rms_normalise, wl.seed), zb)
+    t_lt = time.perf_counter() - t  # one layer-token, single-threaded
+    n_steps = max(1, args.warmup + args.steps)
+    budget_s = 120.0
+    per_step = n_layers
+    if n_steps * -(-per_step // P) * t_lt > budget_s:
+        per_step = max(1, min(n_layers, int(budget_s / (n_steps * t_lt)) * P))
+    try:
+        with multiprocessing.get_context("fork").Pool(min(P, per_step)) as pool:
+            def one(step):
+                layers = list(range(per_step))
+                shares = [(step, layers[i::P]) for i in range(min(P, per_step))]
+                return sum(pool.map(_oracle_step_worker, shares))
+
+            for st in range(args.warmup):
+                one(st)
+            t0 = time.perf_counter()
+            for st in range(args.warmup, args.warmup + args.steps):
+                one(st)
+            elapsed = time.perf_counter() - t0
+    finally:
+        _ORACLE_STATE = None
+    tokens = args.steps * per_step / n_layers
+    tok_s = tokens / elapsed
+    sample = (f"each step: {per_step} of the {n_layers} layer-tokens of one decode_2816 token, split over "
+              f"{min(P, per_step)} forked single-threaded copies of the oracle (layer 0's weights, x per "
+              f"(step, layer)); tokens/s = steps x {per_step}/{n_layers} tokens / timed seconds")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": tok_s, "unit": "tok/s", "n_gpus": args.gpus,
-        "steps": int(rate * seconds), "warmup": len(warm), "ms_per_step": 1000.0 / tok_s,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * elapsed / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": "decode_2816", "layers": n_layers, "tokens_per_step": 1,
-                                        "cache_slots": 16, "policy": "LFU", "zipf_s": 1.1},
-        "cpu_baseline": {"value": tok_s, "unit": "tok/s", "cores": P, "kind": "oracle", "sample": sample},
+        "data": "synthetic (seeded int4/int8 weights and N(0,1) RMS-normalised bf16 activations)",
+        "config": workload_config(wl, n_layers, wl.cache_slots, world),
+        "cpu_baseline": {"value": tok_s, "unit": "tok/s", "cores": min(P, per_step), "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": tok_s, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
 
 # ---------------------------------------------------------------------------
 # our arm
+
+
+class DecodeRig:
+    """A stack of decode layers of one workload, their inputs resident in HBM
+    (x[step][layer][T][d] bf16, drawn per (step, layer)), and the passes the
+    bench times over them."""
+
+    def __init__(self, ctx, dev, stream, wl, n_layers, slots, policy, T, n_steps, seed, resident=False,
+                 weights=None, n_prime=0):
+        import torch
+
+        import expert_streaming_ffn_gb300 as moe
+        import synth
+
+        self.moe, self.torch, self.ctx, self.dev, self.stream = moe, torch, ctx, dev, stream
+        self.wl, self.s, self.L, self.T, self.resident = wl, wl.shapes, n_layers, T, resident
+        s = self.s
+        self.slots = s.n_experts if resident else slots
+        self.layers, self.zbs = [], []
+        w = weights
+        for l in range(n_layers):
+            w = synth.layer_weights(s, l, seed, reuse=w)
+            h = moe.moe_layer_create(ctx, s, self.slots, policy)
+            moe.moe_layer_set_weights(h, w)
+            self.layers.append(h)
+            self.zbs.append(torch.from_numpy(synth.zipf_bias(s, l, wl.zipf_s, wl.zipf_beta, seed)).to(dev)
+                            if wl.zipf_s else None)
+        self.last_weights = w
+        self.reset()
+        self.n_prime = 0 if resident else n_prime
+        # inputs of the timed steps, then of the priming steps (other draws)
+        xs = np.empty((n_steps + self.n_prime, n_layers, T, s.d_model), np.uint16)
+        for st in range(n_steps + self.n_prime):
+            draw = st if st < n_steps else 1_000_000 + st - n_steps
+            for l in range(n_layers):
+                xs[st, l] = synth.tokens(s, l, draw, T, wl.rms_normalise, seed)
+        self.xs_np = xs[:n_steps]
+        self.n_steps = n_steps
+        self.x_dev = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16).to(dev)
+        self.y_dev = torch.empty((n_layers, T, s.d_model), dtype=torch.float32, device=dev)
+        self.row = T * s.d_model * 2
+        self.primed_once = False
+
+    def reset(self):
+        """Empty caches (the cache trajectory starts again), or with every
+        expert resident, every expert copied back in."""
+        for h in self.layers:
+            self.moe.moe_cache_reset(h)
+            if self.resident:
+                self.moe.moe_cache_step(h, np.arange(self.s.n_experts))
+        self.torch.cuda.synchronize(self.dev)
+
+    def step(self, st):
+        base = self.x_dev.data_ptr() + st * self.L * self.row
+        sptr = self.stream.cuda_stream
+        for l in range(self.L):
+            zb = self.zbs[l]
+            self.moe.moe_forward_ptr(self.layers[l], base + l * self.row, self.T,
+                                     zb.data_ptr() if zb is not None else None, self.y_dev[l].data_ptr(), sptr)
+
+    def prime(self, seconds=1.0):
+        """Untimed, before every pass: empty caches, then the priming steps
+        (inputs drawn apart from the timed steps'), which leave the caches in
+        their steady state whatever the counted warm-up. The first time, the
+        priming steps repeat (from empty caches each time) until `seconds`
+        have passed: the host-to-device path runs slowly for the first few
+        hundred milliseconds of sparse copies after set-up."""
+        t0 = time.perf_counter()
+        while True:
+            self.reset()
+            for st in range(self.n_prime):
+                self.step(self.n_steps + st)
+            self.torch.cuda.synchronize(self.dev)
+            if self.primed_once or time.perf_counter() - t0 >= seconds or not self.n_prime:
+                break
+        self.primed_once = True
+
+    def run(self, warmup, steps, profile=False, clocks=None):
+        """Warm-up steps, then `steps` timed ones with CUDA events on the
+        launching stream. Returns (ms, stats per layer, kernel times or None,
+        launches)."""
+        moe, torch = self.moe, self.torch
+        for st in range(warmup):
+            self.step(st)
+        torch.cuda.synchronize(self.dev)
+        for h in self.layers:
+            moe.moe_layer_reset_stats(h)
+        if profile:
+            moe.moe_ctx_set_profiling(self.ctx, True)
+            moe.moe_ctx_reset_kernel_times(self.ctx)
+        launches0 = moe.moe_ctx_launches(self.ctx)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(self.dev)
+        ctxm = clocks if clocks is not None else _Null()
+        with ctxm:
+            ev0.record(self.stream)
+            for st in range(warmup, warmup + steps):
+                self.step(st)
+            ev1.record(self.stream)
+            torch.cuda.synchronize(self.dev)
+        launches = moe.moe_ctx_launches(self.ctx) - launches0
+        kt = None
+        if profile:
+            kt = moe.moe_ctx_kernel_times(self.ctx)
+            moe.moe_ctx_set_profiling(self.ctx, False)
+        return ev0.elapsed_time(ev1), [moe.moe_layer_stats(h) for h in self.layers], kt, launches
+
+    def close(self):
+        for h in self.layers:
+            self.moe.moe_layer_destroy(h)
+        self.layers = []
+        del self.x_dev, self.y_dev
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def _totals(stats):
+    keys = ("hits", "misses", "bypass", "bytes_h2d", "bytes_resident", "exposed_copy_us", "host_wait_us",
+            "host_issue_us")
+    return {k: sum(x[k] for x in stats) for k in keys}
+
+
+def _kernel_table(kt):
+    all_ms = sum(v[1] for v in kt.values())
+    return {k: {"launches": v[0], "ms": round(v[1], 4), "share": round(v[1] / all_ms, 4) if all_ms else 0,
+                "GB_s": round(v[2] / (v[1] * 1e-3) / 1e9, 1) if v[1] > 0 else None}
+            for k, v in kt.items() if v[0] > 0}
+
+
+def _leg_summary(rig, ms, stats, kt, steps, peaks):
+    """tokens/s and what moved, for one timed pass of a decode leg."""
+    tot = _totals(stats)
+    tokens = steps * rig.T
+    lookups = tot["hits"] + tot["misses"]
+    out = {"tok_s": tokens / (ms * 1e-3), "ms_per_layer_step": ms / steps / rig.L,
+           "hit_rate": tot["hits"] / lookups if lookups else None,
+           "resident_MB_per_token": tot["bytes_resident"] / tokens / 1e6,
+           "h2d_MB_per_token": tot["bytes_h2d"] / tokens / 1e6,
+           "hbm_GBs_over_wall": tot["bytes_resident"] / (ms * 1e-3) / 1e9}
+    if kt:
+        ffn = kt.get("expert_ffn")
+        if ffn and ffn[1] > 0:
+            gbs = ffn[2] / (ffn[1] * 1e-3) / 1e9
+            out["expert_ffn"] = {"GB_s": gbs, "frac": gbs / peaks["hbm_gbs"], "launches": ffn[0],
+                                 "mean_us": 1000 * ffn[1] / ffn[0], "bytes_per_launch": ffn[2] / ffn[0]}
+        out["kernels"] = _kernel_table(kt)
+    return out
+
+
+def ffn_replay_timing(layers, stream, rounds=4):
+    """Duration of the decode FFN launch without the per-launch overhead of a
+    pair of CUDA events (several microseconds on this part): each layer's last
+    one-token resident launch is replayed back to back, layer after layer (each
+    layer its own weights, so no launch finds them in L2), all enqueued by one
+    library call, and one pair of events on the launching stream brackets
+    `rounds` passes over the layers. Returns bytes per launch, microseconds per
+    launch and GB/s."""
+    import torch
+
+    import expert_streaming_ffn_gb300 as moe
+
+    torch.cuda.synchronize()
+    rs = torch.cuda.Stream()  # a stream of its own: the launches wait on nothing else
+    sptr = rs.cuda_stream
+    moe.moe_layers_replay_resident(layers, 1, sptr)  # one untimed pass
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(rs)
+    by = moe.moe_layers_replay_resident(layers, rounds, sptr)
+    ev1.record(rs)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    n = rounds * len(layers)
+    return {"launches": n, "bytes_per_launch": by / n, "us_per_launch": 1000.0 * ms / n,
+            "GB_s": by / (ms * 1e-3) / 1e9}
 
 
 def run_ours(args, world, rank, local):
@@ -337,124 +589,33 @@ def run_ours(args, world, rank, local):
     moe.load()
     steps_total = args.warmup + args.steps
     seed = wl.seed + 1000 * rank  # independent replicas
+    peaks, peak_src = measured_peaks()
 
     ctx = moe.moe_ctx_create(local)
-    layers, zbs = [], []
-    w = None
-    slots = s.n_experts if args.resident else wl.cache_slots
-    for l in range(n_layers):
-        w = synth.layer_weights(s, l, seed, reuse=w)
-        h = moe.moe_layer_create(ctx, s, slots, wl.policy)
-        moe.moe_layer_set_weights(h, w)
-        if args.resident:
-            moe.moe_cache_step(h, np.arange(s.n_experts))  # copies every expert into its slot
-        layers.append(h)
-        zbs.append(torch.from_numpy(synth.zipf_bias(s, l, wl.zipf_s, wl.zipf_beta, seed)).to(dev))
-    # inputs resident in HBM: x[step][layer][d] bf16, drawn per (step, layer)
-    xs_np = np.empty((steps_total, n_layers, s.d_model), np.uint16)
-    for st in range(steps_total):
-        for l in range(n_layers):
-            xs_np[st, l] = synth.tokens(s, l, st, 1, wl.rms_normalise, seed)[0]
-    x_dev = torch.from_numpy(xs_np.view(np.int16)).view(torch.bfloat16).to(dev)
-    y_dev = torch.empty((n_layers, s.d_model), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    sptr = stream.cuda_stream
-    row = s.d_model * 2
-
-    def reset_caches():
-        # empty caches (the cache trajectory starts again), or with --resident
-        # every expert copied back in
-        for h in layers:
-            moe.moe_cache_reset(h)
-            if args.resident:
-                moe.moe_cache_step(h, np.arange(s.n_experts))
-
-    def step(st):
-        base = x_dev.data_ptr() + st * n_layers * row
-        for l in range(n_layers):
-            moe.moe_forward_ptr(layers[l], base + l * row, 1, zbs[l].data_ptr(), y_dev[l].data_ptr(), sptr)
-
-    for st in range(args.warmup):
-        step(st)
-    torch.cuda.synchronize(dev)
-    for h in layers:
-        moe.moe_layer_reset_stats(h)
-    launches0 = moe.moe_ctx_launches(ctx)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    with ClockSampler(gpu_bus_id(local)) as clocks:
-        t_wall = time.perf_counter()
-        ev0.record(stream)
-        for st in range(args.warmup, steps_total):
-            step(st)
-        ev1.record(stream)
-        torch.cuda.synchronize(dev)
-        t_wall = time.perf_counter() - t_wall
-    barrier(world)
-    ms = ev0.elapsed_time(ev1)
-    launches = moe.moe_ctx_launches(ctx) - launches0
-    ms_max = max_over_ranks(ms, world)
-    stats = [moe.moe_layer_stats(h) for h in layers]
-    hits = sum(x["hits"] for x in stats)
-    misses = sum(x["misses"] for x in stats)
-    h2d = sum(x["bytes_h2d"] for x in stats)
-    resident = sum(x["bytes_resident"] for x in stats)
-    host_wait = sum(x["host_wait_us"] for x in stats)
-    host_issue = sum(x["host_issue_us"] for x in stats)
-
-    # same steps again, from the same cache state (empty caches, the same
-    # warm-up), with per-kernel CUDA events on the launching stream; the
-    # exposed copy time is measured in this pass too (it needs events)
-    reset_caches()
-    for st in range(args.warmup):
-        step(st)
-    torch.cuda.synchronize(dev)
-    for h in layers:
-        moe.moe_layer_reset_stats(h)
-    moe.moe_ctx_set_profiling(ctx, True)
-    moe.moe_ctx_reset_kernel_times(ctx)
-    for st in range(args.warmup, steps_total):
-        step(st)
-    torch.cuda.synchronize(dev)
-    kt = moe.moe_ctx_kernel_times(ctx)
-    moe.moe_ctx_set_profiling(ctx, False)
-    exposed = sum(moe.moe_layer_stats(h)["exposed_copy_us"] for h in layers)
-    peaks, peak_src = measured_peaks()
-    # The roofline kernel: the one with the most device time among those whose
-    # duration is HBM work. The decode launch over the experts copied in by
-    # the call (expert_ffn_miss) waits for the host-to-device copies, so its
-    # time is the host link's, reported beside the roofline instead.
-    hbm_kinds = {k: v for k, v in kt.items() if k != "expert_ffn_miss" and v[0] > 0}
-    dom = max(hbm_kinds.items(), key=lambda kv: kv[1][1])
-    name, (n_l, tot_ms, by, fl) = dom
-    achieved = by / (tot_ms * 1e-3) / 1e9 if tot_ms > 0 else 0.0
-    all_ms = sum(v[1] for v in kt.values())
-    all_bytes = sum(v[2] for v in kt.values())
-    kernels = {k: {"launches": v[0], "ms": round(v[1], 4), "share": round(v[1] / all_ms, 4) if all_ms else 0,
-                   "GB_s": round(v[2] / (v[1] * 1e-3) / 1e9, 1) if v[1] > 0 else None}
-               for k, v in kt.items() if v[0] > 0}
-
-    # end to end through the public call with host buffers: per step, the
-    # step's x (all layers) host->device from pinned memory, the 30 layer
-    # calls, and y device->host read back
+    rig = DecodeRig(ctx, dev, stream, wl, n_layers, wl.cache_slots, wl.policy, 1, steps_total, seed,
+                    resident=args.resident, n_prime=args.prime_steps)
+    slots = rig.slots
     e2e = None
     if not args.no_e2e:
-        x_host = torch.from_numpy(xs_np.view(np.int16)).view(torch.bfloat16).pin_memory()
+        x_host = torch.from_numpy(rig.xs_np.view(np.int16)).view(torch.bfloat16).pin_memory()
         x_stage = torch.empty((n_layers, s.d_model), dtype=torch.bfloat16, device=dev)
         y_host = torch.empty((n_layers, s.d_model), dtype=torch.float32).pin_memory()
+        sptr = stream.cuda_stream
 
         def e2e_step(st):
-            x_stage.copy_(x_host[st], non_blocking=True)
+            x_stage.copy_(x_host[st].view(n_layers, s.d_model), non_blocking=True)
             for l in range(n_layers):
-                moe.moe_forward_ptr(layers[l], x_stage[l].data_ptr(), 1, zbs[l].data_ptr(), y_dev[l].data_ptr(), sptr)
-            y_host.copy_(y_dev, non_blocking=True)
+                zb = rig.zbs[l]
+                moe.moe_forward_ptr(rig.layers[l], x_stage[l].data_ptr(), 1,
+                                    zb.data_ptr() if zb is not None else None, rig.y_dev[l].data_ptr(), sptr)
+            y_host.copy_(rig.y_dev.view(n_layers, s.d_model), non_blocking=True)
             torch.cuda.current_stream(dev).synchronize()
             return float(y_host[0, 0])
 
-        # the same cache trajectory as the timed loop: empty caches, the same
-        # warm-up steps, then the same timed steps
-        reset_caches()
+        # the same cache trajectory as the timed loop: primed caches, the
+        # same warm-up steps, then the same timed steps
+        rig.prime()
         for st in range(args.warmup):
             e2e_step(st)
         barrier(world)
@@ -464,7 +625,81 @@ def run_ours(args, world, rank, local):
         t_e2e = max_over_ranks(time.perf_counter() - t0, world)
         e2e = {"value": world * args.steps / t_e2e, "unit": "tok/s",
                "h2d_bytes_per_step": n_layers * s.d_model * 2, "d2h_bytes_per_step": n_layers * s.d_model * 4}
+    rig.prime()
+    barrier(world)
+    with ClockSampler(gpu_bus_id(local)) as clocks:
+        t_wall = time.perf_counter()
+        ms, stats, _, launches = rig.run(args.warmup, args.steps)
+        t_wall = time.perf_counter() - t_wall
+    barrier(world)
+    ms_max = max_over_ranks(ms, world)
+    tot = _totals(stats)
 
+    # end to end through the public call with host buffers, measured first
+    # (before the device-timed loop, next to it in time: the host link's speed
+    # drifts over a run): per step, the step's x (all layers) host->device
+    # from pinned memory, the 30 layer calls, and y device->host read back
+    # same steps again, from the same cache state (primed caches, the same
+    # warm-up), with per-kernel CUDA events on the launching stream; the
+    # exposed copy time is measured in this pass too (it needs events)
+    rig.prime()
+    _, pstats, kt, _ = rig.run(args.warmup, args.steps, profile=True)
+    exposed = sum(x["exposed_copy_us"] for x in pstats)
+    # The roofline kernel: the one with the most device time among those whose
+    # duration is HBM work. The decode launch over the experts copied in by
+    # the call (expert_ffn_miss) waits for the host-to-device copies, so its
+    # time is the host link's, reported beside the roofline instead.
+    hbm_kinds = {k: v for k, v in kt.items() if k != "expert_ffn_miss" and v[0] > 0}
+    dom = max(hbm_kinds.items(), key=lambda kv: kv[1][1])
+    name, (n_l, tot_ms, by, fl) = dom
+    single = {"GB_s": by / (tot_ms * 1e-3) / 1e9 if tot_ms > 0 else 0.0,
+              "us_per_launch": 1000.0 * tot_ms / n_l if n_l else None,
+              "bytes_per_launch": by / n_l if n_l else None,
+              "how": "a pair of CUDA events around every launch in a replay of the timed steps"}
+    replay = ffn_replay_timing(rig.layers, stream) if name == "expert_ffn" else None
+    if replay:
+        achieved, bpl = replay["GB_s"], replay["bytes_per_launch"]
+    else:
+        achieved, bpl = single["GB_s"], single["bytes_per_launch"]
+    all_ms = sum(v[1] for v in kt.values())
+    all_bytes = sum(v[2] for v in kt.values())
+
+    # predictive prefetch into HBM (one spare expert buffer per layer): the
+    # same steps from the same primed caches, so the hit rate is the same;
+    # what can change is the exposed copy time
+    prefetch = None
+    if not args.resident and not args.no_legs:
+        for h in rig.layers:
+            moe.moe_layer_set_prefetch(h, True)
+        rig.prime()
+        ms_p, st_p, _, _ = rig.run(args.warmup, args.steps)
+        rig.prime()
+        pf0 = [moe.moe_layer_prefetch_stats(h) for h in rig.layers]
+        _, pst_p, _, _ = rig.run(args.warmup, args.steps, profile=True)
+        pf1 = [moe.moe_layer_prefetch_stats(h) for h in rig.layers]
+        n_ls = rig.L * (args.warmup + args.steps)  # layer-steps of that pass
+        pf_issued = sum(b["issued"] - a["issued"] for a, b in zip(pf0, pf1)) / n_ls
+        pf_used = sum(b["used"] - a["used"] for a, b in zip(pf0, pf1)) / n_ls
+        tp = _totals(st_p)
+        for h in rig.layers:
+            moe.moe_layer_set_prefetch(h, False)
+        prefetch = {"spare_buffers_per_layer": 1,
+                    "off": {"tok_s": world * args.steps / (ms_max * 1e-3), "hit_rate": tot["hits"] / max(1, tot["hits"] + tot["misses"]),
+                            "exposed_copy_us_per_token": exposed / args.steps,
+                            "h2d_MB_per_token": tot["bytes_h2d"] / args.steps / 1e6},
+                    "on": {"tok_s": args.steps / (ms_p * 1e-3), "hit_rate": tp["hits"] / max(1, tp["hits"] + tp["misses"]),
+                           "exposed_copy_us_per_token": sum(x["exposed_copy_us"] for x in pst_p) / args.steps,
+                           "h2d_MB_per_token": tp["bytes_h2d"] / args.steps / 1e6,
+                           "prefetches_per_layer_step": pf_issued,
+                           "misses_served_from_hbm_per_layer_step": pf_used}}
+
+    weights = rig.last_weights
+    rig.close()
+
+    extra = {}
+    if not args.resident and world == 1 and not args.no_legs:
+        extra["resident_upper_bound"] = run_resident_bound(args, ctx, dev, stream, seed, peaks, weights)
+        extra["decode_2048"] = run_decode_2048(args, ctx, dev, stream, seed, peaks)
     prefill = None
     if not args.no_prefill and args.prefill_layers > 0:
         prefill = run_prefill(args, ctx, dev, stream, seed)
@@ -476,9 +711,10 @@ def run_ours(args, world, rank, local):
             storage["pinned_pool_ms_per_layer_token"] = ms_max / args.steps / n_layers
         except Exception as ex:  # noqa: BLE001 - the leg reports its failure; the bench line stands
             storage = {"error": f"{type(ex).__name__}: {ex}"}
+    if not args.no_stress and world == 1 and not args.resident and not args.no_legs:
+        extra["stress"] = run_stress(args, ctx, dev, stream, seed, layers=args.stress_layers_line,
+                                     steps=args.stress_steps_line)
 
-    for h in layers:
-        moe.moe_layer_destroy(h)
     moe.moe_ctx_destroy(ctx)
 
     cpu = None
@@ -501,36 +737,36 @@ def run_ours(args, world, rank, local):
     if rank != 0:
         return
     tok_s = world * args.steps / (ms_max * 1e-3)
-    lookups = hits + misses
+    lookups = tot["hits"] + tot["misses"]
     out = {
         "metric": METRIC, "value": tok_s, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded int4/int8 weights and N(0,1) RMS-normalised bf16 activations)",
-        "config": {"workload": "decode_2816" + (" (every expert resident)" if args.resident else ""),
-                   "layers": n_layers, "tokens_per_step": 1, "d_model": s.d_model,
-                   "experts": s.n_experts, "top_k": s.top_k, "d_ff": s.d_ff, "d_ff_shared": s.d_ff_shared,
-                   "cache_slots": slots, "policy": "LFU", "zipf_s": wl.zipf_s,
-                   "l2": f"inputs larger than L2: {resident / args.steps / 1e9:.2f} GB of weights read per step "
-                         f"vs {L2_BYTES / 2**20:.0f} MiB L2",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
-        "hit_rate": hits / lookups if lookups else None,
-        "h2d_MB_per_token": h2d / args.steps / 1e6,
+        "config": workload_config(wl, n_layers, slots, world, resident=args.resident),
+        "hit_rate": tot["hits"] / lookups if lookups else None,
+        "h2d_MB_per_token": tot["bytes_h2d"] / args.steps / 1e6,
         "exposed_copy_us_per_token": exposed / args.steps,
-        "host_wait_us_per_token": host_wait / args.steps,
-        "host_issue_us_per_token": host_issue / args.steps,
-        "resident_GB_per_token": resident / args.steps / 1e9,
+        "host_wait_us_per_token": tot["host_wait_us"] / args.steps,
+        "host_issue_us_per_token": tot["host_issue_us"] / args.steps,
+        "resident_GB_per_token": tot["bytes_resident"] / args.steps / 1e9,
         "hbm_GBs_all_kernels": all_bytes / (all_ms * 1e-3) / 1e9 if all_ms else None,
         "roofline": {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": ncu_traffic(name, by / n_l if n_l else None),
-                     "algorithmic_bytes_per_launch": by / n_l if n_l else None,
+                     "traffic": ncu_traffic(name, bpl),
+                     "algorithmic_bytes_per_launch": bpl,
+                     "timing": ("each layer's last resident launch replayed back to back, "
+                                f"{replay['launches']} launches between one pair of CUDA events")
+                     if replay else single["how"],
+                     "replay": replay, "single_launch_events": single,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                      else "fallback 6.8 TB/s"},
-        "kernels": kernels,
+        "kernels": _kernel_table(kt),
         "miss_launches": ({"kernel": "expert_ffn_miss", "bound": "host link (copies of missed experts)",
                            "launches": kt["expert_ffn_miss"][0], "ms": round(kt["expert_ffn_miss"][1], 4)}
                           if kt.get("expert_ffn_miss", (0, 0))[1] > 0 else None),
+        **extra,
+        "hbm_prefetch": prefetch,
         "prefill": prefill,
         "storage": storage,
         "cpu_baseline": cpu,
@@ -540,6 +776,74 @@ def run_ours(args, world, rank, local):
         "wall_s_timed_region": t_wall,
     }
     print(json.dumps(out), flush=True)
+
+
+def run_resident_bound(args, ctx, dev, stream, seed, peaks, weights=None):
+    """decode_2816 with every expert resident (S = E): the upper bound of the
+    decode layer with no host link in the way (the analogue of the pages'
+    all-in-memory baseline). --resident-layers layers (their weights, 0.9 GB
+    each, exceed L2 many times over), one token per step."""
+    import synth
+
+    wl = synth.WORKLOADS["decode_2816"]
+    L = args.resident_layers
+    warm, steps = 16, 64
+    rig = DecodeRig(ctx, dev, stream, wl, L, wl.cache_slots, wl.policy, 1, warm + steps, seed, resident=True,
+                    weights=weights)
+    try:
+        ms, stats, _, _ = rig.run(warm, steps)
+        _, pstats, kt, _ = rig.run(warm, steps, profile=True)
+        out = _leg_summary(rig, ms, stats, kt, steps, peaks)
+        rep = ffn_replay_timing(rig.layers, stream)
+        rep["frac"] = rep["GB_s"] / peaks["hbm_gbs"]
+        out.update({"workload": "decode_2816, every expert resident", "layers": L, "steps": steps,
+                    "tok_s_30_layers": out["tok_s"] * L / wl.n_layers, "expert_ffn_replay": rep})
+        # the ordered combine (bit-identical repeats): the same steps, its cost per layer
+        import expert_streaming_ffn_gb300 as moe
+
+        for h in rig.layers:
+            moe.moe_layer_set_deterministic(h, True)
+        rig.run(warm, steps)  # allocates the partial rows
+        ms_d, _, _, _ = rig.run(warm, steps)
+        out["ordered_combine"] = {"tok_s": steps / (ms_d * 1e-3), "ms_per_layer_step": ms_d / steps / L,
+                                  "extra_us_per_layer": 1000.0 * (ms_d - ms) / steps / L}
+        return out
+    finally:
+        rig.close()
+
+
+def run_decode_2048(args, ctx, dev, stream, seed, peaks):
+    """decode_2048: 40 layers (--layers-2048), SiLU, 64 slots, Zipf(0.9),
+    batches 1 and 8, under LFU and under LRU. 256 decode steps per run, the
+    first 64 as warm-up, after a priming pass."""
+    import synth
+
+    wl = synth.WORKLOADS["decode_2048"]
+    L = args.layers_2048
+    warm, steps = 64, 192
+    runs = []
+    weights = None
+    for policy, pname in ((0, "LFU"), (1, "LRU")):
+        for T in (1, 8):
+            rig = DecodeRig(ctx, dev, stream, wl.with_(tokens=T, policy=policy), L, wl.cache_slots, policy, T,
+                            warm + steps, seed, weights=weights, n_prime=16)
+            try:
+                # the host link out of its slow start, then the workload's 256
+                # steps from empty caches: the first 64 warm them
+                rig.prime(seconds=0.5)
+                rig.reset()
+                ms, stats, _, _ = rig.run(warm, steps)
+                rig.reset()
+                _, pstats, kt, _ = rig.run(warm, steps, profile=True)
+                out = _leg_summary(rig, ms, stats, kt, steps, peaks)
+                out["exposed_copy_us_per_token"] = sum(x["exposed_copy_us"] for x in pstats) / (steps * T)
+                out.update({"policy": pname, "batch": T})
+                runs.append(out)
+                weights = rig.last_weights
+            finally:
+                rig.close()
+    return {"workload": "decode_2048", "layers": L, "steps": steps, "warmup": warm, "slots": wl.cache_slots,
+            "runs": runs}
 
 
 def _prefill_pass(ctx, dev, stream, layers, xs, y, prompt=False):
@@ -819,7 +1123,7 @@ def run_storage(args, ctx, dev, stream, seed):
     return out
 
 
-def run_stress(args, ctx, dev, stream, seed):
+def run_stress(args, ctx, dev, stream, seed, layers=None, steps=None):
     """stress_2816: the 2816 shapes with uniform routing (no bias), decode
     batches of 1, 4, 16 and 64 tokens against caches of 8, 16 and 64 slots
     per layer, and a 4096-token prompt in chunks of 128 per cache size.
@@ -836,8 +1140,8 @@ def run_stress(args, ctx, dev, stream, seed):
 
     wl = synth.WORKLOADS["stress_2816"]
     s = wl.shapes
-    L = args.stress_layers
-    K = args.stress_steps
+    L = layers or args.stress_layers
+    K = steps or args.stress_steps
     ws, w = [], None
     for l in range(L):
         w = synth.layer_weights(s, l, seed, reuse=None)

@@ -114,6 +114,10 @@ SIGNATURES = [
     ("moe_store_tier", _i32, [_vp, _vp, _vp]),
     ("moe_layer_create_streamed", _i32, [_vp, _P(moe_shapes), _P(moe_quant_layout), _i32, _i32, _vp, _P(_vp)]),
     ("moe_layer_prefetch", _i32, [_vp, _i32, _P(_i32)]),
+    ("moe_layers_replay_resident", _i32, [_P(_vp), _i32, _i32, _vp, _P(ctypes.c_double)]),
+    ("moe_layer_set_deterministic", _i32, [_vp, _i32]),
+    ("moe_layer_set_prefetch", _i32, [_vp, _i32]),
+    ("moe_layer_prefetch_stats", _i32, [_vp, _P(ctypes.c_uint64), _P(ctypes.c_uint64)]),
 ]
 
 
@@ -245,6 +249,33 @@ def moe_route_noalloc(layer: int, x, zbias, ids, gates, stream=None):
     x bf16 [T][d], ids int32 [T][k], gates f32 [T][k] (T <= 64)."""
     _check(load().moe_route_noalloc(layer, _dptr(x), x.shape[0], _dptr(zbias), _dptr(ids), _dptr(gates),
                                     _stream(stream)), "moe_route_noalloc")
+
+
+def moe_layer_set_prefetch(layer: int, on: bool = True):
+    """Keep one spare expert buffer in HBM, refilled with the most-routed expert not cached."""
+    _check(load().moe_layer_set_prefetch(layer, int(bool(on))), "moe_layer_set_prefetch")
+
+
+def moe_layer_prefetch_stats(layer: int) -> dict:
+    issued, used = ctypes.c_uint64(0), ctypes.c_uint64(0)
+    _check(load().moe_layer_prefetch_stats(layer, ctypes.byref(issued), ctypes.byref(used)), "moe_layer_prefetch_stats")
+    return {"issued": issued.value, "used": used.value}
+
+
+def moe_layer_set_deterministic(layer: int, on: bool = True):
+    """Decode calls sum their output in a fixed order (bit-identical repeats)."""
+    _check(load().moe_layer_set_deterministic(layer, int(bool(on))), "moe_layer_set_deterministic")
+
+
+def moe_layers_replay_resident(layers, rounds: int = 1, stream=None) -> float:
+    """Enqueue, `rounds` times, each layer's last one-token resident FFN launch
+    (kernel timing only: each adds into its call's y again). Returns the
+    weight bytes all the launches read."""
+    arr = (_vp * len(layers))(*layers)
+    by = ctypes.c_double(0.0)
+    _check(load().moe_layers_replay_resident(arr, len(layers), rounds, _stream(stream), ctypes.byref(by)),
+           "moe_layers_replay_resident")
+    return by.value
 
 
 def moe_cache_reset(layer: int):

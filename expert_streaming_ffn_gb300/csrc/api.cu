@@ -307,6 +307,24 @@ struct moe_layer {
     std::deque<StorePin> store_pins;  // in copy-stream order
     std::vector<cudaEvent_t> store_events;  // free events for store_pins
     std::vector<uint32_t> route_hist;
+    // predictive prefetch into HBM (moe_layer_set_prefetch): one spare expert
+    // buffer, refilled after each call's misses with the most-routed expert
+    // that is not resident; a later miss of that expert copies from it
+    bool prefetch = false;
+    uint8_t* d_spare = nullptr;
+    int spare_expert = -1;           // the expert the spare buffer holds (or is being filled with)
+    int spare_miss_expert = -1;      // this call's miss served from the spare buffer, or -1
+    int spare_miss_slot = -1;        // ... and the slot it goes into (-1: it bypasses)
+    bool spare_call = false;         // the current call may serve a miss from the spare buffer
+    cudaEvent_t ev_spare_ready = nullptr;  // copy stream: the last prefetch into the spare landed
+    cudaEvent_t ev_spare_free = nullptr;   // compute stream: the last reads of the spare are done
+    bool spare_free_recorded = false;
+    uint64_t prefetch_issued = 0, prefetch_used = 0;
+    // ordered (deterministic) decode combine: per-unit partial rows, then a
+    // reduce in a fixed order (moe_layer_set_deterministic)
+    bool deterministic = false;
+    float* d_dpart = nullptr;
+    size_t dpart_floats = 0;
     // the last one-token call's resident FFN launch, for moe_layer_replay_resident
     bool record_resident = false;
     bool have_resident = false;
@@ -402,6 +420,27 @@ moe_status ensure_scratch(moe_layer* L, int T) {
     memset(L->h_pub, 0, sizeof(unsigned long long) * pairs);
     L->h_ids.assign(pairs, 0);
     L->cap_T = T;
+    return MOE_OK;
+}
+
+// Partial rows of the ordered decode combine for T tokens: the shared
+// expert's chunks per token, then the routed chunks per pair.
+size_t det_part_floats(const moe_shapes& s, int T) {
+    return (size_t)T * ((size_t)(s.d_ff_shared / 32) + (size_t)s.top_k * (s.d_ff / 32)) * s.d_model;
+}
+
+moe_status ensure_det_scratch(moe_layer* L, int T) {
+    const size_t need = det_part_floats(L->sh, T);
+    if (need <= L->dpart_floats) return MOE_OK;
+    if (L->ev_done) CUDA_TRY(cudaEventSynchronize(L->ev_done));  // the old buffer may still be in use
+    cudaFree(L->d_dpart);
+    L->d_dpart = nullptr;
+    L->dpart_floats = 0;
+    if (cudaMalloc(&L->d_dpart, sizeof(float) * need) != cudaSuccess) {
+        cudaGetLastError();
+        return set_error(MOE_ENOMEM, "ordered-combine scratch for %d tokens (%zu floats) failed", T, need);
+    }
+    L->dpart_floats = need;
     return MOE_OK;
 }
 
@@ -685,6 +724,17 @@ moe_status issue_miss_copies(moe_layer* L, const StepResult& r, bool with_bypass
         const int slot = r.miss_slots[i];
         if (slot < 0 && !with_bypass) continue;
         uint8_t* dst = slot >= 0 ? L->d_slots + (size_t)slot * L->ebytes : C->staging + (size_t)(nb++) * L->ebytes;
+        if (L->spare_call && r.miss_experts[i] == L->spare_expert) {
+            // prefetched: no copy over the host link; the call's kernels read
+            // the spare buffer, and the compute stream then copies it into the
+            // slot (run_experts)
+            if (slot < 0) --nb;  // it takes no staging entry
+            L->spare_miss_expert = r.miss_experts[i];
+            L->spare_miss_slot = slot;
+            L->spare_expert = -1;
+            ++L->prefetch_used;
+            continue;
+        }
         copies.push_back(Copy{i, dst, L->h_pool + (size_t)r.miss_experts[i] * L->ebytes});
     }
     const bool flags = ready_of_miss != nullptr;
@@ -840,7 +890,27 @@ FfnArgs decode_args(moe_layer* L, const uint16_t* x, float* y) {
     a.ready = L->d_ready;
     a.err = L->ctx->err_dev;
     a.trace = nullptr;
+    if (L->deterministic && L->d_dpart) {
+        // partial rows: the shared expert's by token, then the routed by pair
+        const int cs = sh.d_ff_shared / 32, cr = sh.d_ff / 32;
+        const size_t cap = L->dpart_floats / ((size_t)(cs + sh.top_k * cr) * sh.d_model);
+        a.part[0] = L->d_dpart;
+        a.part[1] = L->d_dpart + cap * cs * sh.d_model;
+        a.part_c[0] = cs;
+        a.part_c[1] = cr;
+    }
     return a;
+}
+
+// The ordered combine of a decode call: y = shared + ranks 0..k-1, from the
+// partial rows the call's FFN launches wrote.
+moe_status reduce_parts(moe_layer* L, int T, float* y, cudaStream_t s) {
+    const moe_shapes& sh = L->sh;
+    const FfnArgs a = decode_args(L, nullptr, y);
+    Prof p(L->ctx, s, K_COMBINE, 4.0 * (double)det_part_floats(sh, T) + 4.0 * T * sh.d_model,
+           (double)det_part_floats(sh, T));
+    CUDA_TRY(launch_part_reduce(a.part[0], a.part[1], a.part_c[0], a.part_c[1], sh.top_k, sh.d_model, T, y, s, true));
+    return MOE_OK;
 }
 
 // The shared expert of a decode call on every token. It needs no routing, so
@@ -851,7 +921,9 @@ moe_status run_shared(moe_layer* L, const uint16_t* x, int T, float* y, cudaStre
     std::vector<Item> items;
     for (int t0 = 0; t0 < T; t0 += kFfnMaxNT)
         items.push_back(Item{L->d_shared, t0, std::min(T, t0 + kFfnMaxNT), nullptr, -1, -1, 0});
-    return launch_items_any(L, items, decode_args(L, x, y), K_FFN, s);
+    FfnArgs a = decode_args(L, x, y);
+    if (L->deterministic && T > 1) a.min_nt = 2;
+    return launch_items_any(L, items, a, K_FFN, s);
 }
 
 // `zero_y`, when given, is the call's [T][d] fp32 output, zeroed by the same launch.
@@ -944,7 +1016,9 @@ moe_status run_experts(moe_layer* L, const uint16_t* x, int T, float* y, const s
         const bool is_miss = mi < L->step.miss_experts.size() && L->step.miss_experts[mi] == e;
         const int slot = is_miss ? L->step.miss_slots[mi] : L->cache.slot_of(e);
         const uint8_t* w;
-        if (slot >= 0) {
+        if (is_miss && e == L->spare_miss_expert) {
+            w = L->d_spare;  // prefetched into HBM
+        } else if (slot >= 0) {
             w = L->d_slots + (size_t)slot * L->ebytes;
         } else {
             w = C->staging + (size_t)nb * L->ebytes;
@@ -956,6 +1030,7 @@ moe_status run_experts(moe_layer* L, const uint16_t* x, int T, float* y, const s
                 .push_back(Item{w, b, std::min(b + kFfnMaxNT, (int)L->offsets[e + 1]), L->perm.data(), f.gu, f.dn, 1});
     }
     FfnArgs a = decode_args(L, x, y);
+    if (L->deterministic && T > 1) a.min_nt = 2;  // one kernel shape for every launch of the call
     moe_status st = device_hits ? MOE_OK : launch_items_any(L, items, a, K_FFN, s);
     if (st != MOE_OK) return st;
     std::vector<std::pair<int, int>> upd;
@@ -980,8 +1055,23 @@ moe_status run_experts(moe_layer* L, const uint16_t* x, int T, float* y, const s
         w.copies_done = copies_done;
         CUDA_TRY(cudaEventRecord(w.ffn_start, s));
     }
+    // a miss served from the spare buffer: its kernels wait for the prefetch
+    // copy (an event, not a flag: no kernel spins on it)
+    if (L->spare_miss_expert >= 0) CUDA_TRY(cudaStreamWaitEvent(s, L->ev_spare_ready, 0));
     st = launch_items_any(L, miss, a, K_FFN_MISS, s);
     if (copies_done) L->waits.push_back(w);
+    if (st == MOE_OK && L->spare_miss_expert >= 0) {
+        // then the spare's bytes go into the expert's slot, on this stream,
+        // after the kernels that read the spare; the next prefetch into the
+        // spare waits for this copy
+        if (L->spare_miss_slot >= 0)
+            CUDA_TRY(cudaMemcpyAsync(L->d_slots + (size_t)L->spare_miss_slot * L->ebytes, L->d_spare, L->ebytes,
+                                     cudaMemcpyDeviceToDevice, s));
+        CUDA_TRY(cudaEventRecord(L->ev_spare_free, s));
+        L->spare_free_recorded = true;
+    }
+    L->spare_miss_expert = -1;
+    L->spare_miss_slot = -1;
     return st;
 }
 
@@ -1120,6 +1210,34 @@ double us_since(std::chrono::steady_clock::time_point t) {
 
 // One call: at most kPrefillChunk tokens from moe_forward, or a whole
 // layer-major prompt from moe_forward_prompt.
+// The prefetch of a decode call, queued on the copy stream after the call's
+// kernels were enqueued: the expert routed in the most steps so far (ties to the lower id)
+// that is neither in a slot nor already in the spare buffer goes into the
+// spare buffer ([P1] §9.2 item 3, §9.5 item 2: predict the next experts from
+// routing history and read them ahead). The cache trace does not change: a
+// later miss of that expert is still a miss, copied from the spare buffer.
+moe_status issue_prefetch(moe_layer* L) {
+    int best = -1;
+    uint32_t best_n = 0;
+    for (int e = 0; e < L->sh.n_experts; ++e) {
+        const uint32_t n = L->route_hist[(size_t)e];
+        if (n > best_n && L->cache.slot_of(e) < 0) {
+            best = e;
+            best_n = n;
+        }
+    }
+    if (best < 0 || best == L->spare_expert) return MOE_OK;
+    // the spare buffer may still be read by earlier kernels or copied into a slot
+    if (L->spare_free_recorded) CUDA_TRY(cudaStreamWaitEvent(L->ctx->copy_stream, L->ev_spare_free, 0));
+    CUDA_TRY(cudaMemcpyAsync(L->d_spare, L->h_pool + (size_t)best * L->ebytes, L->ebytes, cudaMemcpyHostToDevice,
+                             L->ctx->copy_stream));
+    CUDA_TRY(cudaEventRecord(L->ev_spare_ready, L->ctx->copy_stream));
+    L->spare_expert = best;
+    ++L->prefetch_issued;
+    L->stats.bytes_h2d += L->ebytes;
+    return MOE_OK;
+}
+
 moe_status forward_chunk(moe_layer* L, const uint16_t* x, int T, const float* zbias, float* y, int32_t* ids_out,
                          float* gates_out, cudaStream_t s) {
     moe_ctx* C = L->ctx;
@@ -1142,6 +1260,10 @@ moe_status forward_chunk(moe_layer* L, const uint16_t* x, int T, const float* zb
     ++L->seq;
     // a decode call's experts add into y, which the router launch zeroes
     const bool decode = T <= kDecodeMaxT;
+    if (decode && L->deterministic) {
+        moe_status st = ensure_det_scratch(L, std::max(T, L->cap_T));
+        if (st != MOE_OK) return st;
+    }
     // one token: the hits are found on the device (the work list holds the
     // shared item and the k pairs)
     const bool device_routed = T == 1 && 1 + sh.top_k <= (int)(sizeof(FfnSmall::item) / sizeof(FfnItem));
@@ -1167,7 +1289,7 @@ moe_status forward_chunk(moe_layer* L, const uint16_t* x, int T, const float* zb
     L->slot_before = L->cache.slot_expert;
     if (!L->cache.step(L->h_ids.data(), npairs, L->step))
         return set_error(MOE_ESTATE, "router produced an invalid id");
-    if (L->store)
+    if (L->store || L->prefetch)
         for (int e : L->step.distinct) ++L->route_hist[(size_t)e];
     if (device_routed) {
         // the resident launch counted every routed pair as a hit
@@ -1185,7 +1307,9 @@ moe_status forward_chunk(moe_layer* L, const uint16_t* x, int T, const float* zb
     L->stats.bypass += L->step.bypass;
     const uint32_t epoch = ++L->epoch;
     std::vector<MissFlags> ready_of_miss;
+    L->spare_call = L->prefetch && T <= kDecodeMaxT;
     st = issue_miss_copies(L, L->step, true, epoch, &ready_of_miss, L->step.miss_experts.size() <= kFlagGroup);
+    L->spare_call = false;
     C->trace_mark("copies", L->id, L->seq);
     if (st != MOE_OK) {
         table_upload(L, s);  // the failed slots were emptied: the device table follows
@@ -1201,6 +1325,8 @@ moe_status forward_chunk(moe_layer* L, const uint16_t* x, int T, const float* zb
         if (st == MOE_OK && L->slot_before != L->cache.slot_expert) st = table_upload(L, s);
     } else {
         st = run_experts(L, x, T, y, ready_of_miss, copies_done, s, device_routed);
+        if (st == MOE_OK && L->deterministic) st = reduce_parts(L, T, y, s);
+        if (st == MOE_OK && L->prefetch) st = issue_prefetch(L);
     }
     if (st != MOE_OK) return st;
     if (ids_out) CUDA_TRY(cudaMemcpyAsync(ids_out, L->d_ids, sizeof(int32_t) * npairs, cudaMemcpyDeviceToDevice, s));
@@ -1330,6 +1456,10 @@ extern "C" void moe_layer_destroy(moe_layer* L) {
     cudaStreamSynchronize(L->ctx->copy_stream);
     drain_waits(L);
     free_scratch(L);
+    cudaFree(L->d_dpart);
+    cudaFree(L->d_spare);
+    if (L->ev_spare_ready) cudaEventDestroy(L->ev_spare_ready);
+    if (L->ev_spare_free) cudaEventDestroy(L->ev_spare_free);
     if (L->store) {
         release_store_pins(L, true);
         for (cudaEvent_t e : L->store_events) cudaEventDestroy(e);
@@ -1467,6 +1597,7 @@ extern "C" moe_status moe_layer_prefetch(moe_layer* L, int32_t n, int32_t* queue
 }
 
 extern "C" moe_status moe_layer_set_weights(moe_layer* L, const moe_host_weights* w) {
+    L->spare_expert = -1;  // the spare buffer holds weights of the old set
     if (!L || !w) return set_error(MOE_EINVAL, "layer or weights is NULL");
     const moe_qmatrix* all[] = {&w->router, &w->shared_gate, &w->shared_up, &w->shared_down, &w->gate, &w->up,
                                 &w->down};
@@ -1679,19 +1810,105 @@ extern "C" moe_status moe_ctx_inject_copy_failure(moe_ctx* C, int64_t nth) {
     return MOE_OK;
 }
 
-extern "C" moe_status moe_layer_replay_resident(moe_layer* L, void* stream, double* bytes) {
-    if (!L) return set_error(MOE_EINVAL, "layer is NULL");
-    if (!L->have_resident) return set_error(MOE_ESTATE, "moe_layer_replay_resident: no one-token call yet");
+extern "C" moe_status moe_layer_set_prefetch(moe_layer* L, int32_t on) {
+    if (!L || (on != 0 && on != 1)) return set_error(MOE_EINVAL, "moe_layer_set_prefetch: bad arguments");
+    if (L->store) return set_error(MOE_EINVAL, "moe_layer_set_prefetch: a streamed layer reads ahead into its tier");
     CUDA_TRY(cudaSetDevice(L->ctx->device));
-    // the routed items read the experts of the last routing that are resident now
-    double by = (double)L->shared_bytes;
-    const int k = L->sh.top_k;
-    if ((int)L->h_ids.size() < k) return set_error(MOE_ESTATE, "moe_layer_replay_resident: no routing recorded");
-    for (int p = 0; p < k; ++p)
-        if (L->cache.slot_of(L->h_ids[p]) >= 0) by += (double)L->ebytes;
-    CUDA_TRY(launch_ffn(L->resident_args, L->resident_list, (cudaStream_t)stream, true));
-    ++L->ctx->launches;
-    if (bytes) *bytes = by;
+    if (L->ev_done) CUDA_TRY(cudaEventSynchronize(L->ev_done));
+    CUDA_TRY(cudaStreamSynchronize(L->ctx->copy_stream));
+    if (on && !L->d_spare && cudaMalloc(&L->d_spare, L->ebytes) != cudaSuccess) {
+        cudaGetLastError();
+        return set_error(MOE_ENOMEM, "prefetch buffer of %zu bytes failed", L->ebytes);
+    }
+    if (on && !L->ev_spare_ready) {
+        CUDA_TRY(cudaEventCreateWithFlags(&L->ev_spare_ready, cudaEventDisableTiming));
+        CUDA_TRY(cudaEventCreateWithFlags(&L->ev_spare_free, cudaEventDisableTiming));
+    }
+    L->spare_free_recorded = false;
+    if (!on) {
+        cudaFree(L->d_spare);
+        L->d_spare = nullptr;
+    }
+    L->prefetch = on != 0;
+    L->spare_expert = -1;
+    if ((int)L->route_hist.size() != L->sh.n_experts) L->route_hist.assign(L->sh.n_experts, 0);
+    return MOE_OK;
+}
+
+extern "C" moe_status moe_layer_prefetch_stats(const moe_layer* L, uint64_t* issued, uint64_t* used) {
+    if (!L) return set_error(MOE_EINVAL, "layer is NULL");
+    if (issued) *issued = L->prefetch_issued;
+    if (used) *used = L->prefetch_used;
+    return MOE_OK;
+}
+
+extern "C" moe_status moe_layer_set_deterministic(moe_layer* L, int32_t on) {
+    if (!L || (on != 0 && on != 1)) return set_error(MOE_EINVAL, "moe_layer_set_deterministic: bad arguments");
+    if (L->ev_done) {
+        CUDA_TRY(cudaSetDevice(L->ctx->device));
+        CUDA_TRY(cudaEventSynchronize(L->ev_done));  // calls in flight keep the mode they started with
+    }
+    L->deterministic = on != 0;
+    return MOE_OK;
+}
+
+extern "C" moe_status moe_layers_replay_resident(moe_layer* const* layers, int32_t n_layers, int32_t rounds,
+                                                 void* stream, double* bytes) {
+    if (!layers || n_layers < 1 || rounds < 1) return set_error(MOE_EINVAL, "moe_layers_replay_resident: bad arguments");
+    double by = 0;
+    for (int i = 0; i < n_layers; ++i) {
+        moe_layer* L = layers[i];
+        if (!L) return set_error(MOE_EINVAL, "layer %d is NULL", i);
+        if (!L->have_resident || (int)L->h_ids.size() < L->sh.top_k)
+            return set_error(MOE_ESTATE, "moe_layers_replay_resident: layer %d made no one-token call yet", i);
+        if (L->ctx->device != layers[0]->ctx->device)
+            return set_error(MOE_EINVAL, "moe_layers_replay_resident: layers on different devices");
+        // the routed items read the experts of the last routing that are resident now
+        double b = (double)L->shared_bytes;
+        for (int p = 0; p < L->sh.top_k; ++p)
+            if (L->cache.slot_of(L->h_ids[p]) >= 0) b += (double)L->ebytes;
+        by += b;
+    }
+    CUDA_TRY(cudaSetDevice(layers[0]->ctx->device));
+    // the routed items resolved on the host (slot addresses of the recorded
+    // routing), so that no unit waits for the previous kernel before it
+    // starts: what is timed is the launch's own work
+    std::vector<FfnSmall> lists(n_layers);
+    std::vector<FfnArgs> args(n_layers);
+    for (int i = 0; i < n_layers; ++i) {
+        moe_layer* L = layers[i];
+        const FfnSmall& src = L->resident_list;
+        FfnSmall& l = lists[i];
+        l = FfnSmall{};
+        l.epoch = src.epoch;
+        int n0 = 0, n1 = 0;
+        for (int it = 0; it < src.n_items; ++it) {
+            FfnItem x = src.item[it];
+            const int fam = it < L->resident_args.fam[0].n_items ? 0 : 1;
+            if (!x.w) {
+                const int e = L->h_ids[src.pair[x.pb]];
+                const int slot = L->cache.slot_of(e);
+                if (slot < 0) continue;
+                x.w = L->d_slots + (size_t)slot * L->ebytes;
+            }
+            x.pb = (int16_t)(n0 + n1);
+            l.pair[n0 + n1] = src.pair[src.item[it].pb];
+            l.item[n0 + n1] = x;
+            if (fam == 0) ++n0; else ++n1;
+        }
+        l.n_items = n0 + n1;
+        args[i] = L->resident_args;
+        args[i].fam[0].n_items = n0;
+        args[i].fam[1].n_items = n1;
+        args[i].ids = nullptr;
+        args[i].slot_of = nullptr;
+    }
+    for (int r = 0; r < rounds; ++r)
+        for (int i = 0; i < n_layers; ++i) {
+            CUDA_TRY(launch_ffn(args[i], lists[i], (cudaStream_t)stream, true));
+            ++layers[i]->ctx->launches;
+        }
+    if (bytes) *bytes = by * rounds;
     return MOE_OK;
 }
 

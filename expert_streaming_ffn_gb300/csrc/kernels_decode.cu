@@ -63,12 +63,12 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 // Top-k of one token's logits by one warp. Lane l holds the candidates of
 // experts l + 32 j as 64-bit words (key << 32 | ~e), so that a larger word is
 // a larger logit or, for equal logits, a lower expert index; it sorts them
-// once, descending. With at most 8 candidates per lane and k <= 8 the lanes'
-// lists are merged by a butterfly (below); otherwise each of the k rounds
-// takes the warp-wide maximum of the lanes' heads (one max-reduction of the
-// keys, one of the index part among the lanes that hold that key), and the
-// lane that owned it moves to its next candidate. Lane r ends up with rank r.
-// Then gates = softmax over the k chosen logits.
+// once, descending. Each of the k rounds then takes the warp-wide maximum of
+// the lanes' heads with two single-instruction reductions (the largest key,
+// then the largest index part, i.e. the lowest expert id, among the lanes
+// holding that key), and the lane that owned it moves to its next candidate
+// (measured faster than a butterfly merge of the lanes' sorted lists). Lane r
+// ends up with rank r. Then gates = softmax over the k chosen logits.
 template <int MAXV>
 __device__ void topk_warp(const float* logits, int E, int k, int lane, int32_t* ids, float* gates,
                           unsigned long long* host_ids, uint32_t seq) {
@@ -92,42 +92,6 @@ __device__ void topk_warp(const float* logits, int E, int k, int lane, int32_t* 
             }
     float mine_v = -INFINITY;
     int mine_i = 0;
-    if (MAXV == 8 && k <= 8) {
-        // Butterfly merge of the lanes' sorted lists: at each step a lane keeps
-        // the 8 largest of its list and its partner's (the larger of c[j] and
-        // the partner's c[7-j] for each j is the 8 largest, in bitonic order;
-        // three half-cleaner stages sort them again). After five steps every
-        // lane holds the 8 largest overall, descending.
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            unsigned long long m[MAXV];
-#pragma unroll
-            for (int j = 0; j < MAXV; ++j) {
-                const unsigned long long o = __shfl_xor_sync(kFull, c[MAXV - 1 - j], off);
-                m[j] = c[j] > o ? c[j] : o;
-            }
-#pragma unroll
-            for (int dist = MAXV / 2; dist >= 1; dist >>= 1)
-#pragma unroll
-                for (int j = 0; j < MAXV; ++j)
-                    if ((j & dist) == 0 && m[j] < m[j + dist]) {
-                        const unsigned long long t = m[j];
-                        m[j] = m[j + dist];
-                        m[j + dist] = t;
-                    }
-#pragma unroll
-            for (int j = 0; j < MAXV; ++j) c[j] = m[j];
-        }
-        unsigned long long w = c[0];
-#pragma unroll
-        for (int j = 1; j < MAXV; ++j)
-            if (lane == j) w = c[j];
-        if (lane < k) {
-            mine_v = key_value((uint32_t)(w >> 32));
-            mine_i = (int)~(uint32_t)w;
-        }
-        k = 0;  // ranks done: skip the rounds below
-    }
     for (int r = 0; r < k; ++r) {
         const uint32_t hk = (uint32_t)(c[0] >> 32), hi = (uint32_t)c[0];
         const uint32_t top = __reduce_max_sync(kFull, hk);
@@ -304,6 +268,51 @@ __global__ void __launch_bounds__(kRouterWarps * 32, TB == 1 ? 5 : 1) router_ker
     }
 }
 
+// One block per (token, 32 output columns). Term j < ns is the j-th group of
+// cr shared-expert chunks, term ns + r the routed pair of rank r; warp w sums
+// terms w, w + warps, ... (each over its chunks in order), and one warp then
+// adds the terms in order.
+__global__ void part_reduce_kernel(const float* __restrict__ part0, const float* __restrict__ part1, int cs, int cr,
+                                   int k, int d, float* __restrict__ y) {
+    extern __shared__ float terms[];  // [ns + k][32]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.y, n = blockIdx.x * 32 + lane;
+    const int ns = (cs + cr - 1) / cr, nterm = ns + k;
+    // the partials were written by the previous kernels of the call
+    ptx::pdl_wait();
+    for (int j = warp; j < nterm; j += blockDim.x >> 5) {
+        const float* src;
+        int c0, c1, cstride;
+        if (j < ns) {
+            src = part0 + (size_t)t * cs * d;
+            c0 = j * cr;
+            c1 = min(cs, c0 + cr);
+        } else {
+            src = part1 + ((size_t)t * k + (j - ns)) * cr * d;
+            c0 = 0;
+            c1 = cr;
+        }
+        cstride = d;
+        float acc = 0.0f;
+        if (n < d) {
+            int c = c0;
+            for (; c + 4 <= c1; c += 4) {
+                const float v0 = __ldcg(src + (size_t)c * cstride + n), v1 = __ldcg(src + (size_t)(c + 1) * cstride + n);
+                const float v2 = __ldcg(src + (size_t)(c + 2) * cstride + n), v3 = __ldcg(src + (size_t)(c + 3) * cstride + n);
+                acc = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(acc, v0), v1), v2), v3);
+            }
+            for (; c < c1; ++c) acc = __fadd_rn(acc, __ldcg(src + (size_t)c * cstride + n));
+        }
+        terms[j * 32 + lane] = acc;
+    }
+    __syncthreads();
+    if (warp == 0 && n < d) {
+        float v = 0.0f;
+        for (int j = 0; j < nterm; ++j) v = __fadd_rn(v, terms[j * 32 + lane]);
+        y[(size_t)t * d + n] = v;
+    }
+}
+
 __global__ void combine_kernel(const float* __restrict__ o, const float* __restrict__ gates, int k, int d,
                                float* __restrict__ y) {
     const int t = blockIdx.y;
@@ -332,6 +341,17 @@ cudaError_t launch_router(const RouterParams& p, cudaStream_t s, bool pdl) {
         dim3((p.E + kRouterWarps - 1) / kRouterWarps, (p.T + kRouterTB - 1) / kRouterTB), dim3(kRouterWarps * 32), sm, s,
         pdl, &la);
     return cudaLaunchKernelEx(&c, router_kernel<kRouterTB>, p);
+}
+
+cudaError_t launch_part_reduce(const float* part0, const float* part1, int cs, int cr, int k, int d, int T, float* y,
+                               cudaStream_t s, bool pdl) {
+    if (cs < 1 || cr < 1 || k < 1 || d % 32 || T < 1) return cudaErrorInvalidValue;
+    const int nterm = (cs + cr - 1) / cr + k;
+    const int warps = std::min(nterm, 16);
+    cudaLaunchAttribute la;
+    const cudaLaunchConfig_t c =
+        launch_config(dim3(d / 32, T), dim3(32 * warps), sizeof(float) * 32 * nterm, s, pdl, &la);
+    return cudaLaunchKernelEx(&c, part_reduce_kernel, part0, part1, cs, cr, k, d, y);
 }
 
 cudaError_t launch_combine(const float* o, const float* gates, int T, int k, int d, float* y, cudaStream_t s) {

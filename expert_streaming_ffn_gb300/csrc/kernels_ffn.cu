@@ -52,6 +52,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "moe_internal.h"
 #include "ptx.cuh"
@@ -221,6 +222,7 @@ __device__ __forceinline__ Unit unit_of(const FfnArgs& a, int u) {
 template <int C>
 struct Shape {
     static constexpr int kThreads = (C + 1) * 32;
+    // ring depth: one CTA of 16 consumer warps per SM has room for five stages
     // ring depth: one CTA of 16 consumer warps per SM has room for five stages
     static constexpr int kStages = C >= 16 ? 5 : 4;
     static constexpr int kStageBytes = 2 * C * kRecord;  // gate/up stage: C groups of gate and of up
@@ -616,10 +618,7 @@ __global__ void __launch_bounds__(Shape<C>::kThreads, 1)
             }
             const float xi = xinv[q];
             const float h = act_fn(vg * xi, a.act) * (vu * xi) * gw;
-            uint32_t mb = __float_as_uint(fabsf(h));
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) mb = max(mb, __shfl_xor_sync(kFull, mb, off));
-            const int sh = range_shift(mb);
+            const int sh = range_shift(__reduce_max_sync(kFull, __float_as_uint(fabsf(h))));
             const float ht = h * exp2i(sh);
             const __half hi = __float2half_rn(ht);
             const __half lo = __float2half_rn(ht - __half2float(hi));
@@ -649,47 +648,68 @@ __global__ void __launch_bounds__(Shape<C>::kThreads, 1)
         if (first_unit) ptx::pdl_wait();
         uint4 hbv[kPass];
         float4 khv[kPass];
-        float* yp[kPass];
+        float* yp[kPass];  // this lane's output row: y, or the unit's partial row
+        const bool ordered = a.part[un.fam] != nullptr;
 #pragma unroll
         for (int p = 0; p < kPass; ++p) {
             hbv[p] = ptx::lds_u4(ptx::smem_addr(hb) + ((p * 8 + g) * 4 + t) * 16);
             const int tok = 4 * p + t;
             khv[p] = kh[tok];
-            yp[p] = tok < nt ? a.y + (size_t)(list.pair[it.pb + tok] / x_div) * a.d : nullptr;
+            yp[p] = nullptr;
+            if (tok < nt) {
+                const int pv = list.pair[it.pb + tok];
+                yp[p] = ordered ? a.part[un.fam] + ((size_t)pv * a.part_c[un.fam] + un.c) * a.d
+                                : a.y + (size_t)(pv / x_div) * a.d;
+            }
         }
-        for (int r0 = 0; r0 < tiles_d; r0 += dn_per) {
-            const int n = min(dn_per, tiles_d - r0);
-            const unsigned char* st = take_stage();
-            if (st) {
-                const uint32_t so = ptx::smem_addr(st);
-                for (int i = warp; i < n; i += kCons) {
-                    // rows 0-7, 8-15, 16-23, 24-31 of the tile: 16 bytes per row
-                    uint32_t wd[4];
-                    ldsm4<0>(so + i * kHalf + lane * 16, wd);
-                    const uint4 sbv = lds4<0>(so + kDnTiles * kHalf + i * kSbBlock + 16 * g);
+        // (two copies of the loop: adds into y, or stores into partial rows)
+        auto down = [&](auto ordered_c) {
+            constexpr bool kOrdered = decltype(ordered_c)::value;
+            for (int r0 = 0; r0 < tiles_d; r0 += dn_per) {
+                const int n = min(dn_per, tiles_d - r0);
+                const unsigned char* st = take_stage();
+                if (st) {
+                    const uint32_t so = ptx::smem_addr(st);
+                    for (int i = warp; i < n; i += kCons) {
+                        // rows 0-7, 8-15, 16-23, 24-31 of the tile: 16 bytes per row
+                        uint32_t wd[4];
+                        ldsm4<0>(so + i * kHalf + lane * 16, wd);
+                        const uint4 sbv = lds4<0>(so + kDnTiles * kHalf + i * kSbBlock + 16 * g);
 #pragma unroll
-                    for (int rb = 0; rb < 2; ++rb) {
-                        uint32_t pg[4], ph[4];
-                        codes16(wd[2 * rb], pg);
-                        codes16(wd[2 * rb + 1], ph);
-                        const float2 f0 = unpack_sb(rb ? sbv.z : sbv.x);
-                        const float2 f1 = unpack_sb(rb ? sbv.w : sbv.y);
-                        const int col = 32 * (r0 + i) + 16 * rb + g;
+                        for (int rb = 0; rb < 2; ++rb) {
+                            uint32_t pg[4], ph[4];
+                            codes16(wd[2 * rb], pg);
+                            codes16(wd[2 * rb + 1], ph);
+                            const float2 f0 = unpack_sb(rb ? sbv.z : sbv.x);
+                            const float2 f1 = unpack_sb(rb ? sbv.w : sbv.y);
+                            const int col = 32 * (r0 + i) + 16 * rb + g;
 #pragma unroll
-                        for (int p = 0; p < kPass; ++p) {
-                            float dd[4];
-                            mma_f16c(dd, pg[0], ph[0], pg[1], ph[1], hbv[p].x, hbv[p].y, khv[p].x, khv[p].y);
-                            mma_f16(dd, pg[2], ph[2], pg[3], ph[3], hbv[p].z, hbv[p].w);
-                            if (yp[p]) {
-                                atomicAdd(yp[p] + col, fmaf(f0.x * khv[p].w, dd[0] + dd[1], f0.y * khv[p].z));
-                                atomicAdd(yp[p] + col + 8, fmaf(f1.x * khv[p].w, dd[2] + dd[3], f1.y * khv[p].z));
+                            for (int p = 0; p < kPass; ++p) {
+                                float dd[4];
+                                mma_f16c(dd, pg[0], ph[0], pg[1], ph[1], hbv[p].x, hbv[p].y, khv[p].x, khv[p].y);
+                                mma_f16(dd, pg[2], ph[2], pg[3], ph[3], hbv[p].z, hbv[p].w);
+                                if (yp[p]) {
+                                    const float v0 = fmaf(f0.x * khv[p].w, dd[0] + dd[1], f0.y * khv[p].z);
+                                    const float v1 = fmaf(f1.x * khv[p].w, dd[2] + dd[3], f1.y * khv[p].z);
+                                    if constexpr (kOrdered) {
+                                        __stcg(yp[p] + col, v0);
+                                        __stcg(yp[p] + col + 8, v1);
+                                    } else {
+                                        atomicAdd(yp[p] + col, v0);
+                                        atomicAdd(yp[p] + col + 8, v1);
+                                    }
+                                }
                             }
                         }
                     }
                 }
+                release_stage();
             }
-            release_stage();
-        }
+        };
+        if (ordered)
+            down(std::true_type{});
+        else
+            down(std::false_type{});
         if (tr && first_unit && warp == 0 && lane == 0) tr[3] = ptx::globaltimer();
         first_unit = false;
     }
@@ -754,7 +774,7 @@ cudaError_t ffn_launch(FfnArgs a, const L& list, cudaStream_t s, bool pdl) {
 template <class L>
 cudaError_t launch_ffn(const FfnArgs& a, const L& list, cudaStream_t s, bool pdl) {
     if (list.n_items == 0) return cudaSuccess;
-    int m = 0;
+    int m = a.min_nt;  // the shape (and so the cross-warp order of the sums) for at least min_nt rows
     for (int i = 0; i < list.n_items; ++i) m = std::max(m, (int)list.item[i].np);
     // one row per item: 16 consumer warps (one CTA per SM); more rows stage
     // more token rows in shared memory and get 8 (a smaller ring)

@@ -152,6 +152,14 @@ struct RouterParams {
 // that kernel to finish; it lets the next kernel start early as well.
 cudaError_t launch_router(const RouterParams& p, cudaStream_t s, bool pdl = false);
 
+// The ordered decode combine: y[t][n] = S + O_0 + ... + O_{k-1}, where S is
+// the shared expert's share of token t (its cs chunk partials part0[t][c][n]
+// summed in groups of cr chunks, the groups then added in order) and O_r the
+// routed share of pair t*k + r (its cr chunk partials part1[t*k+r][c][n]
+// summed in chunk order). The order depends on nothing but the shapes.
+cudaError_t launch_part_reduce(const float* part0, const float* part1, int cs, int cr, int k, int d, int T, float* y,
+                               cudaStream_t s, bool pdl);
+
 // y[t][n] += sum_{r<k} gates[t][r] * o[t*k + r][n], added in rank order.
 cudaError_t launch_combine(const float* o, const float* gates, int T, int k, int d, float* y, cudaStream_t s);
 
@@ -222,6 +230,19 @@ struct FfnArgs {
     const int32_t* slot_of;
     const uint8_t* slots;
     size_t ebytes;
+    // Ordered combine (null: every unit adds into y with fp32 atomics). Unit
+    // (item, c) of family f stores its gate-weighted share of row q (pair
+    // value p = pair[pb + q]: a token for family 0, a pair t*k + r for family
+    // 1) at part[f] + (p * part_c[f] + c) * d, where part_c[f] = inter / 32;
+    // launch_part_reduce then sums them per token in a fixed order.
+    float* part[kFfnFams];
+    int part_c[kFfnFams];
+    // The launch takes the kernel shape for at least min_nt rows per item.
+    // The shape sets how a unit's gate/up group sums are split over warps, so
+    // the ordered combine gives every launch of a multi-token call the same
+    // one (its items can fall into the hit and miss launches differently on
+    // another call).
+    int min_nt;
     // Slot-table changes of this call's cache step, written into slot_of once
     // the previous kernel on the stream (the launch that read the table) has
     // finished: slot_of[upd_expert[i]] = upd_slot[i].

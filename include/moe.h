@@ -167,6 +167,63 @@ size_t moe_expert_bytes(const moe_shapes* shapes);
 moe_status moe_route(moe_layer* layer, const void* x_bf16, int32_t T, const float* zbias, int32_t* ids,
                      float* gates, void* stream);
 
+/* Predictive prefetch into HBM ([P1] §9.2 item 3 and §9.5 item 2: predict
+ * the experts the next steps will need from routing history and read them
+ * ahead). With on = 1 the layer keeps one spare expert buffer in device
+ * memory. After each decode call, the copy stream fills it with the expert
+ * that the layer's steps have routed to most often (ties to the lower id)
+ * among those in no cache slot. A later miss of that expert then costs no
+ * copy over the host link: the call's kernels read the spare buffer (after
+ * an event wait for the prefetch copy), and the call's stream copies it into
+ * the expert's slot behind them. The cache and its hit/miss trace do not
+ * change (a prefetched expert still counts as a miss and enters the cache by
+ * the LFU/LRU rules); only where a miss's bytes come from does. The prefetch
+ * copies share the host link with the misses and count in bytes_h2d. Not for layers created
+ * with moe_layer_create_streamed (they read ahead into their host tier).
+ * Waits for the layer's calls and copies in flight. Errors: MOE_EINVAL,
+ * MOE_ENOMEM, MOE_ECUDA. */
+moe_status moe_layer_set_prefetch(moe_layer* layer, int32_t on);
+
+/* Prefetches issued, and misses served from the spare buffer, since the
+ * layer was created. Either pointer may be NULL. Errors: MOE_EINVAL. */
+moe_status moe_layer_prefetch_stats(const moe_layer* layer, uint64_t* issued, uint64_t* used);
+
+/* Ordered combine for decode calls (T <= 64): with on = 1, a decode call
+ * sums its output in a fixed order, y[t] = S_t + O_{t,0} + ... + O_{t,k-1}
+ * ([P1] §6.2.3: the shared expert's output plus the routed outputs weighted
+ * by their gates, here in rank order r = 0..k-1), where S_t is the shared
+ * expert's share and O_{t,r} the gate-weighted output of the rank-r expert.
+ * The expert FFN kernels then store each work unit's share (32 intermediate
+ * rows of one expert) in a partial row fixed by (token or pair, rows) instead
+ * of adding it into y with fp32 atomics, and one more kernel adds the partial
+ * rows in that order. Two calls on the same x give bit-identical y, whatever
+ * the cache state (which experts were hits, misses or bypasses). Cost: one
+ * kernel launch per call, and T * (d_ff_shared/32 + top_k * d_ff/32) *
+ * d_model floats of layer-owned device memory (3 MB at T = 1 for d_model =
+ * 2816, d_ff = 704, d_ff_shared = 2816, top_k = 8), allocated on the next
+ * call, written and read once per call. With on = 0 (the default) the shares
+ * are added with atomics in arrival order, so y may differ between calls in
+ * the last bits. Prefill calls (T > 64) always combine in rank order. Waits
+ * for the layer's calls in flight. Errors: MOE_EINVAL, MOE_ECUDA. */
+moe_status moe_layer_set_deterministic(moe_layer* layer, int32_t on);
+
+/* Kernel-timing diagnostic (the pages have no counterpart). Enqueues on
+ * `stream`, `rounds` times over, for each of the n_layers layers in turn, the
+ * expert-FFN launch that the layer's last one-token moe_forward call made for
+ * its resident experts: the shared expert and each routed pair of that call's
+ * routing, looked up in the device slot table as it stands now (every expert
+ * the call copied in is resident by then). Each launch adds into its call's y
+ * again, so those y are garbage afterwards; nothing else changes (caches,
+ * statistics, routing). Every launch is a programmatic dependent of the
+ * previous kernel, as in a pipelined decode loop, and one host call enqueues
+ * them all, so a pair of events around this call times the kernel rather
+ * than the host. *bytes (may be NULL) gets the weight bytes all the launches
+ * read. All layers must be on one device.
+ * Errors: MOE_EINVAL, MOE_ESTATE (a layer made no one-token call yet),
+ * MOE_ECUDA. */
+moe_status moe_layers_replay_resident(moe_layer* const* layers, int32_t n_layers, int32_t rounds, void* stream,
+                                      double* bytes);
+
 /* moe_route without any device allocation. The pages have no counterpart:
  * this entry point exists for callers that must not allocate, such as a
  * decode loop that holds a fixed memory budget, or one that cannot afford the

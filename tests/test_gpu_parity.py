@@ -521,3 +521,21 @@ def test_timeline_trace_file(tmp_path, monkeypatch):
         assert 0 < start <= end  # every launch ran and recorded its span
     marks = {l.split()[1] for l in lines if l.startswith("host ")}
     assert {"call", "ids", "copies", "end"} <= marks
+
+
+def test_hbm_prefetch_leaves_every_result_unchanged(ctx):
+    """decode_2816 layer 2 with the spare-buffer prefetch on: misses of the
+    prefetched expert are copied from HBM instead of host memory, and the
+    ids, gates, cache trace and y stay those of the oracle at every step."""
+    s = synth.SHAPES_2816
+    wl = synth.WORKLOADS["decode_2816"]
+    r = Rig(ctx, s, 2, wl.cache_slots)
+    zb = synth.zipf_bias(s, 2, wl.zipf_s)
+    try:
+        moe.moe_layer_set_prefetch(r.h, True)
+        for step in range(40):
+            r.forward(synth.tokens(s, 2, step, 1, True), zb, check_y=step % 4 == 0)
+        st = moe.moe_layer_prefetch_stats(r.h)
+        assert st["issued"] > 0 and st["used"] > 0, st
+    finally:
+        r.close()
