@@ -698,6 +698,7 @@ def run_ours(args, world, rank, local):
 
     extra = {}
     if not args.resident and world == 1 and not args.no_legs:
+        extra["tiny_latency"] = run_tiny_latency(args, ctx, dev, stream, seed)
         extra["resident_upper_bound"] = run_resident_bound(args, ctx, dev, stream, seed, peaks, weights)
         extra["decode_2048"] = run_decode_2048(args, ctx, dev, stream, seed, peaks)
     prefill = None
@@ -810,6 +811,53 @@ def run_resident_bound(args, ctx, dev, stream, seed, peaks, weights=None):
         return out
     finally:
         rig.close()
+
+
+def run_tiny_latency(args, ctx, dev, stream, seed):
+    """tiny (config 0): one layer of d = 512, 16 experts (top-2), 4-slot LFU,
+    4 decode tokens per call, x ~ N(0, 1): latency per call, through the
+    public call, device-timed over 256 consecutive calls (after 64 warm-up
+    calls); the cache trajectory is that of the calls, misses included."""
+    import torch
+
+    import expert_streaming_ffn_gb300 as moe
+    import synth
+
+    wl = synth.WORKLOADS["tiny"]
+    s = wl.shapes
+    h = moe.moe_layer_create(ctx, s, wl.cache_slots, wl.policy)
+    try:
+        moe.moe_layer_set_weights(h, synth.layer_weights(s, 0, seed))
+        n = 320
+        xs = np.stack([synth.tokens(s, 0, st, wl.tokens, wl.rms_normalise, seed) for st in range(n)])
+        x = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16).to(dev)
+        y = torch.empty((wl.tokens, s.d_model), dtype=torch.float32, device=dev)
+        row = wl.tokens * s.d_model * 2
+        sptr = stream.cuda_stream
+
+        def call(i):
+            moe.moe_forward_ptr(h, x.data_ptr() + i * row, wl.tokens, None, y.data_ptr(), sptr)
+
+        for i in range(64):
+            call(i)
+        torch.cuda.synchronize(dev)
+        moe.moe_layer_reset_stats(h)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        t0 = time.perf_counter()
+        for i in range(64, n):
+            call(i)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t0
+        st = moe.moe_layer_stats(h)
+        calls = n - 64
+        return {"workload": "tiny", "tokens_per_call": wl.tokens, "calls": calls,
+                "us_per_call": 1000.0 * ev0.elapsed_time(ev1) / calls, "wall_us_per_call": 1e6 * wall / calls,
+                "hit_rate": st["hits"] / max(1, st["hits"] + st["misses"]),
+                "host_wait_us_per_call": st["host_wait_us"] / calls}
+    finally:
+        moe.moe_layer_destroy(h)
 
 
 def run_decode_2048(args, ctx, dev, stream, seed, peaks):
