@@ -15,19 +15,25 @@
 //     epilogue forms h = act(gate) * up from neighbouring lanes;
 //   phase 2 (down): 128 consecutive output rows.
 // Warp roles in a CTA of 832 threads (one CTA per SM, persistent over jobs):
-//   warps 0-3   MMA issue, one thread each (one thread issues a tcgen05.mma
-//               only every ~125 cycles, a third of the tensor pipe's rate for
-//               these small tiles); warp 0 also allocates TMEM;
+//   warps 0-3   MMA issue, one thread each, K-block kb of a job going to
+//               issuer kb mod nI (one thread issues a tcgen05.mma only about
+//               every 60-125 cycles, whatever N, so several issue in
+//               parallel); warp 0 also allocates TMEM;
 //   warps 4-7   epilogue, one TMEM lane quarter each;
-//   warps 8-23  dequantisation in two groups of 8 warps that take alternate
-//               K-blocks: int4 -> fp16 w = fp16(s * q + b), written into the
-//               128B-swizzled K-major A tile;
+//   warps 8-23  dequantisation in four groups of 4 warps, group g owning A
+//               stage g (the K-blocks whose running index is g mod 4); a
+//               thread turns one A row of 64 codes into fp16 w = fp16(s q + b)
+//               in the 128B-swizzled K-major A tile;
 //   warp 24     bulk copies of the weight codes and scales of 4 K-blocks of
 //               the job's row tiles at a time, into a raw ring (gate/up in
 //               the tiled record format, down column-sliced);
 //   warp 25     TMA loads of the token rows (128B-swizzled fp16).
 // Copies are few and large (a bulk copy costs its issuing thread tens of
 // nanoseconds whatever its size), and the two producers issue in parallel.
+// The single-thread roles (the issuers above all) sit on sub-partitions
+// shared with busy dequantising warps, where every dependent instruction
+// waits its turn: their loops do only the work of their own K-blocks, with
+// stage and phase taken from running counts by masks, not divisions.
 // Every wait is bounded; on expiry the kernel records an error bit, raises an
 // abort flag that makes every other wait give up, drains its asynchronous work
 // and frees its tensor memory before it exits.
@@ -46,9 +52,9 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kThreads = 832;
-// warps 0-3 issue MMAs (one thread each), 4-7 epilogue, 8-23 dequantise (two
-// groups of 8, alternate K-blocks), 24 and 25 load
-constexpr int kIssuers = 4, kWarpEpi = 4, kWarpDq = 8, kDqWarps = 8, kDqGroups = 2, kWarpLoad = 24, kWarpB = 25;
+// warps 0-3 issue MMAs (one thread each), 4-7 epilogue, 8-23 dequantise (four
+// groups of 4, one A stage each), 24 and 25 load
+constexpr int kIssuers = 4, kWarpEpi = 4, kWarpDq = 8, kDqWarps = 4, kDqGroups = 4, kWarpLoad = 24, kWarpB = 25;
 constexpr int kStages = 4;     // A ring, one K-block (64) per stage
 constexpr int kSlotsB = 4;     // B ring: a slot holds as many K-blocks of the job's rows as fit in 16 KB
 constexpr int kRawStages = 4;  // raw ring, kUnit K-blocks per stage
@@ -64,8 +70,11 @@ constexpr int kRawBytes = 4 * kUnit * kRecord;  // 4 row tiles x kUnit records
 constexpr int kTmemCols = 512;
 // Within a job every round of an A stage has the same issuer (kStages is a
 // multiple of nI); between jobs the issuers hand off (see the MMA issue loop).
-static_assert(kStages % kIssuers == 0 && kStages % 2 == 0, "an A stage keeps its issuer within a job");
-static_assert(kStages % kDqGroups == 0, "each dequantising group owns whole A stages");
+static_assert(kStages % kIssuers == 0, "an A stage keeps its issuer within a job");
+static_assert(kStages == kDqGroups, "each dequantising group owns one A stage");
+constexpr int kStageShift = kStages == 8 ? 3 : kStages == 4 ? 2 : kStages == 2 ? 1 : 0;
+constexpr int kSlotShift = kSlotsB == 8 ? 3 : kSlotsB == 4 ? 2 : kSlotsB == 2 ? 1 : 0;
+static_assert((1 << kStageShift) == kStages && (1 << kSlotShift) == kSlotsB, "rings indexed by masks");
 // shared memory: A ring, B ring, raw ring, barriers, TMEM address; +1 KB to align
 constexpr int kSmemBytes = 1024 + kStages * kABytes + kSlotsB * kBBytes + kRawStages * kRawBytes + 320;
 
@@ -251,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 9 handoff
     auto record = [&](int what, int job, int kb) {
         if (!a.trace) return;
-        unsigned long long* rec = a.trace + kPfTraceKb * kPfTracePoints;
+        unsigned long long* rec = a.trace;
         const unsigned k = atomicAdd(reinterpret_cast<unsigned*>(rec), 1u);
         if (k < kPfFailRecords)
             rec[1 + k] = ((unsigned long long)blockIdx.x << 48) | ((unsigned long long)warp << 40) |
@@ -291,9 +300,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         record(1, j, kb0);
                         if (!*abortp) fail(32u);
                     } else {
-                        // diagnostics: when block 0 issues each unit of its first jobs (slot 1 of kb0's row)
-                        if (a.trace && blockIdx.x == 0 && issued < kPfTraceKb / kUnit)
-                            a.trace[0 * kPfTraceKb + issued * kUnit + 1] = ptx::globaltimer();
                         ptx::mbar_arrive_expect_tx(raw_full + r, (uint32_t)(4 * nu * kRecord));
                     }
                 }
@@ -407,10 +413,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp < kIssuers) {
         // ---------------- MMA issue ----------------
+        // An issuer visits only its own K-blocks (kb mod nI == i): it waits on
+        // and releases just their A stages, whose index and phase parity follow
+        // from the CTA's running K-block count. Every issuer waits on every B
+        // slot and arrives once per round on its release, after its own MMAs
+        // that read it (a slot's K-blocks are spread over the issuers).
         if (lane == 0) {
             const int i = warp;  // this issuer
-            int s = 0, sb = 0;
-            uint32_t ph = 0, bph = 0;
+            const uint64_t a_desc0 = sw128_desc(ptx::smem_addr(ringA));
+            const uint64_t b_desc0 = sw128_desc(ptx::smem_addr(ringB));
+            uint32_t C = 0, SB = 0;  // K-blocks and B slots of this CTA's earlier jobs
             int njob = 0;
             for (int j = blockIdx.x; j < P.n_jobs; j += gridDim.x, ++njob) {
                 const Job b = decode_job(P, a, j);
@@ -421,69 +433,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int buf = njob & 1;
                 const uint32_t idesc = f16_idesc(kTileM, nb);
                 const uint32_t d_tmem = tmem + buf * 256 + i * (256 / nI);
-                // the epilogue must have read this accumulator's previous job
                 bool ok = ptx::mbar_wait_sleep(acc_empty + buf, ((njob >> 1) & 1) ^ 1, abortp);
                 if (!ok) record(3, j, 0);
                 ptx::tc_fence_after();
-                bool first = true;
-                for (int kb = 0; kb < nkb; ++kb) {
-                    const int kk = kb % kpb;  // K-block within the B slot
-                    // Every issuer sees each round of a slot filled before it
-                    // arrives on the slot's release, owner of a K-block in it or
-                    // not: an arrival may then only count toward that round.
-                    if (kk == 0 && ok && !ptx::mbar_wait_sleep(b_full + sb, bph, abortp)) {
+                uint32_t acc = 0;
+                // K-block kb of the job is this issuer's when kb % nI == i
+                int kb = i;
+                for (int kb0 = 0; kb0 < nkb; kb0 += kpb, ++SB) {
+                    const int kend = min(kb0 + kpb, nkb);
+                    const int sl = (int)(SB & (kSlotsB - 1));
+                    if (ok && !ptx::mbar_wait_sleep(b_full + sl, (SB >> kSlotShift) & 1, abortp)) {
                         ok = false;
-                        record(4, j, kb);
+                        record(4, j, kb0);
                     }
-                    if (i < nI && kb % nI == i) {
-                        if (ok && !ptx::mbar_wait_sleep(a_full + s, ph, abortp)) {
+                    const uint64_t bslot = b_desc0 + (uint64_t)((sl * kBBytes) >> 4);
+                    for (; ok && i < nI && kb < kend; kb += nI) {
+                        const uint32_t c = C + (uint32_t)kb;
+                        const int st = (int)(c & (kStages - 1));
+                        if (!ptx::mbar_wait_sleep(a_full + st, (c >> kStageShift) & 1, abortp)) {
                             ok = false;
                             record(5, j, kb);
+                            break;
                         }
-                        const bool trace = a.trace && blockIdx.x == 0 && njob == 0 && kb < kPfTraceKb;
-                        if (trace) a.trace[3 * kPfTraceKb + kb] = ptx::globaltimer();
-                        if (ok) {
-                            ptx::tc_fence_after();
-                            const uint64_t ad = sw128_desc(ptx::smem_addr(ringA + s * kABytes));
-                            const uint64_t bd = sw128_desc(ptx::smem_addr(ringB + sb * kBBytes + kk * nb * 128));
+                        ptx::tc_fence_after();
+                        const uint64_t ad = a_desc0 + (uint64_t)((st * kABytes) >> 4);
+                        const uint64_t bd = bslot + (uint64_t)(((kb - kb0) * nb * 128) >> 4);
 #pragma unroll
-                            for (int k = 0; k < 4; ++k)  // K = 16 per MMA: +32 bytes in the swizzled row
-                                ptx::mma_f16_ss(d_tmem, ad + 2 * k, bd + 2 * k, idesc, !(first && k == 0));
-                            first = false;
-                            ptx::mma_commit(a_empty + s);
-                            if (trace) a.trace[4 * kPfTraceKb + kb] = ptx::globaltimer();
+                        for (int k = 0; k < 4; ++k) {  // K = 16 per MMA: +32 bytes in the swizzled row
+                            ptx::mma_f16_ss(d_tmem, ad + 2 * k, bd + 2 * k, idesc, acc);
+                            acc = 1;
                         }
+                        ptx::mma_commit(a_empty + st);
                     }
-                    if (++s == kStages) {
-                        s = 0;
-                        ph ^= 1;
-                    }
-                    if (kk == kpb - 1 || kb == nkb - 1) {  // last K-block of the slot: every issuer arrives
-                        if (ok) ptx::mma_commit(b_empty + sb);
-                        if (++sb == kSlotsB) {
-                            sb = 0;
-                            bph ^= 1;
-                        }
-                    }
+                    // every issuer arrives once per round of every slot (after its own MMAs on it)
+                    if (ok) ptx::mma_commit(b_empty + sl);
                 }
+                C += (uint32_t)nkb;
                 if (ok) {
                     ptx::mma_commit(acc_full + buf);
                 } else if (!*abortp) {
                     fail(128u);
                 }
-                // Hand-off: every issuer has taken its last A stage of this job
-                // before any waits on a stage of the next. K-block kb goes to
-                // issuer kb % nI, so when a job's K-block count is not a multiple
-                // of nI a stage changes owner between jobs; a new owner that ran
-                // ahead would test the stage's phase parity two phases early and
-                // pass it (an mbarrier parity tells only adjacent phases apart).
+                // Hand-off: a stage's owner (kb % nI of the job's K-blocks) can change
+                // between jobs; nobody waits on a stage of the next job before every
+                // issuer has taken its last stage of this one.
                 ptx::mbar_arrive(handoff);
                 if (!ptx::mbar_wait_sleep(handoff, njob & 1, abortp)) {
                     record(9, j, nkb);
                     if (!*abortp) fail(128u);
                 }
             }
-            // every MMA issued by this thread has completed once this arrives
             ptx::mma_commit(drain);
             ptx::mbar_wait_bounded(drain, 0, nullptr);
         }
@@ -573,36 +572,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= kWarpDq && warp < kWarpDq + kDqGroups * kDqWarps) {
         // ---------------- dequantisation ----------------
-        // group g takes the K-blocks whose running index is g mod 2, i.e. the A
-        // stages g and g + 2; within a group, thread t has A row t / 2, half t % 2
+        // group g owns A stage g (the K-blocks whose running index is g mod 4);
+        // thread t of a group dequantises A row t, all 64 inputs
         const int grp = (warp - kWarpDq) / kDqWarps, wg = (warp - kWarpDq) % kDqWarps;
-        const int t = wg * 32 + lane;
-        const int rho = t >> 1, hh = t & 1;
+        const int rho = wg * 32 + lane;
         int tile_raw, rlane;
         if (phase == 1) {
             const int qq = rho >> 5, l = rho & 31;
-            const int wrow = 16 * qq + (l >> 1);  // row within the 64 gate (or up) rows of the tile
+            const int wrow = 16 * qq + (l >> 1);
             tile_raw = (l & 1) * 2 + (wrow >> 5);
             rlane = wrow & 31;
         } else {
             tile_raw = rho >> 5;
             rlane = rho & 31;
         }
-        // where this thread's 16 codes and scale word of K-block u of a raw stage sit:
-        // phase 1 records [tile][u] of kRecord bytes; phase 2 codes [u][half][tile] of
-        // 512 bytes, then scale blocks [u][tile] of 128 bytes
-        const int codes_off = phase == 1 ? tile_raw * kUnit * kRecord + hh * 512 + rlane * 16
-                                         : hh * 2048 + tile_raw * 512 + rlane * 16;
+        const int codes_off = phase == 1 ? tile_raw * kUnit * kRecord + rlane * 16 : tile_raw * 512 + rlane * 16;
+        const int codes_hh = phase == 1 ? 512 : 2048;
         const int codes_step = phase == 1 ? kRecord : 4096;
         const int sb_off = phase == 1 ? tile_raw * kUnit * kRecord + 1024 + sb_pos(rlane) * 4
                                       : kUnit * 4096 + tile_raw * 128 + sb_pos(rlane) * 4;
         const int sb_step = phase == 1 ? kRecord : 512;
         const int swz = rho & 7;
+        const uint32_t arow = ptx::smem_addr(ringA + grp * kABytes + rho * 128);
         int r = 0, s = 0;
-        uint32_t rph = 0, ph = 0;
-        const bool tracer = a.trace && blockIdx.x == 0 && grp == 0 && t == 0;
-        const bool wtracer = a.trace && blockIdx.x == 0 && lane == 0;
-        for (int j = blockIdx.x, njob = 0; j < P.n_jobs; j += gridDim.x, ++njob) {
+        uint32_t rph = 0, gph = 0;
+        for (int j = blockIdx.x; j < P.n_jobs; j += gridDim.x) {
             const Job b = decode_job(P, a, j);
             const int nkb = b.nkb;
             for (int kb0 = 0; kb0 < nkb; kb0 += kUnit) {
@@ -610,57 +604,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool have = ptx::mbar_wait_sleep(raw_full + r, rph, abortp);
                 if (!have && lane == 0) record(7, j, kb0);
                 if (!have && lane == 0 && !*abortp) fail(64u);
-                // shared-space addresses: ringR and ringA come from an aligned
-                // integer, so plain pointer accesses would be generic ones
-                const uint32_t raw_s = ptx::smem_addr(ringR + r * kRawBytes);
-                // this group's K-blocks of the unit: stage s + u is ours when (s + u) % 2 == grp
-                const int u0 = ((s & 1) == grp) ? 0 : 1;
-                uint4 cw[2];
-                uint32_t sbw[2];
-#pragma unroll
-                for (int m = 0; m < 2; ++m) {
-                    const int u = u0 + 2 * m;
-                    if (have && u < nu) {
-                        cw[m] = ptx::lds_u4(raw_s + codes_off + u * codes_step);
-                        sbw[m] = ptx::lds_u32(raw_s + sb_off + u * sb_step);
-                    }
-                }
-                for (int u = 0; u < nu; ++u) {
-                    if (((s & 1) == grp)) {
-                        const int m = (u - u0) >> 1;
-                        const bool trace = tracer && njob == 0 && kb0 + u < kPfTraceKb;
-                        if (trace) a.trace[0 * kPfTraceKb + kb0 + u] = ptx::globaltimer();
-                        // the A stage is free once the MMAs that read it are done
-                        const bool free_a = have && ptx::mbar_wait_sleep(a_empty + s, ph ^ 1, abortp);
-                        if (trace) a.trace[1 * kPfTraceKb + kb0 + u] = ptx::globaltimer();
-                        if (free_a) {
-                            const uint4 c = m ? cw[1] : cw[0];
-                            const uint32_t w = m ? sbw[1] : sbw[0];
-                            const __half2 s2 = __half2half2(__ushort_as_half((unsigned short)(w & 0xFFFFu)));
-                            const __half2 b2 = __half2half2(__ushort_as_half((unsigned short)(w >> 16)));
-                            const uint32_t arow = ptx::smem_addr(ringA + s * kABytes + rho * 128);
-                            const uint32_t words[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)  // 16-byte chunk 4 hh + q (8 elements) of the 128-byte row
-                                ptx::sts_u4(arow + (((4 * hh + q) ^ swz) << 4), dequant8(words[q], s2, b2));
-                            ptx::fence_proxy_async_smem();  // generic-proxy writes, read next by the tensor core
-                        } else if (have && lane == 0) {
-                            record(8, j, kb0 + u);
-                            if (!*abortp) fail(64u);
-                        }
-                        __syncwarp();
-                        if (lane == 0) ptx::mbar_arrive(a_full + s);
-                        if (trace) a.trace[2 * kPfTraceKb + kb0 + u] = ptx::globaltimer();
-                        if (wtracer && njob == 0 && kb0 + u < kPfTraceKb)
-                            a.trace[(5 + wg) * kPfTraceKb + kb0 + u] = ptx::globaltimer();
-                    }
-                    if (++s == kStages) {
-                        s = 0;
-                        ph ^= 1;
-                    }
+                const int u = (grp - s) & 3;  // this group's K-block of the unit, if any
+                uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;
+                uint32_t w = 0;
+                if (have && u < nu) {
+                    const uint32_t raw_s = ptx::smem_addr(ringR + r * kRawBytes);
+                    c0 = ptx::lds_u4(raw_s + codes_off + u * codes_step);
+                    c1 = ptx::lds_u4(raw_s + codes_off + codes_hh + u * codes_step);
+                    w = ptx::lds_u32(raw_s + sb_off + u * sb_step);
                 }
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(raw_empty + r);
+                if (u < nu) {
+                    const bool free_a = have && ptx::mbar_wait_sleep(a_empty + grp, gph ^ 1, abortp);
+                    if (free_a) {
+                        const __half2 s2 = __half2half2(__ushort_as_half((unsigned short)(w & 0xFFFFu)));
+                        const __half2 b2 = __half2half2(__ushort_as_half((unsigned short)(w >> 16)));
+                        const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)  // 16-byte chunk q of the 128-byte row
+                            ptx::sts_u4(arow + ((q ^ swz) << 4), dequant8(words[q], s2, b2));
+                        ptx::fence_proxy_async_smem();
+                    } else if (have && lane == 0) {
+                        record(8, j, kb0 + u);
+                        if (!*abortp) fail(64u);
+                    }
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(a_full + grp);
+                    gph ^= 1;
+                }
+                s = (s + nu) & 3;
                 if (++r == kRawStages) {
                     r = 0;
                     rph ^= 1;

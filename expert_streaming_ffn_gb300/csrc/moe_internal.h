@@ -322,16 +322,11 @@ struct PfArgs {
     float* part;
     size_t part_cap;
     int ks[2];
-    // optional diagnostics: block 0 records %globaltimer for the first
-    // kPfTraceKb K-blocks of its first job at kPfTracePoints moments (raw
-    // records landed, A stage free, A stage written, MMA inputs ready, MMAs
-    // committed, then A stage written by each of the 8 dequantising warps);
-    // null = off
+    // optional diagnostics: a count, then the first kPfFailRecords waits of
+    // the launch that expired (block, warp, which wait, job, K-block); null = off
     unsigned long long* trace;
 };
-constexpr int kPfTraceKb = 64;
-constexpr int kPfTracePoints = 13;
-constexpr int kPfFailRecords = 31;  // after the trace points: a count, then records
+constexpr int kPfFailRecords = 31;
 
 // Converts the chunk's token rows to fp16 for the gate/up B operand:
 // xs[t] = x[t] for t < T and xg[i] = x[pair[i] / k] for i < P.
