@@ -20,14 +20,17 @@
 //               every 60-125 cycles, whatever N, so several issue in
 //               parallel); warp 0 also allocates TMEM;
 //   warps 4-7   epilogue, one TMEM lane quarter each;
-//   warps 8-23  dequantisation in four groups of 4 warps, group g owning A
-//               stage g (the K-blocks whose running index is g mod 4); a
-//               thread turns one A row of 64 codes into fp16 w = fp16(s q + b)
-//               in the 128B-swizzled K-major A tile;
+//   warps 8-23  dequantisation in four groups of 4 warps, group g taking the
+//               K-blocks whose running index is g mod 4 (A stages g and
+//               g + 4 in turn); a thread turns one A row of 64 codes into fp16
+//               w = fp16(s q + b) in the 128B-swizzled K-major A tile;
 //   warp 24     bulk copies of the weight codes and scales of 4 K-blocks of
 //               the job's row tiles at a time, into a raw ring (gate/up in
 //               the tiled record format, down column-sliced);
-//   warp 25     TMA loads of the token rows (128B-swizzled fp16).
+//   warp 25     TMA loads of the token rows (128B-swizzled fp16): a routed
+//               expert's rows, padded to 16, 32, 64 or 128, one 3-D box of a
+//               whole B slot's K-blocks at a time; the shared expert's token
+//               block, one 2-D box per K-block.
 // Copies are few and large (a bulk copy costs its issuing thread tens of
 // nanoseconds whatever its size), and the two producers issue in parallel.
 // The single-thread roles (the issuers above all) sit on sub-partitions
@@ -53,11 +56,8 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kThreads = 832;
 // warps 0-3 issue MMAs (one thread each), 4-7 epilogue, 8-23 dequantise (four
-// groups of 4, one A stage each), 24 and 25 load
+// groups of 4, group g owning A stages g and g + 4), 24 and 25 load
 constexpr int kIssuers = 4, kWarpEpi = 4, kWarpDq = 8, kDqWarps = 4, kDqGroups = 4, kWarpLoad = 24, kWarpB = 25;
-constexpr int kStages = 4;     // A ring, one K-block (64) per stage
-constexpr int kSlotsB = 4;     // B ring: a slot holds as many K-blocks of the job's rows as fit in 16 KB
-constexpr int kRawStages = 4;  // raw ring, kUnit K-blocks per stage
 constexpr int kUnit = 4;
 constexpr int kTileM = 128;
 constexpr int kRecord = 1152;           // 32 rows x 64 codes, then 32 scale/bias words
@@ -68,15 +68,33 @@ constexpr int kRawBytes = 4 * kUnit * kRecord;  // 4 row tiles x kUnit records
 // nI issuers in turn (nI = 4 for up to 64 token rows, else 2), each issuer
 // accumulating into its own 256/nI columns of the buffer; the epilogue sums them.
 constexpr int kTmemCols = 512;
-// Within a job every round of an A stage has the same issuer (kStages is a
-// multiple of nI); between jobs the issuers hand off (see the MMA issue loop).
-static_assert(kStages % kIssuers == 0, "an A stage keeps its issuer within a job");
-static_assert(kStages == kDqGroups, "each dequantising group owns one A stage");
-constexpr int kStageShift = kStages == 8 ? 3 : kStages == 4 ? 2 : kStages == 2 ? 1 : 0;
-constexpr int kSlotShift = kSlotsB == 8 ? 3 : kSlotsB == 4 ? 2 : kSlotsB == 2 ? 1 : 0;
-static_assert((1 << kStageShift) == kStages && (1 << kSlotShift) == kSlotsB, "rings indexed by masks");
-// shared memory: A ring, B ring, raw ring, barriers, TMEM address; +1 KB to align
-constexpr int kSmemBytes = 1024 + kStages * kABytes + kSlotsB * kBBytes + kRawStages * kRawBytes + 320;
+// Ring sizes of a launch's layout. A stage holds one K-block (64) of the A
+// tile; a B slot as many K-blocks of the job's token rows as fit in 16 KB; a
+// raw stage kUnit K-blocks of codes and scales. Within a job every round of an
+// A stage has the same issuer (kStages is a multiple of nI); between jobs the
+// issuers hand off (see the MMA issue loop).
+template <int A, int B, int R, bool D>
+struct PfRings {
+    static constexpr int kStages = A, kSlotsB = B, kRawStages = R;
+    // routed token rows padded to a power of two and loaded one 3-D box per B
+    // slot (else padded to a multiple of 16, 2-D boxes of 16 rows)
+    static constexpr bool kRows3d = D;
+    static constexpr int kStageShift = A == 8 ? 3 : A == 4 ? 2 : A == 2 ? 1 : 0;
+    static constexpr int kSlotShift = B == 8 ? 3 : B == 4 ? 2 : B == 2 ? 1 : 0;
+    static_assert((1 << kStageShift) == A && (1 << kSlotShift) == B, "rings indexed by masks");
+    static_assert(A % kIssuers == 0, "an A stage keeps its issuer within a job");
+    static_assert(A % kDqGroups == 0, "each dequantising group owns whole A stages");
+    // A ring, B ring, raw ring, barriers, TMEM address; +1 KB to align
+    static constexpr int kSmemBytes = 1024 + A * kABytes + B * kBBytes + R * kRawBytes + 320;
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+};
+// Chunks, whose routed experts have few rows each: most of shared memory to
+// the A ring, whose loop dequantise -> MMA -> release then bounds the kernel,
+// two stages per dequantising group; two B slots hold up to 16 K-blocks of
+// 16-row items. Long prompts (~32 rows an expert, often more): four B slots,
+// as two would hold only four K-blocks of 48- or 64-row items.
+using RingsChunk = PfRings<8, 2, 3, true>;
+using RingsPrompt = PfRings<4, 4, 4, false>;
 
 // Shared-memory matrix descriptor of a K-major operand tile whose rows are 128
 // bytes apart with the 128-byte swizzle (8-row atoms of 1024 bytes).
@@ -126,6 +144,13 @@ __device__ __forceinline__ float act_fn(float z, int act) {
 
 // A job: one M tile of one item over K-blocks kb0 .. kb0 + nkb - 1, part
 // `part` of the tile's ks[fam] parts.
+// The routed experts' token rows. Maps 0-3 see them as [K-block][row][64]
+// and load boxes of 16 << i rows by min(8 >> i, K-blocks) K-blocks, a whole B
+// slot at once; map 4 loads 2-D boxes of 16 rows by one K-block.
+struct PfRowMaps {
+    CUtensorMap r[5];
+};
+
 struct Job {
     int item, fam, tile, part, kb0, nkb;
 };
@@ -180,6 +205,19 @@ __device__ __forceinline__ Job decode_job(const Plan& p, const PfArgs& a, int j)
 
 __device__ __forceinline__ int pad16(int n) { return n <= 16 ? 16 : (n + 15) & ~15; }
 
+// Token rows of a job's B operand (the MMA's N): a routed expert's rows padded
+// to a multiple of 16, or to a power of two from 16 where they are loaded one
+// 3-D box per B slot; the shared expert's
+// token block padded to a multiple of 16, or all kPfMaxN when there are several
+// blocks (rows past the last token read as zeros).
+__device__ __forceinline__ int job_rows(const PfArgs& a, int fam, int np, bool rows3d) {
+    if (fam == 0) return a.n_fam0 > 1 ? kPfMaxN : pad16(np);
+    if (!rows3d) return pad16(np);
+    int n = 16;
+    while (n < np) n <<= 1;
+    return n;
+}
+
 __device__ __forceinline__ bool wait_flag(const uint32_t* p, uint32_t want, volatile int* abort) {
     for (uint64_t t0 = 0;;) {
         uint32_t v;
@@ -193,9 +231,13 @@ __device__ __forceinline__ bool wait_flag(const uint32_t* p, uint32_t want, vola
     }
 }
 
+template <class Rg>
 __global__ void __launch_bounds__(kThreads, 1)
     pf_gemm_kernel(const __grid_constant__ PfArgs a, const int phase, const __grid_constant__ CUtensorMap map0,
-                   const __grid_constant__ CUtensorMap map1) {
+                   const __grid_constant__ PfRowMaps rmaps) {
+    constexpr int kStages = Rg::kStages, kSlotsB = Rg::kSlotsB, kRawStages = Rg::kRawStages;
+    constexpr int kStageShift = Rg::kStageShift, kSlotShift = Rg::kSlotShift;
+    constexpr bool kRows3d = Rg::kRows3d;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -358,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- token rows ----------------
         if (lane == 0) {
             ptx::prefetch_tensormap(&map0);
-            ptx::prefetch_tensormap(&map1);
+            for (int q = kRows3d ? 0 : 4; q < (kRows3d ? 4 : 5); ++q) ptx::prefetch_tensormap(&rmaps.r[q]);
             int s = 0;
             uint32_t ph = 0;
             int issued = 0;
@@ -366,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = blockIdx.x; j < P.n_jobs && ok; j += gridDim.x) {
                 const Job b = decode_job(P, a, j);
                 const PfItem it = a.items[b.item];
-                const int nb = pad16(it.np);
+                const int nb = job_rows(a, b.fam, it.np, kRows3d);
                 const int kpb = kPfMaxN / nb;  // K-blocks per slot
                 const int nkb = b.nkb;
                 for (int kb0 = 0; kb0 < nkb; kb0 += kpb) {
@@ -378,19 +420,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     unsigned char* bt = ringB + s * kBBytes;
-                    ptx::mbar_arrive_expect_tx(b_full + s, (uint32_t)(nk * nb * 128));
-                    for (int kk = 0; kk < nk; ++kk) {
-                        unsigned char* dst = bt + kk * nb * 128;
-                        const int x = (b.kb0 + kb0 + kk) * 64;
-                        if (b.fam == 0 && a.n_fam0 == 1) {
-                            ptx::tma_load_2d(dst, &map0, x, 0, b_full + s);  // one box of all the rows
-                        } else {
-                            // 16-row boxes (family 0 too when it has several
-                            // token blocks: its map then has 16-row boxes)
-                            const CUtensorMap* m = b.fam == 0 ? &map0 : &map1;
+                    if (b.fam == 1 && !kRows3d) {
+                        // a routed expert: 16-row boxes, one K-block each
+                        ptx::mbar_arrive_expect_tx(b_full + s, (uint32_t)(nk * nb * 128));
+                        for (int kk = 0; kk < nk; ++kk)
                             for (int r0 = 0; r0 < nb; r0 += 16)
-                                ptx::tma_load_2d(dst + r0 * 128, m, x, it.pb + r0, b_full + s);
-                        }
+                                ptx::tma_load_2d(bt + (kk * nb + r0) * 128, &rmaps.r[4], (b.kb0 + kb0 + kk) * 64,
+                                                 it.pb + r0, b_full + s);
+                    } else if (b.fam == 1) {
+                        // a routed expert: one box of the slot's kpb K-blocks
+                        // (K-blocks past the job's last are loaded and not read)
+                        const int q = nb == 16 ? 0 : nb == 32 ? 1 : nb == 64 ? 2 : 3;
+                        const int depth = min(kpb, P.kblocks[1]);
+                        ptx::mbar_arrive_expect_tx(b_full + s, (uint32_t)(depth * nb * 128));
+                        ptx::tma_load_3d(bt, &rmaps.r[q], 0, it.pb, b.kb0 + kb0, b_full + s);
+                    } else {
+                        // the shared expert: one box of the token block's rows per
+                        // K-block (rows past the last token read as zeros)
+                        ptx::mbar_arrive_expect_tx(b_full + s, (uint32_t)(nk * nb * 128));
+                        for (int kk = 0; kk < nk; ++kk)
+                            ptx::tma_load_2d(bt + kk * nb * 128, &map0, (b.kb0 + kb0 + kk) * 64, it.pb, b_full + s);
                     }
                     ++issued;
                     if (++s == kSlotsB) {
@@ -426,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int njob = 0;
             for (int j = blockIdx.x; j < P.n_jobs; j += gridDim.x, ++njob) {
                 const Job b = decode_job(P, a, j);
-                const int nb = pad16(a.items[b.item].np);
+                const int nb = job_rows(a, b.fam, a.items[b.item].np, kRows3d);
                 const int kpb = kPfMaxN / nb;
                 const int nkb = b.nkb;
                 const int nI = nb <= 64 ? 4 : 2;
@@ -494,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = blockIdx.x; j < P.n_jobs; j += gridDim.x, ++njob) {
             const Job b = decode_job(P, a, j);
             const PfItem it = a.items[b.item];
-            const int nb = pad16(it.np);
+            const int nb = job_rows(a, b.fam, it.np, kRows3d);
             const int buf = njob & 1;
             if (!__all_sync(kFull, ptx::mbar_wait_sleep(acc_full + buf, (njob >> 1) & 1, abortp))) {
                 if (lane == 0) record(6, j, 0);
@@ -554,15 +603,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             } else {
                 const int n = kTileM * b.tile + row;
+                // output row of each column: the token (family 0) or the pair
+                // index (family 1); lane l holds that of columns l, 32 + l, ...
+                int prow[kPfMaxN / 32];
+#pragma unroll
+                for (int q = 0; q < kPfMaxN / 32; ++q) {
+                    const int col = 32 * q + lane;
+                    prow[q] = col >= it.np ? 0 : b.fam == 0 ? it.pb + col : a.pair[it.pb + col];
+                }
                 for (int c = 0; c < nb; c += 16) {
                     uint32_t v[16];
                     load_sum(c, v);
+                    const int pq = c < 32 ? prow[0] : c < 64 ? prow[1] : c < 96 ? prow[2] : prow[3];
 #pragma unroll
                     for (int m = 0; m < 16; ++m) {
                         const int col = c + m;
+                        const int orow = __shfl_sync(kFull, pq, col & 31);
                         if (col >= it.np) break;
-                        const size_t orow = b.fam == 0 ? (size_t)(it.pb + col) : (size_t)a.pair[it.pb + col];
-                        a.out[b.fam][orow * a.d + n] = __uint_as_float(v[m]);
+                        a.out[b.fam][(size_t)orow * a.d + n] = __uint_as_float(v[m]);
                     }
                 }
             }
@@ -572,8 +630,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= kWarpDq && warp < kWarpDq + kDqGroups * kDqWarps) {
         // ---------------- dequantisation ----------------
-        // group g owns A stage g (the K-blocks whose running index is g mod 4);
-        // thread t of a group dequantises A row t, all 64 inputs
+        // group g takes the K-blocks whose running index c is g mod 4, into A
+        // stage c mod kStages; thread t of a group dequantises A row t, all 64
+        // inputs, from words it loads before it releases the raw stage
         const int grp = (warp - kWarpDq) / kDqWarps, wg = (warp - kWarpDq) % kDqWarps;
         const int rho = wg * 32 + lane;
         int tile_raw, rlane;
@@ -593,9 +652,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       : kUnit * 4096 + tile_raw * 128 + sb_pos(rlane) * 4;
         const int sb_step = phase == 1 ? kRecord : 512;
         const int swz = rho & 7;
-        const uint32_t arow = ptx::smem_addr(ringA + grp * kABytes + rho * 128);
-        int r = 0, s = 0;
-        uint32_t rph = 0, gph = 0;
+        const uint32_t arow0 = ptx::smem_addr(ringA + rho * 128);
+        int r = 0;
+        uint32_t rph = 0, cb = 0;
         for (int j = blockIdx.x; j < P.n_jobs; j += gridDim.x) {
             const Job b = decode_job(P, a, j);
             const int nkb = b.nkb;
@@ -604,7 +663,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool have = ptx::mbar_wait_sleep(raw_full + r, rph, abortp);
                 if (!have && lane == 0) record(7, j, kb0);
                 if (!have && lane == 0 && !*abortp) fail(64u);
-                const int u = (grp - s) & 3;  // this group's K-block of the unit, if any
+                const int u = (grp - (int)(cb & 3)) & 3;  // this group's K-block of the unit, if any
+                const uint32_t c = cb + (uint32_t)u;
+                const int st = (int)(c & (kStages - 1));
+                const uint32_t arow = arow0 + st * kABytes;
                 uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;
                 uint32_t w = 0;
                 if (have && u < nu) {
@@ -616,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(raw_empty + r);
                 if (u < nu) {
-                    const bool free_a = have && ptx::mbar_wait_sleep(a_empty + grp, gph ^ 1, abortp);
+                    const bool free_a = have && ptx::mbar_wait_sleep(a_empty + st, ((c >> kStageShift) & 1) ^ 1, abortp);
                     if (free_a) {
                         const __half2 s2 = __half2half2(__ushort_as_half((unsigned short)(w & 0xFFFFu)));
                         const __half2 b2 = __half2half2(__ushort_as_half((unsigned short)(w >> 16)));
@@ -630,10 +692,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!*abortp) fail(64u);
                     }
                     __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(a_full + grp);
-                    gph ^= 1;
+                    if (lane == 0) ptx::mbar_arrive(a_full + st);
                 }
-                s = (s + nu) & 3;
+                cb += (uint32_t)nu;
                 if (++r == kRawStages) {
                     r = 0;
                     rph ^= 1;
@@ -757,6 +818,22 @@ EncodeTiled encode_fn() {
 }
 
 // fp16 [rows][cols] row-major, boxes of 64 columns x box_rows rows, 128-byte swizzle.
+// fp16 [rows][cols] row-major seen as [cols / 64][rows][64]: boxes of 64
+// columns x box_rows rows x box_kb K-blocks, 128-byte swizzle.
+cudaError_t encode_rows3(CUtensorMap* m, const void* base, int rows, int cols, int box_rows, int box_kb) {
+    EncodeTiled fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    if ((reinterpret_cast<uintptr_t>(base) & 15) || cols % 64 || rows < 1) return cudaErrorInvalidValue;
+    const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(cols / 64)};
+    const cuuint64_t strides[2] = {(cuuint64_t)cols * 2, 128};
+    const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)box_kb};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t encode_rows(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) {
     EncodeTiled fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
@@ -813,21 +890,28 @@ cudaError_t launch_pf_gather(const uint16_t* x, int T, int d, const int32_t* pai
 
 cudaError_t launch_pf_gemm(const PfArgs& a, int phase, const void* b0, const void* b1, const int rows[2],
                            cudaStream_t s, int* launched) {
-    {
-        cudaError_t e = ensure_smem_attr((const void*)pf_gemm_kernel, kSmemBytes);
-        if (e != cudaSuccess) return e;
-    }
     if ((phase != 1 && phase != 2) || a.n_items < 1 || a.n_fam0 < 0 || a.n_fam0 > a.n_items || a.d % kTileM ||
         a.inter[0] % 64 || a.inter[1] % 64)
         return cudaErrorInvalidValue;
-    CUtensorMap m0, m1;
+    CUtensorMap m0;
     const int k0 = phase == 1 ? a.d : a.inter[0], k1 = phase == 1 ? a.d : a.inter[1];
     // family 0 is the shared expert over every token row: one item per block
     // of kPfMaxN tokens (a single one loads all its rows as one box)
     if (rows[0] != a.T || a.T < 1 || a.n_fam0 != (a.T + kPfMaxN - 1) / kPfMaxN) return cudaErrorInvalidValue;
-    const int box0 = a.n_fam0 > 1 ? 16 : a.T <= 16 ? 16 : (a.T + 15) & ~15;
+    const int box0 = a.n_fam0 > 1 ? kPfMaxN : a.T <= 16 ? 16 : (a.T + 15) & ~15;
     cudaError_t e = encode_rows(&m0, b0, rows[0], k0, box0);
-    if (e == cudaSuccess) e = encode_rows(&m1, b1, std::max(rows[1], 1), k1, 16);
+    // the chunk layout when the routed experts average at most 24 rows
+    const int n_routed = a.n_items - a.n_fam0;
+    const bool chunk = (long)rows[1] <= 24L * n_routed;
+    PfRowMaps rm{};
+    if (chunk)
+        for (int q = 0; q < 4 && e == cudaSuccess; ++q)
+            e = encode_rows3(&rm.r[q], b1, std::max(rows[1], 1), k1, 16 << q, std::min(8 >> q, k1 / 64));
+    else if (e == cudaSuccess)
+        e = encode_rows(&rm.r[4], b1, std::max(rows[1], 1), k1, 16);
+    if (e == cudaSuccess)
+        e = chunk ? ensure_smem_attr((const void*)pf_gemm_kernel<RingsChunk>, RingsChunk::kSmemBytes)
+                  : ensure_smem_attr((const void*)pf_gemm_kernel<RingsPrompt>, RingsPrompt::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int tiles0 = phase == 1 ? a.inter[0] / 64 : a.d / kTileM;
     const int tiles1 = phase == 1 ? a.inter[1] / 64 : a.d / kTileM;
@@ -849,7 +933,10 @@ cudaError_t launch_pf_gemm(const PfArgs& a, int phase, const void* b0, const voi
     }
     const int jobs = n_t[0] * b.ks[0] + n_t[1] * b.ks[1];
     const int grid = std::min(jobs, num_sms());
-    pf_gemm_kernel<<<grid, kThreads, kSmemBytes, s>>>(b, phase, m0, m1);
+    if (chunk)
+        pf_gemm_kernel<RingsChunk><<<grid, kThreads, RingsChunk::kSmemBytes, s>>>(b, phase, m0, rm);
+    else
+        pf_gemm_kernel<RingsPrompt><<<grid, kThreads, RingsPrompt::kSmemBytes, s>>>(b, phase, m0, rm);
     if (launched) *launched = 1;
     if (split_tiles > 0) {
         cudaError_t e = cudaGetLastError();
