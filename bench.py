@@ -722,7 +722,7 @@ def run_ours(args, world, rank, local):
     if rank == 0 and world == 1 and not args.no_cpu:
         times = oracle_layer_tokens(64, args.cpu_seconds, wl)
         layer_s = statistics.mean(times)
-        single = {"value": 1.0 / (layer_s * n_layers), "unit": "tok/s", "cores": 1, "kind": "oracle",
+        cpu_single = {"value": 1.0 / (layer_s * n_layers), "unit": "tok/s", "cores": 1, "kind": "oracle",
                   "sample": f"{len(times)} layer-tokens of decode_2816 (layers 0-1) single-threaded, "
                             f"extrapolated to {n_layers} layers per token"}
         if isinstance(cpu_par, tuple):
@@ -731,9 +731,9 @@ def run_ours(args, world, rank, local):
                    "sample": f"{P} forked single-threaded copies of the oracle, each running whole layer-tokens "
                              f"of decode_2816 (layer 0) for {args.cpu_seconds:g} s; layer-tokens per second "
                              f"over all copies, divided by {n_layers} layers per token",
-                   "single_thread": single}
+                   "single_thread": cpu_single}
         else:
-            cpu = dict(single, all_cores_error=None if cpu_par is None else repr(cpu_par))
+            cpu = dict(cpu_single, all_cores_error=None if cpu_par is None else repr(cpu_par))
 
     if rank != 0:
         return

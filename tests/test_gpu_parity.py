@@ -293,6 +293,30 @@ def test_prefill_split_k_small_launch(ctx):
         r.close()
 
 
+def test_prefill_chunk_skewed_rows_2816(ctx):
+    """A 128-token chunk of d = 2816 whose routing is skewed by the zbias:
+    expert 0 is in every token's top-k (one item of 128 rows), expert 1 in
+    about half of them, the rest spread thin. The launch still counts as a
+    chunk (a few rows per routed expert on average), so the big items go
+    through the chunk layout's 64- and 128-row token boxes."""
+    s = synth.SHAPES_2816
+    r = Rig(ctx, s, 7, 16)
+    try:
+        xb = synth.tokens(s, 7, 0, 128, True)
+        lg = oracle.router_logits(xb, r.w.router, s.n_experts, None)
+        k = s.top_k
+        kth = np.sort(lg, axis=1)[:, -k]  # each token's k-th largest logit
+        zb = np.zeros(s.n_experts, dtype=np.float32)
+        zb[0] = float(np.max(kth - lg[:, 0])) + 1.0
+        zb[1] = float(np.median(kth - lg[:, 1]))
+        ids, _ = r.forward(xb, zb, y_tokens=[0, 1, 63, 64, 127])
+        counts = np.bincount(ids.ravel(), minlength=s.n_experts)
+        assert counts[0] == 128 and 32 < counts[1] < 128, counts[:2]
+        assert ids.size / np.count_nonzero(counts) <= 24
+    finally:
+        r.close()
+
+
 def _prompt_check(r, xb, y_tokens):
     """One moe_forward_prompt call checked against the oracle: ids bit-exact,
     gates within 1e-6, the cache table after ONE step over all the call's ids,
