@@ -28,7 +28,7 @@ namespace moe {
 
 HostCache::HostCache(int n_experts, int slots, int policy)
     : E(n_experts), S(slots), policy(policy), step_index(0), slot_expert(slots, -1), use_count(slots, 0),
-      stamp(slots, 0), expert_slot(n_experts, -1), pinned(slots, 0) {}
+      stamp(slots, 0), expert_slot(n_experts, -1), pinned(slots, 0), seen(n_experts, 0) {}
 
 void HostCache::reset() {
     std::fill(slot_expert.begin(), slot_expert.end(), -1);
@@ -62,9 +62,19 @@ bool HostCache::step(const int32_t* ids, int n, StepResult& r) {
     r.hits = r.bypass = 0;
     for (int i = 0; i < n; ++i)
         if (ids[i] < 0 || ids[i] >= E) return false;
-    r.distinct.assign(ids, ids + n);
-    std::sort(r.distinct.begin(), r.distinct.end());
-    r.distinct.erase(std::unique(r.distinct.begin(), r.distinct.end()), r.distinct.end());
+    if (n <= 64) {
+        r.distinct.assign(ids, ids + n);
+        std::sort(r.distinct.begin(), r.distinct.end());
+        r.distinct.erase(std::unique(r.distinct.begin(), r.distinct.end()), r.distinct.end());
+    } else {
+        // a prefill step's thousands of ids: mark, then list in ascending order
+        for (int i = 0; i < n; ++i) seen[ids[i]] = 1;
+        for (int e = 0; e < E; ++e)
+            if (seen[e]) {
+                r.distinct.push_back(e);
+                seen[e] = 0;
+            }
+    }
     std::fill(pinned.begin(), pinned.end(), 0);
     // hits: touch and pin
     for (int e : r.distinct) {

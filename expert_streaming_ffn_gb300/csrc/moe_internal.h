@@ -89,6 +89,7 @@ class HostCache {
     int pick_victim() const;
     std::vector<int32_t> expert_slot;
     std::vector<uint8_t> pinned;
+    std::vector<uint8_t> seen;  // scratch of step(), all zero between calls
 };
 
 void group_pairs(const int32_t* ids, int n_pairs, int n_experts, int32_t* offsets, int32_t* perm);

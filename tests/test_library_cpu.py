@@ -84,7 +84,8 @@ def test_host_cache_golden_traces():
 
 @pytest.mark.parametrize("E,S,policy,batch", [(16, 4, moe.LFU, 2), (256, 16, moe.LFU, 8), (256, 64, moe.LRU, 64),
                                               (256, 16, moe.LRU, 8), (64, 1, moe.LFU, 3), (256, 256, moe.LFU, 8),
-                                              (1024, 32, moe.LFU, 128)])
+                                              (1024, 32, moe.LFU, 128), (256, 16, moe.LRU, 1024),
+                                              (256, 256, moe.LFU, 2048)])
 def test_host_cache_matches_oracle_trace(E, S, policy, batch):
     rng = np.random.default_rng(E * 7 + S + policy)
     c = moe.moe_host_cache_create(E, S, policy)
