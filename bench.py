@@ -1019,14 +1019,18 @@ def run_prefill(args, ctx, dev, stream, seed):
         if slots != s.n_experts:
             moe.moe_layer_destroy(h)
             h, w = make(s, slots, 0, w)
-        ms4, kt4, st4 = _prefill_pass(ctx, dev, stream, [h], xs[:1], y, prompt=True)
+        # all resident: the mean of 3 calls (the same work each time); streaming:
+        # one call on the fresh cache (a repeat would find it warm)
+        reps = 3 if slots == s.n_experts else 1
+        ms4, kt4, st4 = _prefill_pass(ctx, dev, stream, [h] * reps, xs[:1] * reps, y, prompt=True)
         moe.moe_layer_destroy(h)
+        ms4 /= reps
         kms4 = sum(kt4[k][1] for k in ("gemm_gateup", "gemm_down"))
         fl4 = sum(kt4[k][3] for k in ("gemm_gateup", "gemm_down"))
-        lm[name] = {"tok_s_per_layer": prompt / (ms4 * 1e-3), "wall_ms": ms4,
+        lm[name] = {"tok_s_per_layer": prompt / (ms4 * 1e-3), "wall_ms": ms4, "calls": reps,
                     "expert_TFLOPs": fl4 / (kms4 * 1e-3) / 1e12 if kms4 else None,
-                    "h2d_GB": st4[0]["bytes_h2d"] / 1e9,
-                    "exposed_copy_ms": st4[0]["exposed_copy_us"] / 1e3,
+                    "h2d_GB": st4[-1]["bytes_h2d"] / reps / 1e9,
+                    "exposed_copy_ms": st4[-1]["exposed_copy_us"] / reps / 1e3,
                     "kernels": _gemm_summary(kt4, peaks)}
     out["layer_major"] = lm
 

@@ -25,9 +25,14 @@ namespace moe {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kRouterWarps = 4;
+constexpr int kRouterWarps = 4;  // expert rows per block (decode and short inputs)
 constexpr int kRouterTB = 8;     // tokens per block
 constexpr int kRouterBatch = 8;  // runs per lane whose loads are issued together
+// Long inputs (prefill, T >= 64): router_wide_kernel, 8 warps by 8 tokens a
+// block with the token rows staged once as fp32, each warp taking 1 or 4
+// expert rows in turn (see there).
+constexpr int kRouterWideWarps = 8, kRouterWideTB = 8, kRouterWideBatch = 4;
+constexpr int kRouterWideMinT = 64, kRouterWideMaxD = 6144;
 
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
     uint4 v;
@@ -140,43 +145,76 @@ __device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
     return old;
 }
 
-template <int TB>
-__global__ void __launch_bounds__(kRouterWarps * 32, TB == 1 ? 5 : 1) router_kernel(const RouterParams p) {
+// The end of a router launch: the last block of each token block to finish
+// (counted on the token block's arrival counter) runs the top-k of its tokens
+// with its W warps and resets the counter. Each block's arrival is a release
+// of its logits, and the count the last one reads an acquire of all of them.
+template <int W>
+__device__ __forceinline__ void router_finish(const RouterParams& p, int t0, int nt, int warp, int lane) {
+    __shared__ int is_last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned prev = atom_add_acq_rel(p.counters + blockIdx.y, 1u);
+        is_last = prev == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!is_last) {
+        if (p.span && threadIdx.x == 0) atomicMax(p.span + 1, (unsigned long long)ptx::globaltimer());
+        return;
+    }
+    for (int j = warp; j < nt; j += W) {
+        const int t = t0 + j;
+        unsigned long long* hid = p.host_ids ? p.host_ids + (size_t)t * p.k : nullptr;
+        if (p.E <= 256)
+            topk_warp<8>(p.logits + (size_t)t * p.E, p.E, p.k, lane, p.ids + (size_t)t * p.k,
+                         p.gates + (size_t)t * p.k, hid, p.seq);
+        else
+            topk_warp_large(p.logits + (size_t)t * p.E, p.E, p.k, lane, p.ids + (size_t)t * p.k,
+                            p.gates + (size_t)t * p.k, hid, p.seq);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        p.counters[blockIdx.y] = 0;
+        if (p.span) atomicMax(p.span + 1, (unsigned long long)ptx::globaltimer());
+    }
+}
+
+template <int TB, int W, int KB>
+__global__ void __launch_bounds__(W * 32, TB == 1 ? 5 : 1) router_kernel(const RouterParams p) {
     extern __shared__ uint4 xsm[];  // the block's token rows, [nt][d / 8] of 8 bf16 each
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = blockIdx.x * kRouterWarps + warp;
+    const int e_first = blockIdx.x * W + warp;  // this warp's expert row
     const int t0 = blockIdx.y * TB;
     const int nt = min(TB, p.T - t0);
     const int runs = p.d >> 4;
     const int vec = p.d >> 3;
-    const bool has_row = e < p.E;
     // the next kernel may start now; this one reads x and writes y only
     // after the previous kernel has finished (griddepcontrol.wait below)
     ptx::pdl_launch_dependents();
     if (p.span && threadIdx.x == 0) atomicMin(p.span, (unsigned long long)ptx::globaltimer());
-    const uint8_t* row0 = p.codes + (size_t)(has_row ? e : 0) * p.d;
-    if (has_row)
-        for (int c = lane; c < runs && c < 32 * kRouterBatch; c += 32)
+    if (e_first < p.E) {
+        const uint8_t* row0 = p.codes + (size_t)e_first * p.d;
+        for (int c = lane; c < runs && c < 32 * KB; c += 32)
             asm volatile("prefetch.global.L2 [%0];" ::"l"(row0 + (size_t)c * 16));
+    }
     ptx::pdl_wait();
     if (p.zero) {
         const int nb = gridDim.x * gridDim.y * blockDim.x;
         for (int i = (blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x; i < p.zero_n; i += nb)
             p.zero[i] = 0.0f;
     }
-    const uint8_t* row = p.codes + (size_t)(has_row ? e : 0) * p.d;
-    const uint32_t* sbrow = p.sb + (size_t)(has_row ? e : 0) * (p.d >> 6);
     // Lane l owns runs c = l + 32 i (16 inputs each), walked in increasing c.
-    // A batch's loads are all in flight together; the first batch is issued
-    // before the token rows are staged, so the two latencies overlap.
-    // one token: six runs per lane in flight (d = 2816 has 5.5 per lane), few
-    // enough registers to share an SM with an FFN CTA; more tokens: eight
-    constexpr int kB = TB == 1 ? 6 : kRouterBatch;
-    uint4 q[kB];
-    uint32_t sbw[kB];
+    // A batch's KB loads are all in flight together; the first batch of the
+    // first row is issued before the token rows are staged, so the two
+    // latencies overlap.
+    uint4 q[KB];
+    uint32_t sbw[KB];
+    const uint8_t* row = nullptr;
+    const uint32_t* sbrow = nullptr;
+    bool has_row = false;
     auto load_batch = [&](int b0) {
 #pragma unroll
-        for (int i = 0; i < kB; ++i) {
+        for (int i = 0; i < KB; ++i) {
             const int c = lane + 32 * (b0 + i);
             if (has_row && c < runs) {
                 q[i] = ld_stream(row + (size_t)c * 16);
@@ -184,6 +222,12 @@ __global__ void __launch_bounds__(kRouterWarps * 32, TB == 1 ? 5 : 1) router_ker
             }
         }
     };
+    auto set_row = [&](int e) {
+        has_row = e < p.E;
+        row = p.codes + (size_t)(has_row ? e : 0) * p.d;
+        sbrow = p.sb + (size_t)(has_row ? e : 0) * (p.d >> 6);
+    };
+    set_row(e_first);
     load_batch(0);
     {
         // the token rows, eight loads per thread in flight at a time
@@ -201,13 +245,14 @@ __global__ void __launch_bounds__(kRouterWarps * 32, TB == 1 ? 5 : 1) router_ker
     }
     __syncthreads();
     if (has_row) {
+        const int e = e_first;
         float acc[TB];
 #pragma unroll
         for (int j = 0; j < TB; ++j) acc[j] = 0.0f;
-        for (int b0 = 0; 32 * b0 < runs; b0 += kB) {
+        for (int b0 = 0; 32 * b0 < runs; b0 += KB) {
             if (b0 > 0) load_batch(b0);
 #pragma unroll
-            for (int i = 0; i < kB; ++i) {
+            for (int i = 0; i < KB; ++i) {
                 const int c = lane + 32 * (b0 + i);
                 if (c >= runs) continue;
                 const float2 f = unpack_sb(sbw[i]);
@@ -237,35 +282,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32, TB == 1 ? 5 : 1) router_ker
             }
         }
     }
-    // The last block of this token block to finish runs the top-k. Each
-    // block's arrival is a release of its logits, and the count the last one
-    // reads an acquire of all of them.
-    __shared__ int is_last;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const unsigned prev = atom_add_acq_rel(p.counters + blockIdx.y, 1u);
-        is_last = prev == gridDim.x - 1;
-    }
-    __syncthreads();
-    if (!is_last) {
-        if (p.span && threadIdx.x == 0) atomicMax(p.span + 1, (unsigned long long)ptx::globaltimer());
-        return;
-    }
-    for (int j = warp; j < nt; j += kRouterWarps) {
-        const int t = t0 + j;
-        unsigned long long* hid = p.host_ids ? p.host_ids + (size_t)t * p.k : nullptr;
-        if (p.E <= 256)
-            topk_warp<8>(p.logits + (size_t)t * p.E, p.E, p.k, lane, p.ids + (size_t)t * p.k,
-                         p.gates + (size_t)t * p.k, hid, p.seq);
-        else
-            topk_warp_large(p.logits + (size_t)t * p.E, p.E, p.k, lane, p.ids + (size_t)t * p.k,
-                            p.gates + (size_t)t * p.k, hid, p.seq);
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        p.counters[blockIdx.y] = 0;
-        if (p.span) atomicMax(p.span + 1, (unsigned long long)ptx::globaltimer());
-    }
+    router_finish<W>(p, t0, nt, warp, lane);
 }
 
 // One block per (token, 32 output columns). Term j < ns is the j-th group of
@@ -323,24 +340,164 @@ __global__ void combine_kernel(const float* __restrict__ o, const float* __restr
     y[(size_t)t * d + n] = acc;
 }
 
+// The router over a long input. The block's token rows are staged once as
+// fp32 (the exact values of the bf16 inputs), laid out so that the 16 inputs
+// of lane l's run slot i are four float4 at [token][i][quad][l]: a warp's
+// loads are conflict-free and the loop does no unpacking. Each warp takes R
+// expert rows in turn, so a staged token row serves 8 R rows (R = 4 for long
+// prompts, 1 for a chunk, whose fewer token blocks need more blocks across
+// the experts). Every logit is one warp's sum over the same runs in the same
+// order, with the same butterfly, as in router_kernel: the same bits.
+template <int R>
+__global__ void __launch_bounds__(kRouterWideWarps * 32, 2) router_wide_kernel(const RouterParams p) {
+    constexpr int TB = kRouterWideTB, W = kRouterWideWarps, KB = kRouterWideBatch;
+    extern __shared__ float4 xw[];  // [nt][NI][4][32]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e_first = (blockIdx.x * W + warp) * R;
+    const int t0 = blockIdx.y * TB;
+    const int nt = min(TB, p.T - t0);
+    const int runs = p.d >> 4, NI = (runs + 31) >> 5;
+    ptx::pdl_launch_dependents();
+    if (p.span && threadIdx.x == 0) atomicMin(p.span, (unsigned long long)ptx::globaltimer());
+    if (e_first < p.E) {
+        const uint8_t* row0 = p.codes + (size_t)e_first * p.d;
+        for (int c = lane; c < runs && c < 32 * KB; c += 32)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(row0 + (size_t)c * 16));
+    }
+    ptx::pdl_wait();
+    if (p.zero) {
+        const int nb = gridDim.x * gridDim.y * blockDim.x;
+        for (int i = (blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x; i < p.zero_n; i += nb)
+            p.zero[i] = 0.0f;
+    }
+    uint4 q[KB];
+    uint32_t sbw[KB];
+    const uint8_t* row = nullptr;
+    const uint32_t* sbrow = nullptr;
+    bool has_row = false;
+    auto load_batch = [&](int b0) {
+#pragma unroll
+        for (int i = 0; i < KB; ++i) {
+            const int c = lane + 32 * (b0 + i);
+            if (has_row && c < runs) {
+                q[i] = ld_stream(row + (size_t)c * 16);
+                sbw[i] = __ldg(sbrow + (c >> 2));
+            }
+        }
+    };
+    auto set_row = [&](int e) {
+        has_row = e < p.E;
+        row = p.codes + (size_t)(has_row ? e : 0) * p.d;
+        sbrow = p.sb + (size_t)(has_row ? e : 0) * (p.d >> 6);
+    };
+    set_row(e_first);
+    load_batch(0);
+    {
+        // 8-input chunk k of token j: run k / 2, quads 2 (k & 1) and 2 (k & 1) + 1
+        const int per_row = p.d >> 3;
+        const uint4* xg = reinterpret_cast<const uint4*>(p.x + (size_t)t0 * p.d);
+        const int n = nt * per_row;
+        for (int i0 = threadIdx.x; i0 < n; i0 += 4 * blockDim.x) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (i0 + u * (int)blockDim.x < n) v[u] = __ldg(xg + i0 + u * blockDim.x);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int idx = i0 + u * (int)blockDim.x;
+                if (idx < n) {
+                    const int j = idx / per_row, k = idx - j * per_row;
+                    const int c = k >> 1, base = ((j * NI + (c >> 5)) * 4 + 2 * (k & 1)) * 32 + (c & 31);
+                    xw[base] = make_float4(bf16_lo(v[u].x), bf16_hi(v[u].x), bf16_lo(v[u].y), bf16_hi(v[u].y));
+                    xw[base + 32] = make_float4(bf16_lo(v[u].z), bf16_hi(v[u].z), bf16_lo(v[u].w), bf16_hi(v[u].w));
+                }
+            }
+        }
+    }
+    __syncthreads();
+    for (int rr = 0; rr < R; ++rr) {
+        const int e = e_first + rr;
+        if (rr > 0) {
+            set_row(e);
+            load_batch(0);
+        }
+        if (!has_row) break;
+        float acc[TB];
+#pragma unroll
+        for (int j = 0; j < TB; ++j) acc[j] = 0.0f;
+        for (int b0 = 0; 32 * b0 < runs; b0 += KB) {
+            if (b0 > 0) load_batch(b0);
+#pragma unroll
+            for (int i = 0; i < KB; ++i) {
+                const int c = lane + 32 * (b0 + i);
+                if (c >= runs) continue;
+                const float2 f = unpack_sb(sbw[i]);
+                const uint32_t qw[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
+                float w[16];
+#pragma unroll
+                for (int m = 0; m < 16; ++m) w[m] = __fmaf_rn(f.x, byte_code(qw[m >> 2], m & 3), f.y);
+                const float4* xs = xw + (size_t)(b0 + i) * 4 * 32 + lane;
+#pragma unroll
+                for (int j = 0; j < TB; ++j) {
+                    if (j < nt) {
+                        const float4* xj = xs + (size_t)j * NI * 4 * 32;
+#pragma unroll
+                        for (int qq = 0; qq < 4; ++qq) {
+                            const float4 xv = xj[qq * 32];
+                            acc[j] = __fmaf_rn(w[4 * qq + 0], xv.x, acc[j]);
+                            acc[j] = __fmaf_rn(w[4 * qq + 1], xv.y, acc[j]);
+                            acc[j] = __fmaf_rn(w[4 * qq + 2], xv.z, acc[j]);
+                            acc[j] = __fmaf_rn(w[4 * qq + 3], xv.w, acc[j]);
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < TB; ++j) {
+            if (j < nt) {
+                float v = acc[j];
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(kFull, v, off));
+                if (lane == 0) p.logits[(size_t)(t0 + j) * p.E + e] = p.zbias ? __fadd_rn(v, p.zbias[e]) : v;
+            }
+        }
+    }
+    router_finish<W>(p, t0, nt, warp, lane);
+}
+
 }  // namespace
 
 cudaError_t launch_router(const RouterParams& p, cudaStream_t s, bool pdl) {
-    cudaError_t e = ensure_smem_attr((const void*)router_kernel<kRouterTB>, (size_t)kRouterTB * kMaxDModel * 2);
+    cudaError_t e =
+        ensure_smem_attr((const void*)router_kernel<kRouterTB, kRouterWarps, kRouterBatch>, (size_t)kRouterTB * kMaxDModel * 2);
     if (e != cudaSuccess) return e;
-    e = ensure_smem_attr((const void*)router_kernel<1>, (size_t)kMaxDModel * 2);
+    e = ensure_smem_attr((const void*)router_kernel<1, kRouterWarps, 6>, (size_t)kMaxDModel * 2);
     if (e != cudaSuccess) return e;
-    const size_t sm = (size_t)std::min(kRouterTB, p.T) * p.d * 2;
+    const auto wide_smem = [](int d) { return (size_t)kRouterWideTB * (((d >> 4) + 31) >> 5) * 4 * 32 * 16; };
+    e = ensure_smem_attr((const void*)router_wide_kernel<1>, wide_smem(kRouterWideMaxD));
+    if (e == cudaSuccess) e = ensure_smem_attr((const void*)router_wide_kernel<4>, wide_smem(kRouterWideMaxD));
+    if (e != cudaSuccess) return e;
     cudaLaunchAttribute la;
     if (p.T == 1) {
-        const cudaLaunchConfig_t c =
-            launch_config(dim3((p.E + kRouterWarps - 1) / kRouterWarps, 1), dim3(kRouterWarps * 32), sm, s, pdl, &la);
-        return cudaLaunchKernelEx(&c, router_kernel<1>, p);
+        const cudaLaunchConfig_t c = launch_config(dim3((p.E + kRouterWarps - 1) / kRouterWarps, 1),
+                                                   dim3(kRouterWarps * 32), (size_t)p.d * 2, s, pdl, &la);
+        return cudaLaunchKernelEx(&c, router_kernel<1, kRouterWarps, 6>, p);
     }
+    if (p.T >= kRouterWideMinT && p.d <= kRouterWideMaxD) {
+        // four expert rows a warp once there are enough token blocks to fill the GPU
+        const int R = p.T >= 512 ? 4 : 1;
+        const int rows = kRouterWideWarps * R;
+        const cudaLaunchConfig_t c =
+            launch_config(dim3((p.E + rows - 1) / rows, (p.T + kRouterWideTB - 1) / kRouterWideTB),
+                          dim3(kRouterWideWarps * 32), wide_smem(p.d), s, pdl, &la);
+        return R == 4 ? cudaLaunchKernelEx(&c, router_wide_kernel<4>, p) : cudaLaunchKernelEx(&c, router_wide_kernel<1>, p);
+    }
+    const size_t sm = (size_t)std::min(kRouterTB, p.T) * p.d * 2;
     const cudaLaunchConfig_t c = launch_config(
         dim3((p.E + kRouterWarps - 1) / kRouterWarps, (p.T + kRouterTB - 1) / kRouterTB), dim3(kRouterWarps * 32), sm, s,
         pdl, &la);
-    return cudaLaunchKernelEx(&c, router_kernel<kRouterTB>, p);
+    return cudaLaunchKernelEx(&c, router_kernel<kRouterTB, kRouterWarps, kRouterBatch>, p);
 }
 
 cudaError_t launch_part_reduce(const float* part0, const float* part1, int cs, int cr, int k, int d, int T, float* y,
