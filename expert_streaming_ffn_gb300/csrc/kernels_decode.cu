@@ -12,6 +12,9 @@
 //                 (call number << 32 | id), so the host sees the routing as
 //                 soon as it lands, without a copy, an event or a fence
 //                 ([P1] §2.4: the ids go to the CPU for the cache lookup).
+// router_wide_kernel  the same routing for 64 tokens or more (prefill), with
+//                 the block's token rows staged once as fp32 and each warp
+//                 taking several expert rows: the same logits, bit for bit.
 // combine_kernel  y += sum_r gate_r * o_r in rank order ([P1] §6.2.3 fusion).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
