@@ -32,8 +32,8 @@ constexpr int kRouterWarps = 4;  // expert rows per block (decode and short inpu
 constexpr int kRouterTB = 8;     // tokens per block
 constexpr int kRouterBatch = 8;  // runs per lane whose loads are issued together
 // Long inputs (prefill, T >= 64): router_wide_kernel, 8 warps by 8 tokens a
-// block with the token rows staged once as fp32, each warp taking 1 or 4
-// expert rows in turn (see there).
+// block with the token rows staged once as fp32, each warp taking 2 or 4
+// expert rows, two at a time (see there).
 constexpr int kRouterWideWarps = 8, kRouterWideTB = 8, kRouterWideBatch = 4;
 constexpr int kRouterWideMinT = 64, kRouterWideMaxD = 6144;
 
@@ -347,13 +347,16 @@ __global__ void combine_kernel(const float* __restrict__ o, const float* __restr
 // fp32 (the exact values of the bf16 inputs), laid out so that the 16 inputs
 // of lane l's run slot i are four float4 at [token][i][quad][l]: a warp's
 // loads are conflict-free and the loop does no unpacking. Each warp takes R
-// expert rows in turn, so a staged token row serves 8 R rows (R = 4 for long
-// prompts, 1 for a chunk, whose fewer token blocks need more blocks across
+// expert rows, two at a time, so that every input it loads from shared memory
+// feeds two FMAs (one input per FMA would need four times the SM's
+// shared-memory bandwidth); a staged token row serves 8 R rows (R = 4 for long
+// prompts, 2 for a chunk, whose fewer token blocks need more blocks across
 // the experts). Every logit is one warp's sum over the same runs in the same
 // order, with the same butterfly, as in router_kernel: the same bits.
 template <int R>
 __global__ void __launch_bounds__(kRouterWideWarps * 32, 2) router_wide_kernel(const RouterParams p) {
-    constexpr int TB = kRouterWideTB, W = kRouterWideWarps, KB = kRouterWideBatch;
+    constexpr int TB = kRouterWideTB, W = kRouterWideWarps, KB = kRouterWideBatch, RP = 2;
+    static_assert(R % RP == 0, "rows in pairs");
     extern __shared__ float4 xw[];  // [nt][NI][4][32]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e_first = (blockIdx.x * W + warp) * R;
@@ -362,38 +365,44 @@ __global__ void __launch_bounds__(kRouterWideWarps * 32, 2) router_wide_kernel(c
     const int runs = p.d >> 4, NI = (runs + 31) >> 5;
     ptx::pdl_launch_dependents();
     if (p.span && threadIdx.x == 0) atomicMin(p.span, (unsigned long long)ptx::globaltimer());
-    if (e_first < p.E) {
-        const uint8_t* row0 = p.codes + (size_t)e_first * p.d;
-        for (int c = lane; c < runs && c < 32 * KB; c += 32)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(row0 + (size_t)c * 16));
-    }
+    for (int r = 0; r < RP; ++r)
+        if (e_first + r < p.E) {
+            const uint8_t* row0 = p.codes + (size_t)(e_first + r) * p.d;
+            for (int c = lane; c < runs && c < 32 * KB; c += 32)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(row0 + (size_t)c * 16));
+        }
     ptx::pdl_wait();
     if (p.zero) {
         const int nb = gridDim.x * gridDim.y * blockDim.x;
         for (int i = (blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x; i < p.zero_n; i += nb)
             p.zero[i] = 0.0f;
     }
-    uint4 q[KB];
-    uint32_t sbw[KB];
-    const uint8_t* row = nullptr;
-    const uint32_t* sbrow = nullptr;
-    bool has_row = false;
+    uint4 q[RP][KB];
+    uint32_t sbw[RP][KB];
+    const uint8_t* row[RP];
+    const uint32_t* sbrow[RP];
+    bool has[RP];
     auto load_batch = [&](int b0) {
 #pragma unroll
-        for (int i = 0; i < KB; ++i) {
-            const int c = lane + 32 * (b0 + i);
-            if (has_row && c < runs) {
-                q[i] = ld_stream(row + (size_t)c * 16);
-                sbw[i] = __ldg(sbrow + (c >> 2));
+        for (int r = 0; r < RP; ++r)
+#pragma unroll
+            for (int i = 0; i < KB; ++i) {
+                const int c = lane + 32 * (b0 + i);
+                if (has[r] && c < runs) {
+                    q[r][i] = ld_stream(row[r] + (size_t)c * 16);
+                    sbw[r][i] = __ldg(sbrow[r] + (c >> 2));
+                }
             }
+    };
+    auto set_rows = [&](int e0) {
+#pragma unroll
+        for (int r = 0; r < RP; ++r) {
+            has[r] = e0 + r < p.E;
+            row[r] = p.codes + (size_t)(has[r] ? e0 + r : 0) * p.d;
+            sbrow[r] = p.sb + (size_t)(has[r] ? e0 + r : 0) * (p.d >> 6);
         }
     };
-    auto set_row = [&](int e) {
-        has_row = e < p.E;
-        row = p.codes + (size_t)(has_row ? e : 0) * p.d;
-        sbrow = p.sb + (size_t)(has_row ? e : 0) * (p.d >> 6);
-    };
-    set_row(e_first);
+    set_rows(e_first);
     load_batch(0);
     {
         // 8-input chunk k of token j: run k / 2, quads 2 (k & 1) and 2 (k & 1) + 1
@@ -418,27 +427,32 @@ __global__ void __launch_bounds__(kRouterWideWarps * 32, 2) router_wide_kernel(c
         }
     }
     __syncthreads();
-    for (int rr = 0; rr < R; ++rr) {
-        const int e = e_first + rr;
+    for (int rr = 0; rr < R; rr += RP) {
+        const int e0 = e_first + rr;
         if (rr > 0) {
-            set_row(e);
+            set_rows(e0);
             load_batch(0);
         }
-        if (!has_row) break;
-        float acc[TB];
+        if (!has[0]) break;
+        float acc[RP][TB];
 #pragma unroll
-        for (int j = 0; j < TB; ++j) acc[j] = 0.0f;
+        for (int r = 0; r < RP; ++r)
+#pragma unroll
+            for (int j = 0; j < TB; ++j) acc[r][j] = 0.0f;
         for (int b0 = 0; 32 * b0 < runs; b0 += KB) {
             if (b0 > 0) load_batch(b0);
 #pragma unroll
             for (int i = 0; i < KB; ++i) {
                 const int c = lane + 32 * (b0 + i);
                 if (c >= runs) continue;
-                const float2 f = unpack_sb(sbw[i]);
-                const uint32_t qw[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
-                float w[16];
+                float w[RP][16];
 #pragma unroll
-                for (int m = 0; m < 16; ++m) w[m] = __fmaf_rn(f.x, byte_code(qw[m >> 2], m & 3), f.y);
+                for (int r = 0; r < RP; ++r) {
+                    const float2 f = unpack_sb(sbw[r][i]);
+                    const uint32_t qw[4] = {q[r][i].x, q[r][i].y, q[r][i].z, q[r][i].w};
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) w[r][m] = __fmaf_rn(f.x, byte_code(qw[m >> 2], m & 3), f.y);
+                }
                 const float4* xs = xw + (size_t)(b0 + i) * 4 * 32 + lane;
 #pragma unroll
                 for (int j = 0; j < TB; ++j) {
@@ -447,22 +461,30 @@ __global__ void __launch_bounds__(kRouterWideWarps * 32, 2) router_wide_kernel(c
 #pragma unroll
                         for (int qq = 0; qq < 4; ++qq) {
                             const float4 xv = xj[qq * 32];
-                            acc[j] = __fmaf_rn(w[4 * qq + 0], xv.x, acc[j]);
-                            acc[j] = __fmaf_rn(w[4 * qq + 1], xv.y, acc[j]);
-                            acc[j] = __fmaf_rn(w[4 * qq + 2], xv.z, acc[j]);
-                            acc[j] = __fmaf_rn(w[4 * qq + 3], xv.w, acc[j]);
+#pragma unroll
+                            for (int r = 0; r < RP; ++r) {
+                                acc[r][j] = __fmaf_rn(w[r][4 * qq + 0], xv.x, acc[r][j]);
+                                acc[r][j] = __fmaf_rn(w[r][4 * qq + 1], xv.y, acc[r][j]);
+                                acc[r][j] = __fmaf_rn(w[r][4 * qq + 2], xv.z, acc[r][j]);
+                                acc[r][j] = __fmaf_rn(w[r][4 * qq + 3], xv.w, acc[r][j]);
+                            }
                         }
                     }
                 }
             }
         }
 #pragma unroll
-        for (int j = 0; j < TB; ++j) {
-            if (j < nt) {
-                float v = acc[j];
+        for (int r = 0; r < RP; ++r) {
+            if (!has[r]) continue;
+            const int e = e0 + r;
 #pragma unroll
-                for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(kFull, v, off));
-                if (lane == 0) p.logits[(size_t)(t0 + j) * p.E + e] = p.zbias ? __fadd_rn(v, p.zbias[e]) : v;
+            for (int j = 0; j < TB; ++j) {
+                if (j < nt) {
+                    float v = acc[r][j];
+#pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1) v = __fadd_rn(v, __shfl_xor_sync(kFull, v, off));
+                    if (lane == 0) p.logits[(size_t)(t0 + j) * p.E + e] = p.zbias ? __fadd_rn(v, p.zbias[e]) : v;
+                }
             }
         }
     }
@@ -478,7 +500,7 @@ cudaError_t launch_router(const RouterParams& p, cudaStream_t s, bool pdl) {
     e = ensure_smem_attr((const void*)router_kernel<1, kRouterWarps, 6>, (size_t)kMaxDModel * 2);
     if (e != cudaSuccess) return e;
     const auto wide_smem = [](int d) { return (size_t)kRouterWideTB * (((d >> 4) + 31) >> 5) * 4 * 32 * 16; };
-    e = ensure_smem_attr((const void*)router_wide_kernel<1>, wide_smem(kRouterWideMaxD));
+    e = ensure_smem_attr((const void*)router_wide_kernel<2>, wide_smem(kRouterWideMaxD));
     if (e == cudaSuccess) e = ensure_smem_attr((const void*)router_wide_kernel<4>, wide_smem(kRouterWideMaxD));
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute la;
@@ -489,12 +511,12 @@ cudaError_t launch_router(const RouterParams& p, cudaStream_t s, bool pdl) {
     }
     if (p.T >= kRouterWideMinT && p.d <= kRouterWideMaxD) {
         // four expert rows a warp once there are enough token blocks to fill the GPU
-        const int R = p.T >= 512 ? 4 : 1;
+        const int R = p.T >= 512 ? 4 : 2;
         const int rows = kRouterWideWarps * R;
         const cudaLaunchConfig_t c =
             launch_config(dim3((p.E + rows - 1) / rows, (p.T + kRouterWideTB - 1) / kRouterWideTB),
                           dim3(kRouterWideWarps * 32), wide_smem(p.d), s, pdl, &la);
-        return R == 4 ? cudaLaunchKernelEx(&c, router_wide_kernel<4>, p) : cudaLaunchKernelEx(&c, router_wide_kernel<1>, p);
+        return R == 4 ? cudaLaunchKernelEx(&c, router_wide_kernel<4>, p) : cudaLaunchKernelEx(&c, router_wide_kernel<2>, p);
     }
     const size_t sm = (size_t)std::min(kRouterTB, p.T) * p.d * 2;
     const cudaLaunchConfig_t c = launch_config(
