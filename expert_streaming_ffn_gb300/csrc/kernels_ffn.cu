@@ -356,6 +356,14 @@ __global__ void __launch_bounds__(Shape<C>::kThreads, 1)
     const int n_units = a.fam[0].n_items * (a.fam[0].inter >> 5) + a.fam[1].n_items * (a.fam[1].inter >> 5);
     const int dn_stages = (tiles_d + kDnTiles - 1) / kDnTiles;
     const int dn_per = (tiles_d + dn_stages - 1) / dn_stages;  // down row tiles per stage
+    // This CTA's units: round robin for one token (every SM streams in the
+    // first wave); for several, a contiguous run, so that consecutive units
+    // share an item and the token rows it staged (measured 12 % faster at 8
+    // tokens, 5 % slower at one)
+    const int per_cta = NT == 1 ? 1 : (n_units + gridDim.x - 1) / gridDim.x;
+    const int u_begin = NT == 1 ? (int)blockIdx.x : (int)blockIdx.x * per_cta;
+    const int u_end = NT == 1 ? n_units : min(n_units, u_begin + per_cta);
+    const int u_step = NT == 1 ? (int)gridDim.x : 1;
 
     unsigned long long* tr = a.trace ? a.trace + (size_t)blockIdx.x * kFfnTracePoints : nullptr;
     if (a.span && threadIdx.x == 0) atomicMin(a.span, (unsigned long long)ptx::globaltimer());
@@ -404,7 +412,7 @@ __global__ void __launch_bounds__(Shape<C>::kThreads, 1)
                     phase ^= 1;
                 }
             };
-            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            for (int u = u_begin; u < u_end && ok; u += u_step) {
                 const Unit un = unit_of(a, u);
                 const FfnItem& it = list.item[un.item];
                 if (!it.w) ptx::pdl_wait();  // the router's ids (a no-op once passed)
@@ -513,7 +521,7 @@ __global__ void __launch_bounds__(Shape<C>::kThreads, 1)
         }
     };
     bool first_unit = true;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+    for (int u = u_begin; u < u_end; u += u_step) {
         const Unit un = unit_of(a, u);
         const FfnItem& it = list.item[un.item];
         if (!it.w) {
