@@ -77,7 +77,7 @@ template <int A, int B, int R, bool D>
 struct PfRings {
     static constexpr int kStages = A, kSlotsB = B, kRawStages = R;
     // routed token rows padded to a power of two and loaded one 3-D box per B
-    // slot (else padded to a multiple of 16, 2-D boxes of 16 rows)
+    // slot (else padded to a multiple of 16, 2-D boxes of 16, 64 or 128 rows)
     static constexpr bool kRows3d = D;
     static constexpr int kStageShift = A == 8 ? 3 : A == 4 ? 2 : A == 2 ? 1 : 0;
     static constexpr int kSlotShift = B == 8 ? 3 : B == 4 ? 2 : B == 2 ? 1 : 0;
@@ -146,9 +146,9 @@ __device__ __forceinline__ float act_fn(float z, int act) {
 // `part` of the tile's ks[fam] parts.
 // The routed experts' token rows. Maps 0-3 see them as [K-block][row][64]
 // and load boxes of 16 << i rows by min(8 >> i, K-blocks) K-blocks, a whole B
-// slot at once; map 4 loads 2-D boxes of 16 rows by one K-block.
+// slot at once; maps 4-6 load 2-D boxes of 16, 64 and 128 rows by one K-block.
 struct PfRowMaps {
-    CUtensorMap r[5];
+    CUtensorMap r[7];
 };
 
 struct Job {
@@ -420,7 +420,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     unsigned char* bt = ringB + s * kBBytes;
-                    if (b.fam == 1 && !kRows3d) {
+                    if (b.fam == 1 && !kRows3d && (nb == 128 || nb == 64)) {
+                        // a routed expert of 64 or 128 rows: one box per K-block
+                        // (a box load costs its issuing thread ~100 ns)
+                        const CUtensorMap* m = &rmaps.r[nb == 128 ? 6 : 5];
+                        ptx::mbar_arrive_expect_tx(b_full + s, (uint32_t)(nk * nb * 128));
+                        for (int kk = 0; kk < nk; ++kk)
+                            ptx::tma_load_2d(bt + kk * nb * 128, m, (b.kb0 + kb0 + kk) * 64, it.pb, b_full + s);
+                    } else if (b.fam == 1 && !kRows3d) {
                         // a routed expert: 16-row boxes, one K-block each
                         ptx::mbar_arrive_expect_tx(b_full + s, (uint32_t)(nk * nb * 128));
                         for (int kk = 0; kk < nk; ++kk)
@@ -908,7 +915,8 @@ cudaError_t launch_pf_gemm(const PfArgs& a, int phase, const void* b0, const voi
         for (int q = 0; q < 4 && e == cudaSuccess; ++q)
             e = encode_rows3(&rm.r[q], b1, std::max(rows[1], 1), k1, 16 << q, std::min(8 >> q, k1 / 64));
     else if (e == cudaSuccess)
-        e = encode_rows(&rm.r[4], b1, std::max(rows[1], 1), k1, 16);
+        for (int q = 4; q < 7 && e == cudaSuccess; ++q)
+            e = encode_rows(&rm.r[q], b1, std::max(rows[1], 1), k1, q == 4 ? 16 : q == 5 ? 64 : 128);
     if (e == cudaSuccess)
         e = chunk ? ensure_smem_attr((const void*)pf_gemm_kernel<RingsChunk>, RingsChunk::kSmemBytes)
                   : ensure_smem_attr((const void*)pf_gemm_kernel<RingsPrompt>, RingsPrompt::kSmemBytes);
